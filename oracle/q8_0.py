@@ -12,7 +12,9 @@ bit for bit):
     amax = max_i |x_i|                 exact
     d    = amax / 127                  float32 division, correctly rounded
     q_i  = round(x_i / d)              float32 division, then round half away
-                                       from zero; all codes 0 when amax == 0
+                                       from zero; all codes 0 when d == 0
+                                       (amax == 0, or amax so small that
+                                       amax/127 underflows: x/d is undefined)
     d_h  = fp16(d)                     round to nearest even, subnormals kept
 Dequantisation: xhat_i = float(d_h) * q_i, exact in float32 (11 x 8 bits).
 The f16 cache stores fp16(x) with round to nearest even.
@@ -37,7 +39,7 @@ def quantize_blocks(x):
     xb = x.reshape(shape[:-1] + (shape[-1] // BLOCK, BLOCK))
     amax = np.abs(xb).max(axis=-1)
     d = amax / np.float32(127.0)                      # float32 / float32 -> float32
-    nonzero = amax > 0
+    nonzero = d > 0
     divisor = np.where(nonzero, d, np.float32(1.0)).astype(np.float32)
     ratio = xb / divisor[..., None]                   # float32 division, correctly rounded
     r = ratio.astype(np.float64)                      # exact widening; |r| + 0.5 is exact too

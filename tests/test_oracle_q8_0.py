@@ -110,6 +110,16 @@ def test_f16_rounding_hand_values():
     assert f16_bits(q8_0.to_f16(vals)).tolist() == bits
 
 
+def test_underflowing_scale_codes_zero():
+    # amax = 2^-140: amax/127 underflows to float32 zero, x/d is undefined, the block codes to zeros
+    x = np.zeros(32, np.float32)
+    x[0] = np.float32(2.0 ** -140)
+    x[1] = -np.float32(2.0 ** -141)
+    assert float(np.float32(2.0 ** -140) / np.float32(127)) == 0.0
+    d_h, q = q8_0.quantize_blocks(x)
+    assert (q == 0).all() and int(f16_bits(d_h)[0]) == 0
+
+
 def test_rejects_non_finite():
     x = np.zeros(32, np.float32)
     x[3] = np.inf
