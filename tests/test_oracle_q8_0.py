@@ -111,11 +111,11 @@ def test_f16_rounding_hand_values():
 
 
 def test_underflowing_scale_codes_zero():
-    # amax = 2^-140: amax/127 underflows to float32 zero, x/d is undefined, the block codes to zeros
+    # amax = 2^-144 = 32 * 2^-149: amax/127 rounds to float32 zero, x/d is undefined, the block codes to zeros
     x = np.zeros(32, np.float32)
-    x[0] = np.float32(2.0 ** -140)
-    x[1] = -np.float32(2.0 ** -141)
-    assert float(np.float32(2.0 ** -140) / np.float32(127)) == 0.0
+    x[0] = np.float32(2.0 ** -144)
+    x[1] = -np.float32(2.0 ** -145)
+    assert float(np.float32(2.0 ** -144) / np.float32(127)) == 0.0
     d_h, q = q8_0.quantize_blocks(x)
     assert (q == 0).all() and int(f16_bits(d_h)[0]) == 0
 
