@@ -1,0 +1,507 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention-over-KV-cache hot path on GB300.
+
+One step = one request on every layer of the workload: the prompt prefilled in
+chunks (kv_cache_append + prefill_chunk_attn per chunk), the decode steps
+(kv_cache_append + decode_attn per token, the loop captured once in a CUDA
+graph), then the cache state serialised from the head-major cache
+(kv_state_get) and restored into a layer-major cache (kv_state_set).
+
+`value` is the whole request's throughput per attention layer: (prompt +
+generated tokens) x layers / step time, summed over ranks.  The phases are
+reported beside it (prefill tok/s, decode tok/s, state GB/s).  The roofline
+object is for the dominant kernel, the prefill attention, whose algorithmic
+work per chunk is 4 * H_q * D * sum_t (t + 1) flops (causal half only).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       python bench.py --impl reference ...   (the CPU oracle, bounded sample)
+Multi-GPU (torchrun): every rank runs an independent replica (weak scaling).
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "prefill tok/s and decode tok/s per attention layer; % tensor/HBM roofline"
+DEFAULT_WORKLOAD = "f16_17k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(w, chunks=None):
+    """Algorithmic flops of prefill attention: 4*H_q*D*(t+1) per query row t (QK^T and PV, causal)."""
+    out = []
+    for p, c in (chunks or w.chunks()):
+        rows = c * p + c * (c + 1) // 2
+        out.append(4.0 * w.n_head_q * w.head_dim * rows)
+    return out
+
+
+def cache_bytes_per_token(w):
+    if w.cache == "q8_0":
+        return 2 * w.n_head_kv * w.head_dim * 34 // 32
+    return 2 * w.n_head_kv * w.head_dim * 2
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": float(np.median(busy)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- GPU arm
+class GpuRequest:
+    """Inputs resident in HBM (and pinned host copies for the end-to-end run), two caches, output buffers."""
+
+    def __init__(self, kvc, w, device, seed_offset):
+        import torch
+        self.torch, self.kvc, self.w, self.dev = torch, kvc, w, device
+        wl = w if seed_offset == 0 else si.Workload(**{**w.__dict__, "seed": w.seed + 1000 * seed_offset})
+        self.wl = wl
+        self.host, self.dev_in = [], []
+        for layer in range(w.n_layer):
+            q, k, v = si.layer_qkv(wl, layer)
+            hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+            self.host.append((hq, hk, hv))
+            self.dev_in.append(tuple(t.to(device) for t in (hq, hk, hv)))
+        self.src = kvc.KVCache(w.n_layer, w.n_ctx, w.n_head_kv, w.head_dim, w.cache, "head_major", device)
+        self.dst = kvc.KVCache(w.n_layer, w.n_ctx, w.n_head_kv, w.head_dim, w.cache, "layer_major", device)
+        self.out_p = torch.empty(w.n_layer, w.n_prompt, w.n_head_q, w.head_dim, device=device)
+        self.out_d = torch.empty(w.n_layer, max(w.n_decode, 1), w.n_head_q, w.head_dim, device=device)
+        self.scratch = torch.empty(self.src.scratch_bytes(w.n_head_q), dtype=torch.uint8, device=device)
+        self.state = torch.empty(self.src.state_size(w.n_tokens), dtype=torch.uint8, device=device)
+        self.host_out_p = torch.empty(self.out_p.shape, dtype=torch.float32).pin_memory()
+        self.host_out_d = torch.empty(self.out_d.shape, dtype=torch.float32).pin_memory()
+        self.host_state = torch.empty(self.state.shape, dtype=torch.uint8).pin_memory()
+        self.chunks = w.chunks()
+        self.graphs = []
+        self.flops = prefill_flops(w)
+
+    def launches_per_step(self):
+        w = self.w
+        return w.n_layer * (2 * len(self.chunks) + 3 * w.n_decode) + 3
+
+    def _decode_loop(self, layer):
+        kvc, w = self.kvc, self.w
+        q, k, v = self.dev_in[layer]
+        for i in range(w.n_decode):
+            pos = w.n_prompt + i
+            kvc.kv_cache_append(self.src, layer, pos, k[pos:pos + 1], v[pos:pos + 1])
+            kvc.decode_attn(self.src, layer, pos, q[pos], out=self.out_d[layer, i], scratch=self.scratch)
+
+    def capture(self):
+        """Capture each layer's decode loop in a CUDA graph (after one eager run)."""
+        torch = self.torch
+        for layer in range(self.w.n_layer):
+            self._decode_loop(layer)
+        torch.cuda.synchronize()
+        self.graphs = []
+        for layer in range(self.w.n_layer):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._decode_loop(layer)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def step(self, ev=None):
+        """One request on every layer.  ev: dict of event lists to record phase/launch times."""
+        kvc, w, torch = self.kvc, self.w, self.torch
+        E = torch.cuda.Event
+        for layer in range(w.n_layer):
+            q, k, v = self.dev_in[layer]
+            if ev is not None:
+                e0 = E(enable_timing=True); e0.record(); ev["prefill"].append([e0])
+            for ci, (p, c) in enumerate(self.chunks):
+                kvc.kv_cache_append(self.src, layer, p, k[p:p + c], v[p:p + c])
+                if ev is not None:
+                    a = E(enable_timing=True); a.record()
+                kvc.prefill_chunk_attn(self.src, layer, p, q[p:p + c], out=self.out_p[layer, p:p + c])
+                if ev is not None:
+                    b = E(enable_timing=True); b.record(); ev["attn"].append((a, b, self.flops[ci]))
+            if ev is not None:
+                e1 = E(enable_timing=True); e1.record(); ev["prefill"][-1].append(e1)
+            if w.n_decode:
+                if self.graphs:
+                    self.graphs[layer].replay()
+                else:
+                    self._decode_loop(layer)
+            if ev is not None:
+                e2 = E(enable_timing=True); e2.record(); ev["decode"].append((e1, e2))
+        if ev is not None:
+            e3 = E(enable_timing=True); e3.record()
+        kvc.kv_state_get(self.src, w.n_tokens, dst=self.state)
+        n = kvc.kv_state_set(self.dst, self.state)
+        assert n == w.n_tokens
+        if ev is not None:
+            e4 = E(enable_timing=True); e4.record(); ev["state"].append((e3, e4))
+
+    def h2d(self):
+        for (hq, hk, hv), (dq, dk, dv) in zip(self.host, self.dev_in):
+            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+
+    def d2h(self):
+        self.host_out_p.copy_(self.out_p, non_blocking=True)
+        self.host_out_d.copy_(self.out_d, non_blocking=True)
+        self.host_state.copy_(self.state, non_blocking=True)
+
+    def io_bytes(self):
+        h2d = sum(t.numel() * t.element_size() for trip in self.host for t in trip)
+        d2h = sum(t.numel() * t.element_size() for t in (self.host_out_p, self.host_out_d, self.host_state))
+        return h2d, d2h
+
+
+def l2_flush(torch, buf):
+    buf.add_(1)
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import decode_attention_kv_cache_gb300 as kvc
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = si.WORKLOADS[args.workload]
+    req = GpuRequest(kvc, w, device, seed_offset=rank)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MiB > 129 MB L2
+    req.step()
+    if w.n_decode:
+        req.capture()
+    for _ in range(args.warmup):
+        l2_flush(torch, flush)
+        req.step()
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+
+    # ---- timed region: K steps, L2 flushed before each (outside the step's events)
+    ev = {"prefill": [], "attn": [], "decode": [], "state": []}
+    steps = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        l2_flush(torch, flush)
+        s0 = torch.cuda.Event(enable_timing=True); s0.record()
+        req.step(ev)
+        s1 = torch.cuda.Event(enable_timing=True); s1.record()
+        steps.append((s0, s1))
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in steps]
+    total_ms = dist_max(sum(step_ms), world)
+    attn_ms = sum(a.elapsed_time(b) for a, b, _ in ev["attn"])
+    attn_flops = sum(f for _, _, f in ev["attn"])
+    n_attn = len(ev["attn"])
+    prefill_ms = sum(x[0].elapsed_time(x[1]) for x in ev["prefill"])
+    decode_ms = sum(a.elapsed_time(b) for a, b in ev["decode"])
+    state_ms = sum(a.elapsed_time(b) for a, b in ev["state"])
+    K = args.steps
+    tokens = (w.n_prompt + w.n_decode) * w.n_layer
+    value = tokens * world * K / (total_ms / 1e3)
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(2):
+            req.h2d(); req.step(); req.d2h()
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        e_ms = []
+        for _ in range(K):
+            l2_flush(torch, flush)
+            a = torch.cuda.Event(enable_timing=True); a.record()
+            req.h2d(); req.step(); req.d2h()
+            b = torch.cuda.Event(enable_timing=True); b.record()
+            b.synchronize()
+            e_ms.append(a.elapsed_time(b))
+        e_total = dist_max(sum(e_ms), world)
+        h2d, d2h = req.io_bytes()
+        e2e = {"value": tokens * world * K / (e_total / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_total / K}
+    assert kvc.kvc_device_status() == 0
+
+    peaks, peak_src = load_peaks()
+    achieved = attn_flops / (attn_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roof = {"kernel": "prefill_chunk_attn (tcgen05 f16 x f16 -> f32)", "bound": "tensor",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": "%s dense bf16 burst (f16 runs at the bf16 rate)" % peak_src,
+            "traffic": None, "launches": n_attn // K, "avg_launch_ms": attn_ms / n_attn,
+            "algorithmic_flops_per_step": attn_flops / K}
+    bt = cache_bytes_per_token(w)
+    dec_bytes = sum(w.n_layer * ((w.n_prompt + i + 1) * bt + w.n_head_q * w.head_dim * (2 + 4)
+                                 + 2 * w.n_head_kv * w.head_dim * 2 + bt) for i in range(w.n_decode))
+    state_bytes = 2 * 2 * req.state.numel()
+    phases = {
+        "prefill_tok_s": w.n_prompt * w.n_layer * K / (prefill_ms / 1e3),
+        "prefill_ms_per_step": prefill_ms / K,
+        "prefill_attn_ms_per_step": attn_ms / K,
+        "decode_tok_s": (w.n_decode * w.n_layer * K / (decode_ms / 1e3)) if w.n_decode else None,
+        "decode_ms_per_step": decode_ms / K,
+        "decode_algorithmic_GB_s": (dec_bytes * K / (decode_ms / 1e3) / 1e9) if w.n_decode else None,
+        "state_ms_per_step": state_ms / K,
+        "state_algorithmic_GB_s": state_bytes * K / (state_ms / 1e3) / 1e9,
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xf16->f32 (tensor), f32 softmax; int8/f16 cache", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": w.name, "n_layer": w.n_layer, "n_head_q": w.n_head_q, "n_head_kv": w.n_head_kv,
+                   "head_dim": w.head_dim, "cache": w.cache, "in_dtype": w.in_dtype, "n_ctx": w.n_ctx,
+                   "n_prompt": w.n_prompt, "chunk": w.chunk, "n_decode": w.n_decode,
+                   "parallelism": "replicas (one independent layer stack per GPU)",
+                   "l2": "flushed (256 MiB write) before each timed step", "decode_loop": "CUDA graph"},
+        "phases": phases, "roofline": roof, "e2e": e2e, "gpu_launches": req.launches_per_step() * K,
+        "clocks": clk,
+    }
+    return line
+
+
+# --------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
+def oracle_sample(w, max_chunks=6, rows_per_chunk=4, decode_samples=3):
+    """Time the oracle on a bounded sample of one layer's request; extrapolate to the whole request.
+
+    Appends (quantisation) of every token and the state pack/unpack are timed
+    whole.  Prefill: for up to `max_chunks` evenly spaced chunks, the cache
+    dequantisation (scaled by cache length) and the attention of
+    `rows_per_chunk` rows (scaled by the causal row work sum (t+1)).  Decode:
+    `decode_samples` steps, scaled by sum (pos+1).
+    """
+    from oracle import state as ostate
+    from oracle.attention import attend
+    from oracle.cache import OracleCache
+
+    q, k, v = si.layer_qkv(w, 0)
+    qf, kf, vf = (t.float().numpy() for t in (q, k, v))
+    o = OracleCache(1, w.n_ctx, w.n_head_kv, w.head_dim, w.cache)
+    chunks = w.chunks()
+    t0 = time.perf_counter()
+    for p, c in chunks:
+        o.append(0, p, kf[p:p + c], vf[p:p + c])
+    for p in range(w.n_prompt, w.n_tokens):
+        o.append(0, p, kf[p:p + 1], vf[p:p + 1])
+    t_append = time.perf_counter() - t0
+    pick = sorted(set(np.linspace(0, len(chunks) - 1, min(max_chunks, len(chunks))).round().astype(int).tolist()))
+    rng = np.random.default_rng(w.seed)
+    t_deq = t_att = 0.0
+    deq_units = att_units = 0.0
+    for ci in pick:
+        p, c = chunks[ci]
+        t1 = time.perf_counter()
+        kh, vh = o.dequantized(0, p + c)
+        t2 = time.perf_counter()
+        rows = np.unique(np.concatenate([[0, c - 1], rng.choice(c, size=min(rows_per_chunk, c), replace=False)]))
+        attend(qf[p + rows], p + rows, kh, vh)
+        t3 = time.perf_counter()
+        t_deq += t2 - t1
+        t_att += t3 - t2
+        deq_units += p + c
+        att_units += float(np.sum(p + rows + 1))
+    full_deq_units = float(sum(p + c for p, c in chunks))
+    full_att_units = float(w.n_prompt) * (w.n_prompt + 1) / 2
+    t_prefill = t_deq * full_deq_units / deq_units + t_att * full_att_units / att_units
+    t_decode = 0.0
+    if w.n_decode:
+        steps = sorted(set(np.linspace(0, w.n_decode - 1, min(decode_samples, w.n_decode)).round().astype(int)))
+        t4 = time.perf_counter()
+        units = 0.0
+        for i in steps:
+            pos = w.n_prompt + i
+            o.decode(0, pos, qf[pos])
+            units += pos + 1
+        full = float(sum(w.n_prompt + i + 1 for i in range(w.n_decode)))
+        t_decode = (time.perf_counter() - t4) * full / units
+    t5 = time.perf_counter()
+    blob = ostate.pack(o, w.n_tokens)
+    o2 = OracleCache(1, w.n_ctx, w.n_head_kv, w.head_dim, w.cache)
+    ostate.unpack(blob, o2)
+    t_state = time.perf_counter() - t5
+    total = t_append + t_prefill + t_decode + t_state
+    return {"value": (w.n_prompt + w.n_decode) / total, "seconds_extrapolated": total,
+            "seconds_measured": time.perf_counter() - t0,
+            "parts_s": {"append": t_append, "prefill": t_prefill, "decode": t_decode, "state": t_state},
+            "sample": "one layer; appends and state whole; prefill: %d of %d chunks, %d rows each, "
+                      "dequantisation scaled by cache length, attention by causal row work; decode: %d of %d "
+                      "steps scaled by key count" % (len(pick), len(chunks), rows_per_chunk + 2,
+                                                     min(decode_samples, w.n_decode), w.n_decode)}
+
+
+def cpu_baseline(workload):
+    """The oracle in a child process restricted to one thread (so `cores` is exact)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    env.pop("WORLD_SIZE", None)
+    env.pop("RANK", None)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", workload],
+                       capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["value"], "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": d["sample"],
+            "seconds_measured": d["seconds_measured"], "parts_s": d["parts_s"]}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, timed on this host's cores on a bounded sample per step."""
+    if rank != 0:
+        return None
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(k, "1")
+    w = si.WORKLOADS[args.workload]
+    small = dict(max_chunks=2, rows_per_chunk=2, decode_samples=1)
+    for _ in range(args.warmup):
+        oracle_sample(w, **small)
+    vals, secs = [], []
+    samp = None
+    for _ in range(args.steps):
+        d = oracle_sample(w, **small)
+        vals.append(d["value"])
+        secs.append(d["seconds_extrapolated"])
+        samp = d["sample"]
+    value = float(np.mean(vals))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": w.name, "n_layer": 1, "n_prompt": w.n_prompt, "n_decode": w.n_decode},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": samp},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+
+    if args.oracle_child:
+        print(json.dumps(oracle_sample(si.WORKLOADS[args.workload])))
+        return
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_gpu(args, rank, world, local)
+    if rank == 0:
+        w = si.WORKLOADS[args.workload]
+        if w.n_layer == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+"""Python binding of libkvc: attention over a device-resident q8_0/f16 KV cache on GB300.
+
+Argument marshalling only.  Every step of the path (quantise-and-append,
+chunked prefill attention, split-K decode attention, state pack/unpack) runs in
+the library's CUDA kernels; torch supplies device memory and the current
+stream.  The functions carry the names of the C ABI in include/kvc.h.
+
+There is no fallback: importing this package fails if libkvc.so has not been
+built (python -m decode_attention_kv_cache_gb300.build), and every call raises
+KvcError when the library reports an error.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+KVC_OK, KVC_EINVAL, KVC_ERANGE, KVC_ENOSPC, KVC_EFORMAT, KVC_ECUDA, KVC_EDEVICE = 0, -1, -2, -3, -4, -5, -6
+CACHE_TYPES = {"f16": 0, "q8_0": 1}
+LAYOUTS = {"head_major": 0, "layer_major": 1}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+
+class KvcError(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__("%s: %s (%d)" % (what, lib.kvc_strerror(status).decode(), status))
+        self.status = status
+
+
+class kvc_desc(ctypes.Structure):
+    _fields_ = [("n_layer", ctypes.c_int32), ("n_ctx", ctypes.c_int32), ("n_head_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("type", ctypes.c_int32), ("layout", ctypes.c_int32)]
+
+
+class kvc_cache(ctypes.Structure):
+    _fields_ = [("d", kvc_desc), ("k_q", ctypes.c_void_p), ("k_s", ctypes.c_void_p),
+                ("v_q", ctypes.c_void_p), ("v_s", ctypes.c_void_p)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libkvc.so is not built; run `python -m decode_attention_kv_cache_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I32, SZ, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+    sig = {
+        "kvc_cache_bytes": (ctypes.c_int, [P(kvc_desc), P(SZ), P(SZ), P(SZ), P(SZ)]),
+        "kvc_scratch_bytes": (ctypes.c_int, [P(kvc_desc), I32, P(SZ)]),
+        "kv_state_size": (SZ, [P(kvc_desc), I32]),
+        "kvc_cache_init": (ctypes.c_int, [P(kvc_cache), P(kvc_desc), VP, VP, VP, VP]),
+        "kv_cache_append": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, VP, I32, VP]),
+        "prefill_chunk_attn": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, I32, I32, VP, VP]),
+        "decode_attn": (ctypes.c_int, [P(kvc_cache), I32, I32, VP, I32, I32, VP, VP, SZ, VP]),
+        "kv_state_get": (ctypes.c_int, [P(kvc_cache), I32, VP, SZ, VP]),
+        "kv_state_set": (ctypes.c_int, [P(kvc_cache), VP, SZ, P(I32), VP]),
+        "kvc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "kvc_device_status": (ctypes.c_int, [P(I32)]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    return L
+
+
+lib = _load()
+
+
+def _check(status, what):
+    if status != KVC_OK:
+        raise KvcError(status, what)
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, what, dtype=None):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % what)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s" % (what, dtype))
+
+
+def make_desc(n_layer, n_ctx, n_head_kv, head_dim, cache_type="q8_0", layout="head_major"):
+    return kvc_desc(n_layer, n_ctx, n_head_kv, head_dim, CACHE_TYPES[cache_type], LAYOUTS[layout])
+
+
+def cache_bytes(desc):
+    s = [ctypes.c_size_t() for _ in range(4)]
+    _check(lib.kvc_cache_bytes(ctypes.byref(desc), *[ctypes.byref(x) for x in s]), "kvc_cache_bytes")
+    return tuple(x.value for x in s)
+
+
+class KVCache:
+    """A cache whose four buffers are torch allocations on `device`.
+
+    Codes/values: k_q, v_q; scales (q8_0 only): k_s, v_s.  The buffers are
+    exposed as typed views in the layout of the descriptor.
+    """
+
+    def __init__(self, n_layer, n_ctx, n_head_kv, head_dim, cache_type="q8_0", layout="head_major",
+                 device="cuda"):
+        self.desc = make_desc(n_layer, n_ctx, n_head_kv, head_dim, cache_type, layout)
+        self.n_layer, self.n_ctx, self.n_head_kv, self.head_dim = n_layer, n_ctx, n_head_kv, head_dim
+        self.cache_type, self.layout = cache_type, layout
+        self.device = torch.device(device)
+        kq, ks, vq, vs = cache_bytes(self.desc)
+        self._bufs = [torch.empty(max(n, 16), dtype=torch.uint8, device=self.device) for n in (kq, ks, vq, vs)]
+        self._sizes = (kq, ks, vq, vs)
+        self.c = kvc_cache()
+        scales = cache_type == "q8_0"
+        _check(lib.kvc_cache_init(ctypes.byref(self.c), ctypes.byref(self.desc), _ptr(self._bufs[0]),
+                                  _ptr(self._bufs[1]) if scales else ctypes.c_void_p(0), _ptr(self._bufs[2]),
+                                  _ptr(self._bufs[3]) if scales else ctypes.c_void_p(0)), "kvc_cache_init")
+
+    def _shape(self, last):
+        if self.layout == "head_major":
+            return (self.n_head_kv, self.n_layer, self.n_ctx, last)
+        return (self.n_layer, self.n_ctx, self.n_head_kv, last)
+
+    def codes(self, kv):
+        """K (kv=0) or V (kv=1) codes (int8) or values (float16), in layout order."""
+        b = self._bufs[2 * kv][: self._sizes[2 * kv]]
+        dt = torch.int8 if self.cache_type == "q8_0" else torch.float16
+        return b.view(dt).view(self._shape(self.head_dim))
+
+    def scales(self, kv):
+        if self.cache_type != "q8_0":
+            return None
+        b = self._bufs[2 * kv + 1][: self._sizes[2 * kv + 1]]
+        return b.view(torch.float16).view(self._shape(self.head_dim // 32))
+
+    def scratch_bytes(self, n_head_q):
+        n = ctypes.c_size_t()
+        _check(lib.kvc_scratch_bytes(ctypes.byref(self.desc), n_head_q, ctypes.byref(n)), "kvc_scratch_bytes")
+        return n.value
+
+    def state_size(self, n_tokens):
+        return lib.kv_state_size(ctypes.byref(self.desc), n_tokens)
+
+
+def kv_cache_append(cache, layer, pos0, k, v, stream=None):
+    """Quantise/round and store K, V [n, H_kv, D] at positions [pos0, pos0 + n) of `layer`."""
+    _need(k, "k"); _need(v, "v", k.dtype)
+    st = lib.kv_cache_append(ctypes.byref(cache.c), layer, pos0, k.shape[0], _ptr(k), _ptr(v), DTYPES[k.dtype],
+                             _stream(stream, k.device))
+    _check(st, "kv_cache_append")
+
+
+def prefill_chunk_attn(cache, layer, pos0, q, out=None, stream=None):
+    """Causal attention of chunk rows q [C, H_q, D] at positions [pos0, pos0 + C); returns out [C, H_q, D] f32."""
+    _need(q, "q")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    st = lib.prefill_chunk_attn(ctypes.byref(cache.c), layer, pos0, q.shape[0], _ptr(q), DTYPES[q.dtype],
+                                q.shape[1], _ptr(out), _stream(stream, q.device))
+    _check(st, "prefill_chunk_attn")
+    return out
+
+
+def decode_attn(cache, layer, pos, q, out=None, scratch=None, stream=None):
+    """Attention of one query token q [H_q, D] at position pos; returns out [H_q, D] f32."""
+    _need(q, "q")
+    n_head_q = q.shape[0]
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if scratch is None:
+        scratch = torch.empty(cache.scratch_bytes(n_head_q), dtype=torch.uint8, device=q.device)
+    _need(out, "out", torch.float32); _need(scratch, "scratch")
+    st = lib.decode_attn(ctypes.byref(cache.c), layer, pos, _ptr(q), DTYPES[q.dtype], n_head_q, _ptr(out),
+                         _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream, q.device))
+    _check(st, "decode_attn")
+    return out
+
+
+def kv_state_get(cache, n_tokens, dst=None, stream=None):
+    """Serialise positions [0, n_tokens) into dst (uint8 CUDA tensor); returns dst."""
+    n = cache.state_size(n_tokens)
+    if dst is None:
+        dst = torch.empty(max(n, 16), dtype=torch.uint8, device=cache.device)
+    _need(dst, "dst")
+    st = lib.kv_state_get(ctypes.byref(cache.c), n_tokens, _ptr(dst), dst.numel() * dst.element_size(),
+                          _stream(stream, cache.device))
+    _check(st, "kv_state_get")
+    return dst[:n]
+
+
+def kv_state_set(cache, src, stream=None):
+    """Restore a state (uint8 CUDA tensor of exactly the state's size); returns n_tokens."""
+    _need(src, "src")
+    n = ctypes.c_int32(-1)
+    st = lib.kv_state_set(ctypes.byref(cache.c), _ptr(src), src.numel() * src.element_size(), ctypes.byref(n),
+                          _stream(stream, cache.device))
+    _check(st, "kv_state_set")
+    return n.value
+
+
+def kvc_device_status():
+    """Synchronise and read/clear the device status word (non-zero: a kernel gave up a bounded wait)."""
+    s = ctypes.c_int32(0)
+    _check(lib.kvc_device_status(ctypes.byref(s)), "kvc_device_status")
+    return s.value

@@ -1,0 +1,48 @@
+// Internal declarations shared by the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+// Element strides of one cache buffer family.  Element (layer, pos, head, i)
+// of the codes sits at layer*c_layer + pos*c_tok + head*c_head + i; the scale
+// of block b at layer*s_layer + pos*s_tok + head*s_head + b.
+struct Geom {
+    int64_t c_layer, c_tok, c_head;
+    int64_t s_layer, s_tok, s_head;
+};
+
+inline Geom geom_of(const kvc_desc &d) {
+    const int64_t D = d.head_dim, nb = d.head_dim / 32, H = d.n_head_kv, L = d.n_layer, T = d.n_ctx;
+    Geom g;
+    if (d.layout == KVC_HEAD_MAJOR) {
+        g.c_head = L * T * D; g.c_layer = T * D; g.c_tok = D;
+        g.s_head = L * T * nb; g.s_layer = T * nb; g.s_tok = nb;
+    } else {
+        g.c_layer = T * H * D; g.c_tok = H * D; g.c_head = D;
+        g.s_layer = T * H * nb; g.s_tok = H * nb; g.s_head = nb;
+    }
+    return g;
+}
+
+inline int dtype_bytes(int dtype) { return dtype == KVC_IN_F32 ? 4 : 2; }
+
+// Launchers: arguments are already validated; return KVC_OK or KVC_ECUDA.
+int launch_append(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *k,
+                  const void *v, int dtype, cudaStream_t s);
+int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, int dtype,
+                   int n_head_q, float *out, cudaStream_t s);
+int decode_max_split();
+int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
+                  float *out, float *scratch, cudaStream_t s);
+int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream_t s);
+int launch_state_unpack(const kvc_cache &c, int n_tokens, const uint8_t *src, cudaStream_t s);
+
+// Device status word set by kernels that give up a bounded wait.
+int read_and_clear_device_status(int32_t *status);
+
+}  // namespace kvc

@@ -1,0 +1,187 @@
+/*
+ * kvc.h - C ABI of libkvc: one transformer attention layer's hot path over a
+ * device-resident KV cache on NVIDIA GB300 (sm_103a).
+ *
+ * The path, as the source pages describe it:
+ *   - a prompt is processed in ubatches ("chunks") of C tokens against the
+ *     growing KV cache, then generation decodes one token at a time
+ *     (llama.cpp PR #58 "completion : allow the prompt to be processed under
+ *     its own split mode", section "Why"; llama.cpp PR #17 "--split-overlap",
+ *     section "How"; strata #1441 "Prompt chunks sized for a layer split's
+ *     pipeline", section "Summary");
+ *   - the cache is device-resident and stored as q8_0 or f16 (PR #58,
+ *     section "Why"; llama.cpp PR #59 "llama : switch the split mode of a live
+ *     context", section "Why");
+ *   - the cache state is serialised in a layout-independent form that restores
+ *     byte-identical into a cache split by layer or by head (PR #58, section
+ *     "What this does"; PR #59, section "What this adds", step 1).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise.  The
+ *     caller allocates and owns every buffer (cache, inputs, outputs, scratch,
+ *     state) and the stream; the library allocates no device memory.
+ *   - Work is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Only kv_state_set synchronises (once, to read the
+ *     32-byte header before anything is written).
+ *   - Q, K, V and the outputs are token-major and contiguous:
+ *       q   [n_tokens][n_head_q ][head_dim]   in kvc_dtype
+ *       k,v [n_tokens][n_head_kv][head_dim]   in kvc_dtype
+ *       out [n_tokens][n_head_q ][head_dim]   float32
+ *   - Every argument is checked before anything is launched.  A call that
+ *     returns an error has launched nothing and written nothing: the cache
+ *     stays as it was and usable (the pages' rule that a failure must leave a
+ *     working context, PR #58 section "Memory"; PR #59 section "What this
+ *     adds").  Errors of asynchronous work surface at the caller's next
+ *     synchronisation; the kernels contain no unbounded waits.
+ *
+ * Cache contents.  A cache holds n_layer layers of n_ctx positions of
+ * n_head_kv heads of head_dim values, for K and for V.  Cache types:
+ *   KVC_Q8_0: blocks of 32 consecutive values along head_dim; each block has
+ *             one fp16 scale d = fp16(amax/127) and 32 int8 codes
+ *             q = round(x / (amax/127)) (float32 division, ties away from zero),
+ *             all codes and d zero for an all-zero block.  The stored value is
+ *             d * q.  Codes and scales live in separate arrays.
+ *   KVC_F16:  fp16(x), round to nearest even.  The scale arrays are unused.
+ * Layouts (element offsets; nb = head_dim/32; codes use head_dim, scales nb):
+ *   KVC_HEAD_MAJOR  [n_head_kv][n_layer][n_ctx][head_dim]   (split by head)
+ *   KVC_LAYER_MAJOR [n_layer][n_ctx][n_head_kv][head_dim]   (split by layer)
+ *
+ * Supported shapes: head_dim a multiple of 32 for append and state calls;
+ * head_dim 64 or 128 for the attention calls; n_head_q a multiple of
+ * n_head_kv; n_head_q / n_head_kv <= 16 for decode_attn.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kvc_stream_t; /* a cudaStream_t */
+
+/* Status codes: 0 on success, negative on error. */
+#define KVC_OK       0
+#define KVC_EINVAL  -1 /* null pointer, unsupported shape, dtype or type, bad alignment */
+#define KVC_ERANGE  -2 /* layer or positions outside the cache */
+#define KVC_ENOSPC  -3 /* a destination or scratch buffer is too small */
+#define KVC_EFORMAT -4 /* a state stream that does not match its header or the cache */
+#define KVC_ECUDA   -5 /* a CUDA call or launch failed */
+#define KVC_EDEVICE -6 /* a kernel gave up a bounded wait (see kvc_device_status) */
+
+typedef enum { KVC_F16 = 0, KVC_Q8_0 = 1 } kvc_cache_type;
+typedef enum { KVC_IN_F32 = 0, KVC_IN_BF16 = 1, KVC_IN_F16 = 2 } kvc_dtype;
+typedef enum { KVC_HEAD_MAJOR = 0, KVC_LAYER_MAJOR = 1 } kvc_layout;
+
+/* Shape, type and layout of a cache.  Plain data. */
+typedef struct {
+    int32_t n_layer;
+    int32_t n_ctx;
+    int32_t n_head_kv;
+    int32_t head_dim;
+    int32_t type;    /* kvc_cache_type */
+    int32_t layout;  /* kvc_layout */
+} kvc_desc;
+
+/* A cache: its descriptor and four caller-owned device buffers.  For q8_0,
+ * k_q/v_q hold int8 codes and k_s/v_s fp16 scales; for f16, k_q/v_q hold the
+ * fp16 values and k_s/v_s are NULL.  Buffers must be 16-byte aligned and at
+ * least as large as kvc_cache_bytes reports.  Plain data, copied by value. */
+typedef struct {
+    kvc_desc d;
+    void *k_q;
+    void *k_s;
+    void *v_q;
+    void *v_s;
+} kvc_cache;
+
+/* ---- size queries and set-up (host only, no CUDA call) -------------------- */
+
+/* Bytes of each of the four cache buffers (scale sizes are 0 for f16).
+ * Returns KVC_EINVAL for an invalid descriptor. */
+int kvc_cache_bytes(const kvc_desc *desc, size_t *k_q, size_t *k_s, size_t *v_q, size_t *v_s);
+
+/* Bytes of the scratch buffer decode_attn needs for this cache and n_head_q:
+ * float32 partial results of the split-K pass, [n_head_q][max_split][head_dim + 2]. */
+int kvc_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, size_t *bytes);
+
+/* Bytes of the serialised state of n_tokens positions: 32 + n_layer * n_tokens *
+ * 2 * record, record = n_head_kv * head_dim/32 * 34 (q8_0) or n_head_kv *
+ * head_dim * 2 (f16).  Returns 0 for an invalid descriptor or n_tokens. */
+size_t kv_state_size(const kvc_desc *desc, int32_t n_tokens);
+
+/* Fill *out from a descriptor and four device buffers after checking them
+ * (shape, non-null, 16-byte alignment).  Writes *out only on success. */
+int kvc_cache_init(kvc_cache *out, const kvc_desc *desc, void *k_q, void *k_s, void *v_q, void *v_s);
+
+/* ---- hot path ---------------------------------------------------------------- */
+
+/* Append (quantise and store) the K/V rows of n_tokens tokens at cache
+ * positions [pos0, pos0 + n_tokens) of `layer`.  k, v: [n_tokens][n_head_kv]
+ * [head_dim] in `dtype`, values finite.  q8_0 blocks and f16 values exactly as
+ * defined above (bit-exact: float32 IEEE division, round half away from zero,
+ * fp16 round to nearest even).  n_tokens == 0 is a no-op.
+ * Errors: KVC_EINVAL (null, dtype), KVC_ERANGE (layer, pos0 + n_tokens > n_ctx). */
+int kv_cache_append(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens,
+                    const void *k, const void *v, int32_t dtype, kvc_stream_t stream);
+
+/* Causal attention of a chunk's query rows over the cache:
+ *   out[i][h] = sum_{j <= pos0+i} softmax_j(q[i][h] . khat[j][h/G] / sqrt(head_dim)) vhat[j][h/G]
+ * for i in [0, n_tokens), G = n_head_q / n_head_kv, khat/vhat the values the
+ * cache holds for `layer` at positions [0, pos0 + n_tokens).  The chunk's own
+ * K/V must have been appended (kv_cache_append earlier on the same stream).
+ * Rows are independent of how the prompt is cut into chunks.  Computed with
+ * fp16 tensor-core products and float32 accumulation and softmax.
+ * q: [n_tokens][n_head_q][head_dim] in dtype (f32, bf16 or f16); out float32.
+ * Errors: KVC_EINVAL (null, dtype, head_dim not 64/128, heads), KVC_ERANGE. */
+int prefill_chunk_attn(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens,
+                       const void *q, int32_t dtype, int32_t n_head_q, float *out,
+                       kvc_stream_t stream);
+
+/* Single-token decode attention at position pos: the formula above with one
+ * query row at pos, keys [0, pos].  The token's K/V must have been appended.
+ * Split-K over the key range into float32 partials in `scratch` (size from
+ * kvc_scratch_bytes), then a combine pass.  q: [n_head_q][head_dim] in dtype;
+ * out: [n_head_q][head_dim] float32.
+ * Errors: KVC_EINVAL, KVC_ERANGE, KVC_ENOSPC (scratch too small). */
+int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, int32_t dtype,
+                int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
+                kvc_stream_t stream);
+
+/* Serialise positions [0, n_tokens) of every layer into dst (device memory,
+ * dst_bytes >= kv_state_size).  The stream does not depend on the layout.
+ * Format: 32-byte header of eight little-endian uint32 (magic 'KVC1',
+ * version 1, n_layer, n_head_kv, head_dim, type, n_tokens, 0); then for each
+ * layer, for each position, the K record then the V record; a record holds
+ * the kv heads in order, each as head_dim/32 blocks of [fp16 scale LE][32
+ * int8 codes] (q8_0) or head_dim fp16 values LE (f16).
+ * Errors: KVC_EINVAL, KVC_ERANGE (n_tokens > n_ctx), KVC_ENOSPC. */
+int kv_state_get(const kvc_cache *cache, int32_t n_tokens, void *dst, size_t dst_bytes,
+                 kvc_stream_t stream);
+
+/* Restore a state written by kv_state_get (from a cache of any layout) into
+ * `cache`.  src: device memory of src_bytes.  Synchronises `stream` once to
+ * read the header, validates it (magic, version, shape and type equal to the
+ * cache's, n_tokens <= n_ctx, src_bytes equal to the size the header implies)
+ * and only then writes.  *n_tokens_out receives n_tokens on success.
+ * Errors: KVC_EINVAL (null), KVC_EFORMAT (any header mismatch), KVC_ECUDA. */
+int kv_state_set(kvc_cache *cache, const void *src, size_t src_bytes, int32_t *n_tokens_out,
+                 kvc_stream_t stream);
+
+/* ---- diagnostics ------------------------------------------------------------- */
+
+/* A short static description of a status code. */
+const char *kvc_strerror(int status);
+
+/* Synchronise the current device, then read and clear the device-side status
+ * word that kernels set when a bounded wait gives up (0 = none).  Returns
+ * KVC_ECUDA if the synchronisation fails. */
+int kvc_device_status(int32_t *status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

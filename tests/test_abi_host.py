@@ -1,0 +1,127 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and its host-side checks and size queries behave as
+documented (no call here reaches CUDA)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import state as ostate
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvc.h")
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    from decode_attention_kv_cache_gb300 import build as b
+    if not os.path.exists(b.LIB):
+        b.build()
+    import decode_attention_kv_cache_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\([^;{]*\)\s*;", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ["kv_cache_append", "prefill_chunk_attn", "decode_attn", "kv_state_get", "kv_state_set",
+              "kv_state_size", "kvc_cache_bytes", "kvc_scratch_bytes", "kvc_cache_init", "kvc_strerror",
+              "kvc_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kvc):
+    lib = ctypes.CDLL(kvc.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing
+
+
+def test_cache_bytes(kvc):
+    d = kvc.make_desc(64, 32768, 8, 128, "q8_0", "head_major")
+    kq, ks, vq, vs = kvc.cache_bytes(d)
+    n = 64 * 32768 * 8 * 128
+    assert (kq, ks, vq, vs) == (n, n // 16, n, n // 16)
+    d = kvc.make_desc(1, 20480, 8, 128, "f16", "layer_major")
+    assert kvc.cache_bytes(d) == (2 * 20480 * 1024, 0, 2 * 20480 * 1024, 0)
+
+
+@pytest.mark.parametrize("shape", [(1, 512, 2, 64, "q8_0"), (64, 32768, 8, 128, "q8_0"), (1, 20480, 8, 128, "f16"),
+                                   (3, 40, 1, 32, "q8_0"), (2, 9, 3, 96, "f16")])
+def test_state_size_agrees_with_the_oracle(kvc, shape):
+    L, T, H, D, ct = shape
+    d = kvc.make_desc(L, T, H, D, ct)
+    for n in (0, 1, 7, T):
+        assert kvc.lib.kv_state_size(ctypes.byref(d), n) == ostate.state_size(L, H, D, ct, n)
+    assert kvc.lib.kv_state_size(ctypes.byref(d), T + 1) == 0
+    assert kvc.lib.kv_state_size(ctypes.byref(d), -1) == 0
+
+
+def test_invalid_descriptors(kvc):
+    out = ctypes.c_size_t()
+    for bad in [kvc.make_desc(1, 16, 2, 48), kvc.make_desc(0, 16, 2, 64), kvc.make_desc(1, 16, 0, 64),
+                kvc.kvc_desc(1, 16, 2, 64, 7, 0), kvc.kvc_desc(1, 16, 2, 64, 1, 5)]:
+        s = [ctypes.c_size_t() for _ in range(4)]
+        assert kvc.lib.kvc_cache_bytes(ctypes.byref(bad), *[ctypes.byref(x) for x in s]) == kvc.KVC_EINVAL
+    d = kvc.make_desc(1, 16, 2, 64)
+    assert kvc.lib.kvc_scratch_bytes(ctypes.byref(d), 3, ctypes.byref(out)) == kvc.KVC_EINVAL
+    assert kvc.lib.kvc_scratch_bytes(ctypes.byref(d), 4, ctypes.byref(out)) == kvc.KVC_OK
+    assert out.value == 4 * 256 * 66 * 4
+
+
+def _fake_cache(kvc, cache_type="q8_0", misalign=0):
+    c = kvc.kvc_cache()
+    d = kvc.make_desc(2, 64, 2, 64, cache_type)
+    p = [ctypes.c_void_p(0x10000 * (i + 1) + misalign) for i in range(4)]
+    rc = kvc.lib.kvc_cache_init(ctypes.byref(c), ctypes.byref(d), *p)
+    return rc, c
+
+
+def test_cache_init_checks(kvc):
+    assert _fake_cache(kvc)[0] == kvc.KVC_OK
+    assert _fake_cache(kvc, misalign=8)[0] == kvc.KVC_EINVAL
+    c = kvc.kvc_cache()
+    d = kvc.make_desc(2, 64, 2, 64, "q8_0")
+    assert kvc.lib.kvc_cache_init(ctypes.byref(c), ctypes.byref(d), ctypes.c_void_p(0x10000), None,
+                                  ctypes.c_void_p(0x20000), None) == kvc.KVC_EINVAL
+    d = kvc.make_desc(2, 64, 2, 64, "f16")   # f16 needs no scale buffers
+    assert kvc.lib.kvc_cache_init(ctypes.byref(c), ctypes.byref(d), ctypes.c_void_p(0x10000), None,
+                                  ctypes.c_void_p(0x20000), None) == kvc.KVC_OK
+
+
+def test_hot_path_checks_run_before_any_launch(kvc):
+    _, c = _fake_cache(kvc)
+    k = ctypes.c_void_p(0x40000)
+    S = None
+    assert kvc.lib.kv_cache_append(ctypes.byref(c), 2, 0, 4, k, k, 1, S) == kvc.KVC_ERANGE
+    assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, 62, 4, k, k, 1, S) == kvc.KVC_ERANGE
+    assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, -1, 4, k, k, 1, S) == kvc.KVC_ERANGE
+    assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, 0, 4, k, k, 9, S) == kvc.KVC_EINVAL
+    assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, 0, 4, None, k, 1, S) == kvc.KVC_EINVAL
+    assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, 10, 0, None, None, 1, S) == kvc.KVC_OK  # empty: no-op
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 60, 5, k, 1, 4, k, S) == kvc.KVC_ERANGE
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 0, 5, k, 1, 3, k, S) == kvc.KVC_EINVAL
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 3, 0, None, 1, 4, None, S) == kvc.KVC_OK
+    assert kvc.lib.decode_attn(ctypes.byref(c), 0, 64, k, 1, 4, k, k, 1 << 20, S) == kvc.KVC_ERANGE
+    assert kvc.lib.decode_attn(ctypes.byref(c), 0, 5, k, 1, 4, k, k, 100, S) == kvc.KVC_ENOSPC
+    assert kvc.lib.decode_attn(ctypes.byref(c), 0, 5, k, 1, 36, k, k, 1 << 24, S) == kvc.KVC_EINVAL  # G = 18 > 16
+    assert kvc.lib.kv_state_get(ctypes.byref(c), 65, k, 1 << 20, S) == kvc.KVC_ERANGE
+    assert kvc.lib.kv_state_get(ctypes.byref(c), 10, k, 100, S) == kvc.KVC_ENOSPC
+    assert kvc.lib.kv_state_set(ctypes.byref(c), k, 16, ctypes.byref(ctypes.c_int32()), S) == kvc.KVC_EFORMAT
+    # unsupported head_dim for attention (append and state accept any multiple of 32)
+    c96 = kvc.kvc_cache()
+    d96 = kvc.make_desc(1, 64, 2, 96, "f16")
+    assert kvc.lib.kvc_cache_init(ctypes.byref(c96), ctypes.byref(d96), k, None, k, None) == kvc.KVC_OK
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c96), 0, 0, 5, k, 1, 4, k, S) == kvc.KVC_EINVAL
+
+
+def test_strerror(kvc):
+    for code in (0, -1, -2, -3, -4, -5, -6, 12):
+        assert len(kvc.lib.kvc_strerror(code)) > 0

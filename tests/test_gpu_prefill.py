@@ -1,0 +1,95 @@
+"""prefill_chunk_attn on the GPU: within tolerance of the oracle, and bitwise
+independent of the chunking and of the cache layout."""
+
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+from oracle.cache import OracleCache
+from parity_util import assert_cache_equal, assert_close, np32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvc(cuda_device):
+    import decode_attention_kv_cache_gb300 as m
+    return m
+
+
+def gpu_prefill(kvc, w, layout, chunk, layer=0, qkv=None):
+    g = kvc.KVCache(w.n_layer, w.n_ctx, w.n_head_kv, w.head_dim, w.cache, layout)
+    q, k, v = qkv if qkv is not None else si.layer_qkv(w, layer)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    out = torch.empty(w.n_prompt, w.n_head_q, w.head_dim, device="cuda")
+    for p, c in w.chunks(chunk):
+        kvc.kv_cache_append(g, layer, p, kd[p:p + c], vd[p:p + c])
+        kvc.prefill_chunk_attn(g, layer, p, qd[p:p + c], out=out[p:p + c])
+    torch.cuda.synchronize()
+    return g, out
+
+
+def oracle_prefill(w, chunk, layer=0, qkv=None):
+    o = OracleCache(w.n_layer, w.n_ctx, w.n_head_kv, w.head_dim, w.cache)
+    q, k, v = qkv if qkv is not None else si.layer_qkv(w, layer)
+    outs = []
+    for p, c in w.chunks(chunk):
+        o.append(layer, p, np32(k[p:p + c]), np32(v[p:p + c]))
+        outs.append(o.prefill_chunk(layer, p, np32(q[p:p + c])))
+    return o, np.concatenate(outs)
+
+
+CASES = [
+    # H_q, H_kv, D, cache, in dtype, prompt, chunk
+    (4, 2, 64, "q8_0", "f32", 256, 64),
+    (8, 2, 128, "q8_0", "bf16", 333, 100),
+    (8, 2, 128, "f16", "bf16", 333, 128),
+    (5, 1, 128, "q8_0", "f16", 260, 129),
+    (2, 2, 64, "f16", "f32", 140, 7),
+    (10, 2, 128, "q8_0", "bf16", 520, 520),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "%d-%d-%d-%s-%s-%d-%d" % c)
+def test_prefill_matches_oracle(kvc, case):
+    hq, hkv, d, cache, dt, n, chunk = case
+    w = si.small_workload("pf", hq, hkv, d, cache, dt, n_prompt=n, chunk=chunk, n_decode=0, seed=n + d,
+                          k_outlier_frac=0.02)
+    g, out = gpu_prefill(kvc, w, "head_major", chunk)
+    o, ref = oracle_prefill(w, chunk)
+    assert_cache_equal(g, o, n)
+    assert_close(out.cpu().numpy(), ref, "prefill")
+
+
+def test_prefill_chunk_and_layout_invariance(kvc):
+    w = si.small_workload("inv", 10, 2, 128, "q8_0", "bf16", n_prompt=700, chunk=0, n_decode=0, seed=21)
+    qkv = si.layer_qkv(w, 0)
+    _, whole = gpu_prefill(kvc, w, "head_major", 0, qkv=qkv)
+    for chunk in (1, 37, 128, 300):
+        for layout in ("head_major", "layer_major"):
+            if chunk == 1 and layout == "layer_major":
+                continue
+            _, out = gpu_prefill(kvc, w, layout, chunk, qkv=qkv)
+            assert torch.equal(out, whole), "chunk %d %s changed the result" % (chunk, layout)
+    _, ref = oracle_prefill(w, 0, qkv=qkv)
+    assert_close(whole.cpu().numpy(), ref)
+
+
+def test_prefill_f16_cache_invariance(kvc):
+    w = si.small_workload("inv16", 8, 8, 64, "f16", "bf16", n_prompt=400, chunk=0, n_decode=0, seed=22)
+    qkv = si.layer_qkv(w, 0)
+    _, whole = gpu_prefill(kvc, w, "layer_major", 0, qkv=qkv)
+    _, out = gpu_prefill(kvc, w, "head_major", 96, qkv=qkv)
+    assert torch.equal(out, whole)
+
+
+def test_prefill_other_layer_and_repeatability(kvc):
+    w = si.small_workload("lay", 8, 2, 128, "f16", "bf16", n_prompt=300, chunk=150, n_decode=0, seed=23, n_layer=2)
+    qkv = si.layer_qkv(w, 1)
+    _, a = gpu_prefill(kvc, w, "head_major", 150, layer=1, qkv=qkv)
+    _, b = gpu_prefill(kvc, w, "head_major", 150, layer=1, qkv=qkv)
+    assert torch.equal(a, b)
+    _, ref = oracle_prefill(w, 150, layer=1, qkv=qkv)
+    assert_close(a.cpu().numpy(), ref)
+    assert kvc.kvc_device_status() == 0
