@@ -5,9 +5,10 @@ chunked prefill attention, split-K decode attention, state pack/unpack) runs in
 the library's CUDA kernels; torch supplies device memory and the current
 stream.  The functions carry the names of the C ABI in include/kvc.h.
 
-There is no fallback: importing this package fails if libkvc.so has not been
-built (python -m decode_attention_kv_cache_gb300.build), and every call raises
-KvcError when the library reports an error.
+There is no fallback: the library is loaded on first use, which raises
+ImportError if libkvc.so has not been built (python -m
+decode_attention_kv_cache_gb300.build); every call raises KvcError when the
+library reports an error.
 """
 
 import ctypes
@@ -26,7 +27,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
 class KvcError(RuntimeError):
     def __init__(self, status, what):
-        super().__init__("%s: %s (%d)" % (what, lib.kvc_strerror(status).decode(), status))
+        super().__init__("%s: %s (%d)" % (what, _lib().kvc_strerror(status).decode(), status))
         self.status = status
 
 
@@ -64,7 +65,20 @@ def _load():
     return L
 
 
-lib = _load()
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _lib()
+    raise AttributeError(name)
 
 
 def _check(status, what):
@@ -95,7 +109,7 @@ def make_desc(n_layer, n_ctx, n_head_kv, head_dim, cache_type="q8_0", layout="he
 
 def cache_bytes(desc):
     s = [ctypes.c_size_t() for _ in range(4)]
-    _check(lib.kvc_cache_bytes(ctypes.byref(desc), *[ctypes.byref(x) for x in s]), "kvc_cache_bytes")
+    _check(_lib().kvc_cache_bytes(ctypes.byref(desc), *[ctypes.byref(x) for x in s]), "kvc_cache_bytes")
     return tuple(x.value for x in s)
 
 
@@ -117,7 +131,7 @@ class KVCache:
         self._sizes = (kq, ks, vq, vs)
         self.c = kvc_cache()
         scales = cache_type == "q8_0"
-        _check(lib.kvc_cache_init(ctypes.byref(self.c), ctypes.byref(self.desc), _ptr(self._bufs[0]),
+        _check(_lib().kvc_cache_init(ctypes.byref(self.c), ctypes.byref(self.desc), _ptr(self._bufs[0]),
                                   _ptr(self._bufs[1]) if scales else ctypes.c_void_p(0), _ptr(self._bufs[2]),
                                   _ptr(self._bufs[3]) if scales else ctypes.c_void_p(0)), "kvc_cache_init")
 
@@ -140,17 +154,17 @@ class KVCache:
 
     def scratch_bytes(self, n_head_q):
         n = ctypes.c_size_t()
-        _check(lib.kvc_scratch_bytes(ctypes.byref(self.desc), n_head_q, ctypes.byref(n)), "kvc_scratch_bytes")
+        _check(_lib().kvc_scratch_bytes(ctypes.byref(self.desc), n_head_q, ctypes.byref(n)), "kvc_scratch_bytes")
         return n.value
 
     def state_size(self, n_tokens):
-        return lib.kv_state_size(ctypes.byref(self.desc), n_tokens)
+        return _lib().kv_state_size(ctypes.byref(self.desc), n_tokens)
 
 
 def kv_cache_append(cache, layer, pos0, k, v, stream=None):
     """Quantise/round and store K, V [n, H_kv, D] at positions [pos0, pos0 + n) of `layer`."""
     _need(k, "k"); _need(v, "v", k.dtype)
-    st = lib.kv_cache_append(ctypes.byref(cache.c), layer, pos0, k.shape[0], _ptr(k), _ptr(v), DTYPES[k.dtype],
+    st = _lib().kv_cache_append(ctypes.byref(cache.c), layer, pos0, k.shape[0], _ptr(k), _ptr(v), DTYPES[k.dtype],
                              _stream(stream, k.device))
     _check(st, "kv_cache_append")
 
@@ -161,7 +175,7 @@ def prefill_chunk_attn(cache, layer, pos0, q, out=None, stream=None):
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32)
-    st = lib.prefill_chunk_attn(ctypes.byref(cache.c), layer, pos0, q.shape[0], _ptr(q), DTYPES[q.dtype],
+    st = _lib().prefill_chunk_attn(ctypes.byref(cache.c), layer, pos0, q.shape[0], _ptr(q), DTYPES[q.dtype],
                                 q.shape[1], _ptr(out), _stream(stream, q.device))
     _check(st, "prefill_chunk_attn")
     return out
@@ -176,7 +190,7 @@ def decode_attn(cache, layer, pos, q, out=None, scratch=None, stream=None):
     if scratch is None:
         scratch = torch.empty(cache.scratch_bytes(n_head_q), dtype=torch.uint8, device=q.device)
     _need(out, "out", torch.float32); _need(scratch, "scratch")
-    st = lib.decode_attn(ctypes.byref(cache.c), layer, pos, _ptr(q), DTYPES[q.dtype], n_head_q, _ptr(out),
+    st = _lib().decode_attn(ctypes.byref(cache.c), layer, pos, _ptr(q), DTYPES[q.dtype], n_head_q, _ptr(out),
                          _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream, q.device))
     _check(st, "decode_attn")
     return out
@@ -188,7 +202,7 @@ def kv_state_get(cache, n_tokens, dst=None, stream=None):
     if dst is None:
         dst = torch.empty(max(n, 16), dtype=torch.uint8, device=cache.device)
     _need(dst, "dst")
-    st = lib.kv_state_get(ctypes.byref(cache.c), n_tokens, _ptr(dst), dst.numel() * dst.element_size(),
+    st = _lib().kv_state_get(ctypes.byref(cache.c), n_tokens, _ptr(dst), dst.numel() * dst.element_size(),
                           _stream(stream, cache.device))
     _check(st, "kv_state_get")
     return dst[:n]
@@ -198,7 +212,7 @@ def kv_state_set(cache, src, stream=None):
     """Restore a state (uint8 CUDA tensor of exactly the state's size); returns n_tokens."""
     _need(src, "src")
     n = ctypes.c_int32(-1)
-    st = lib.kv_state_set(ctypes.byref(cache.c), _ptr(src), src.numel() * src.element_size(), ctypes.byref(n),
+    st = _lib().kv_state_set(ctypes.byref(cache.c), _ptr(src), src.numel() * src.element_size(), ctypes.byref(n),
                           _stream(stream, cache.device))
     _check(st, "kv_state_set")
     return n.value
@@ -207,5 +221,5 @@ def kv_state_set(cache, src, stream=None):
 def kvc_device_status():
     """Synchronise and read/clear the device status word (non-zero: a kernel gave up a bounded wait)."""
     s = ctypes.c_int32(0)
-    _check(lib.kvc_device_status(ctypes.byref(s)), "kvc_device_status")
+    _check(_lib().kvc_device_status(ctypes.byref(s)), "kvc_device_status")
     return s.value
