@@ -278,6 +278,7 @@ def run_gpu(args, rank, world, local):
     clocks.start()
     dist_barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("kvc_timed")
     for _ in range(args.steps):
         l2_flush(torch, flush)
         s0 = torch.cuda.Event(enable_timing=True); s0.record()
@@ -285,6 +286,7 @@ def run_gpu(args, rank, world, local):
         s1 = torch.cuda.Event(enable_timing=True); s1.record()
         steps.append((s0, s1))
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     dist_barrier(world)
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in steps]
