@@ -128,6 +128,20 @@ int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *
                          (cudaStream_t)stream);
 }
 
+int decode_attn_noalloc(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, int32_t dtype,
+                        int32_t n_head_q, float *out, kvc_stream_t stream) {
+    if (!cache_ok(cache) || !dtype_ok(dtype)) return KVC_EINVAL;
+    if (cache->d.head_dim != 64 && cache->d.head_dim != 128) return KVC_EINVAL;
+    if (n_head_q <= 0 || n_head_q % cache->d.n_head_kv || n_head_q / cache->d.n_head_kv > 16)
+        return KVC_EINVAL;
+    if (layer < 0 || layer >= cache->d.n_layer || pos < 0 || pos >= cache->d.n_ctx) return KVC_ERANGE;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) return KVC_EINVAL;
+    size_t need = 0;
+    kvc_scratch_bytes(&cache->d, n_head_q, &need);
+    if (need > decode_noalloc_capacity()) return KVC_ENOSPC;  // more partials than the fixed array holds
+    return launch_decode_noalloc(*cache, layer, pos, q, dtype, n_head_q, out, (cudaStream_t)stream);
+}
+
 int kv_state_get(const kvc_cache *cache, int32_t n_tokens, void *dst, size_t dst_bytes, kvc_stream_t stream) {
     if (!cache_ok(cache) || !dst || !aligned16(dst) || n_tokens < 0) return KVC_EINVAL;
     if (n_tokens > cache->d.n_ctx) return KVC_ERANGE;

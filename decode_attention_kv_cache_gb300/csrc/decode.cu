@@ -424,7 +424,46 @@ int launch_d(const kvc_cache &c, int layer, int pos, const void *q, int dtype, i
     }
 }
 
+// ---- fixed scratch for decode_attn_noalloc ---------------------------------------------
+// Some callers cannot allocate device memory: code hosted inside an engine that
+// owns every device allocation, or code on a path where cudaMalloc's implicit
+// device synchronisation is not allowed.  For them the split-K partials live in
+// this file-scope device array instead of a caller buffer.  Every device that
+// loads the library holds it until the process exits; all calls share it.
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)8 << 20;  // 8 MiB
+static __device__ __align__(256) float g_noalloc_scratch[NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+// The array's device address on the current device.  In host code the symbol
+// name is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) through cudaGetSymbolAddress and cached.
+int noalloc_scratch_address(float **out) {
+    constexpr int MAX_DEVICES = 64;
+    static std::mutex mu;
+    static float *addr[MAX_DEVICES] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KVC_ECUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KVC_ECUDA;
+        addr[dev] = static_cast<float *>(p);
+    }
+    *out = addr[dev];
+    return KVC_OK;
+}
+
 }  // namespace
+
+size_t decode_noalloc_capacity() { return NOALLOC_SCRATCH_BYTES; }
+
+int launch_decode_noalloc(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
+                          float *out, cudaStream_t s) {
+    float *scratch = nullptr;
+    const int rc = noalloc_scratch_address(&scratch);
+    if (rc != KVC_OK) return rc;
+    // every partial the combine pass reads is written by the split pass first: nothing needs clearing
+    return launch_decode(c, layer, pos, q, dtype, n_head_q, out, scratch, s);
+}
 
 int decode_max_split() { return MAX_SPLIT; }
 

@@ -39,6 +39,9 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
 int decode_max_split();
 int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                   float *out, float *scratch, cudaStream_t s);
+size_t decode_noalloc_capacity();
+int launch_decode_noalloc(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
+                          float *out, cudaStream_t s);
 int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream_t s);
 int launch_state_unpack(const kvc_cache &c, int n_tokens, const uint8_t *src, cudaStream_t s);
 

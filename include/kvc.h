@@ -150,6 +150,24 @@ int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *
                 int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
                 kvc_stream_t stream);
 
+/* decode_attn without a scratch argument, for callers that cannot allocate
+ * device memory themselves (code hosted by an engine that owns every device
+ * allocation, or a path where cudaMalloc's implicit synchronisation is not
+ * allowed).  The source pages have no counterpart of this call; it is a
+ * convenience of this library.  The split-K partials go to a fixed 8 MiB
+ * device array inside the library (held on every device that loads it, until
+ * the process exits): calls whose kvc_scratch_bytes(desc, n_head_q) exceeds
+ * 8 MiB (n_head_q * 256 * (head_dim + 2) * 4 bytes, i.e. n_head_q > 63 at
+ * head_dim 128) are rejected with KVC_ENOSPC before anything is launched.
+ * The call allocates nothing.  Its first call on a device looks up that
+ * array's device address (cudaGetSymbolAddress) with the device current;
+ * make that first call before capturing a stream into a CUDA graph.  All
+ * calls share the one array: calls that overlap on the GPU (other streams,
+ * other threads) race and must be serialised by the caller.  Arguments,
+ * result and errors otherwise as decode_attn. */
+int decode_attn_noalloc(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, int32_t dtype,
+                        int32_t n_head_q, float *out, kvc_stream_t stream);
+
 /* Serialise positions [0, n_tokens) of every layer into dst (device memory,
  * dst_bytes >= kv_state_size).  The stream does not depend on the layout.
  * Format: 32-byte header of eight little-endian uint32 (magic 'KVC1',
