@@ -168,6 +168,7 @@ class GpuRequest:
         self.out_p = torch.empty(w.n_layer, w.n_prompt, w.n_head_q, w.head_dim, device=device)
         self.out_d = torch.empty(w.n_layer, max(w.n_decode, 1), w.n_head_q, w.head_dim, device=device)
         self.scratch = torch.empty(self.src.scratch_bytes(w.n_head_q), dtype=torch.uint8, device=device)
+        self.pscratch = self.src.prefill_scratch(w.n_head_q, w.chunk if w.chunk > 0 else w.n_prompt)
         self.state = torch.empty(self.src.state_size(w.n_tokens), dtype=torch.uint8, device=device)
         self.host_out_p = torch.empty(self.out_p.shape, dtype=torch.float32).pin_memory()
         self.host_out_d = torch.empty(self.out_d.shape, dtype=torch.float32).pin_memory()
@@ -214,7 +215,8 @@ class GpuRequest:
                 kvc.kv_cache_append(self.src, layer, p, k[p:p + c], v[p:p + c])
                 if ev is not None:
                     a = E(enable_timing=True); a.record()
-                kvc.prefill_chunk_attn(self.src, layer, p, q[p:p + c], out=self.out_p[layer, p:p + c])
+                kvc.prefill_chunk_attn(self.src, layer, p, q[p:p + c], out=self.out_p[layer, p:p + c],
+                                       scratch=self.pscratch)
                 if ev is not None:
                     b = E(enable_timing=True); b.record(); ev["attn"].append((a, b, self.flops[ci]))
             if ev is not None:

@@ -52,7 +52,8 @@ def _load():
         "kv_state_size": (SZ, [P(kvc_desc), I32]),
         "kvc_cache_init": (ctypes.c_int, [P(kvc_cache), P(kvc_desc), VP, VP, VP, VP]),
         "kv_cache_append": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, VP, I32, VP]),
-        "prefill_chunk_attn": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, I32, I32, VP, VP]),
+        "kvc_prefill_scratch_bytes": (ctypes.c_int, [P(kvc_desc), I32, I32, P(SZ)]),
+        "prefill_chunk_attn": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, I32, I32, VP, VP, SZ, VP]),
         "decode_attn": (ctypes.c_int, [P(kvc_cache), I32, I32, VP, I32, I32, VP, VP, SZ, VP]),
         "kv_state_get": (ctypes.c_int, [P(kvc_cache), I32, VP, SZ, VP]),
         "kv_state_set": (ctypes.c_int, [P(kvc_cache), VP, SZ, P(I32), VP]),
@@ -157,6 +158,17 @@ class KVCache:
         _check(_lib().kvc_scratch_bytes(ctypes.byref(self.desc), n_head_q, ctypes.byref(n)), "kvc_scratch_bytes")
         return n.value
 
+    def prefill_scratch_bytes(self, n_head_q, max_tokens):
+        n = ctypes.c_size_t()
+        _check(_lib().kvc_prefill_scratch_bytes(ctypes.byref(self.desc), n_head_q, max_tokens, ctypes.byref(n)),
+               "kvc_prefill_scratch_bytes")
+        return n.value
+
+    def prefill_scratch(self, n_head_q, max_tokens):
+        """A zero-filled prefill scratch buffer for chunks of up to max_tokens rows."""
+        return torch.zeros(max(self.prefill_scratch_bytes(n_head_q, max_tokens), 16), dtype=torch.uint8,
+                           device=self.device)
+
     def state_size(self, n_tokens):
         return _lib().kv_state_size(ctypes.byref(self.desc), n_tokens)
 
@@ -169,14 +181,20 @@ def kv_cache_append(cache, layer, pos0, k, v, stream=None):
     _check(st, "kv_cache_append")
 
 
-def prefill_chunk_attn(cache, layer, pos0, q, out=None, stream=None):
-    """Causal attention of chunk rows q [C, H_q, D] at positions [pos0, pos0 + C); returns out [C, H_q, D] f32."""
+def prefill_chunk_attn(cache, layer, pos0, q, out=None, scratch=None, stream=None):
+    """Causal attention of chunk rows q [C, H_q, D] at positions [pos0, pos0 + C); returns out [C, H_q, D] f32.
+
+    scratch: a zero-filled uint8 CUDA buffer (KVCache.prefill_scratch); one is made when None.
+    """
     _need(q, "q")
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-    _need(out, "out", torch.float32)
+    if scratch is None:
+        scratch = cache.prefill_scratch(q.shape[1], max(q.shape[0], 1))
+    _need(out, "out", torch.float32); _need(scratch, "scratch")
     st = _lib().prefill_chunk_attn(ctypes.byref(cache.c), layer, pos0, q.shape[0], _ptr(q), DTYPES[q.dtype],
-                                q.shape[1], _ptr(out), _stream(stream, q.device))
+                                q.shape[1], _ptr(out), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                _stream(stream, q.device))
     _check(st, "prefill_chunk_attn")
     return out
 

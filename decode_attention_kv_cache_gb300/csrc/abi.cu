@@ -101,16 +101,27 @@ int kv_cache_append(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t
     return launch_append(*cache, layer, pos0, n_tokens, k, v, dtype, (cudaStream_t)stream);
 }
 
+int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t max_tokens, size_t *bytes) {
+    if (!desc_ok(desc) || !bytes || n_head_q <= 0 || n_head_q % desc->n_head_kv) return KVC_EINVAL;
+    if (max_tokens <= 0 || max_tokens > desc->n_ctx) return KVC_ERANGE;
+    const size_t b = prefill_scratch_bytes(*desc, n_head_q, max_tokens);
+    if (b == 0) return KVC_EINVAL;
+    *bytes = b;
+    return KVC_OK;
+}
+
 int prefill_chunk_attn(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens,
-                       const void *q, int32_t dtype, int32_t n_head_q, float *out, kvc_stream_t stream) {
+                       const void *q, int32_t dtype, int32_t n_head_q, float *out, void *scratch,
+                       size_t scratch_bytes, kvc_stream_t stream) {
     if (!cache_ok(cache) || !dtype_ok(dtype)) return KVC_EINVAL;
     if (cache->d.head_dim != 64 && cache->d.head_dim != 128) return KVC_EINVAL;
     if (n_head_q <= 0 || n_head_q % cache->d.n_head_kv || n_head_q > 65535 || n_tokens < 0) return KVC_EINVAL;
     if (layer < 0 || layer >= cache->d.n_layer || pos0 < 0 || (int64_t)pos0 + n_tokens > cache->d.n_ctx)
         return KVC_ERANGE;
     if (n_tokens == 0) return KVC_OK;
-    if (!q || !out || !aligned16(q) || !aligned16(out)) return KVC_EINVAL;
-    return launch_prefill(*cache, layer, pos0, n_tokens, q, dtype, n_head_q, out, (cudaStream_t)stream);
+    if (!q || !out || !scratch || !aligned16(q) || !aligned16(out) || !aligned16(scratch)) return KVC_EINVAL;
+    return launch_prefill(*cache, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, scratch_bytes,
+                          (cudaStream_t)stream);
 }
 
 int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, int32_t dtype,

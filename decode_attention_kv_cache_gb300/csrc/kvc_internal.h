@@ -34,8 +34,9 @@ inline int dtype_bytes(int dtype) { return dtype == KVC_IN_F32 ? 4 : 2; }
 // Launchers: arguments are already validated; return KVC_OK or KVC_ECUDA.
 int launch_append(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *k,
                   const void *v, int dtype, cudaStream_t s);
+size_t prefill_scratch_bytes(const kvc_desc &d, int n_head_q, int max_tokens);
 int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, int dtype,
-                   int n_head_q, float *out, cudaStream_t s);
+                   int n_head_q, float *out, void *scratch, size_t scratch_bytes, cudaStream_t s);
 int decode_max_split();
 int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                   float *out, float *scratch, cudaStream_t s);

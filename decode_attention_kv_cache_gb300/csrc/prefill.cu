@@ -9,30 +9,36 @@
 // llama.cpp PR #58 "completion : allow the prompt to be processed under its
 // own split mode", section "Why").
 //
-// Design (one CTA = 128 query rows of one query head; key tiles of 128 at
-// absolute positions 0, 128, 256, ...):
-//   warp 0      TMA producer: the Q tile once, then the K/V tiles (int8 codes
-//               for q8_0, fp16 values for f16) into shared memory.
-//   warp 1      allocates 512 TMEM columns; one lane issues the MMAs:
-//               S = Q K^T (M=128, N=128, fp16 x fp16 -> fp32 in TMEM), and
-//               O += P V (M=128, N=D, V as an MN-major operand).
-//   warps 4-7   softmax: thread r owns query row r (TMEM lane r); reads its S
-//               row from TMEM, applies the causal mask, keeps a running max
-//               and sum, writes P (fp16) to shared memory for the PV MMA, and
-//               in the end divides O by the sum and stores it (fp32).
-//   warps 8-11  (q8_0 only) dequantise the int8 K/V tile: thread r converts key
-//               row r to fp16 d*q in the 128-byte-swizzled operand layout.
-// The running max is re-based only when it grows by more than 2^8, so most
-// tiles need no O rescale; the decision is per row, so results stay exact
-// per row and independent of the chunking.
+// Work decomposition.  A unit is 128 query rows of one query head.  The units
+// of one kv group are listed q-tile-major and taken in pairs, so a CTA works on
+// two Q tiles that read the same K/V tiles (two query heads of the group, or
+// the last head of one q-tile with the first of the next).  The keys of a pair
+// are cut at ABSOLUTE split boundaries of ST tiles (ST is fixed by the cache
+// size): an item is (pair, split).  Persistent CTAs (one per SM) take items
+// round-robin.  An item whose pair has one split writes the output directly;
+// otherwise it writes its partial (O, running max, sum) and the last item of
+// the pair to finish merges the partials in split order.  Because tiles and
+// splits sit at absolute positions and every merge runs in split order, a
+// row's result does not depend on how the prompt is cut into chunks.
 //
-// Operand type: fp16 for Q, K, V and P (the same tensor rate as bf16): int8
-// codes are exact in fp16, d*q rounds once to 11 bits, and the f16 cache
-// feeds the MMA as stored.
-//
-// Every mbarrier wait is bounded (2 s wall clock); a wait that gives up sets a
-// device status word and the CTA skips the rest of its work, frees its TMEM
-// and exits.
+// One CTA:
+//   warp 0      TMA producer: the two Q tiles of an item, then K and V tiles
+//               (int8 codes into a raw ring for q8_0; fp16 values straight into
+//               the operand ring for f16).
+//   warp 1      allocates all 512 TMEM columns (S/P and O for both Q tiles);
+//               one lane issues tcgen05.mma: S = Q K^T (both operands in shared
+//               memory) and O += P V (P from tensor memory, V as an MN-major
+//               shared-memory operand), interleaved as
+//               PV_A(k), S_A(k+1), PV_B(k), S_B(k+1) so each softmax has two
+//               MMAs' time to turn S into P.
+//   warps 4-7   softmax of Q tile A, warps 8-11 of Q tile B: thread r owns row r
+//               (TMEM lane r): row max, exp2, fp16 P written back over S in
+//               tensor memory, O rescaled in TMEM only when the running max
+//               grows by more than 2^8; epilogue O / l.
+//   warps 12-15 (q8_0) dequantise int8 rows into fp16 d*q in the 128-byte
+//               swizzled operand layout.
+// Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
+// status word and the CTA skips its remaining work, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,33 +58,34 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = 128;           // query rows per CTA
+constexpr int BM = 128;           // query rows per Q tile
 constexpr int BN = 128;           // keys per tile
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;
-
-enum Bar {
-    B_QFULL, B_QREADY, B_RAWFULL, B_RAWEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1,
-    B_SFULL0, B_SFULL1, B_PFULL, B_ODONE, NBAR
-};
+constexpr int MAX_SPLITS = 64;
+// a partial row: D values, the running max, the sum, two pad floats (keeps rows 16-byte aligned)
+#define PART_ROW(D) ((D) + 4)
 
 template <int D, bool Q8>
-struct Layout {
-    static constexpr int Q_BYTES = BM * D * 2;
-    static constexpr int KV_BYTES = BN * D * 2;    // one fp16 K or V stage
-    static constexpr int P_BYTES = BM * BN * 2;
-    static constexpr int RAW_BYTES = Q8 ? BN * D : 0;
+struct Cfg {
+    static constexpr int QT_BYTES = BM * D * 2;    // one fp16 Q tile
+    static constexpr int ST_BYTES = BN * D * 2;    // one ring stage: a fp16 K or V tile
+    static constexpr int RAW_BYTES = BN * D;       // one int8 K or V tile
+    static constexpr int NS = Q8 ? 3 : 5;          // fp16 operand ring stages
+    static constexpr int NR = Q8 ? 4 : 1;          // int8 raw ring stages
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-    static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-    static constexpr int OFF_RAWK = OFF_P + P_BYTES;
-    static constexpr int OFF_RAWV = OFF_RAWK + RAW_BYTES;
-    static constexpr int OFF_BAR = OFF_RAWV + RAW_BYTES;
-    static constexpr int USED = OFF_BAR + 256;
-    // at least ~120 KB so that one CTA runs per SM (it allocates all 512 TMEM columns)
-    static constexpr int ALLOC = (USED + 1024 > 122880) ? USED + 1024 : 122880;
-    static constexpr int THREADS = Q8 ? 384 : 256;
+    static constexpr int OFF_RING = OFF_Q + 2 * QT_BYTES;
+    static constexpr int OFF_RAW = OFF_RING + NS * ST_BYTES;
+    static constexpr int OFF_BAR = OFF_RAW + (Q8 ? NR * RAW_BYTES : 0);
+    static constexpr int USED = OFF_BAR + 512;
+    static constexpr int ALLOC = (USED + 1024 > 122880) ? USED + 1024 : 122880;  // one CTA per SM
+    static constexpr int THREADS = Q8 ? 512 : 384;
+};
+
+enum Bar {
+    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ODONE0, B_ODONE1,
+    B_OFREE0, B_OFREE1, B_EPI, B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
+    B_RAW_EMPTY = B_RAW_FULL + 8, NBAR = B_RAW_EMPTY + 8
 };
 
 struct Args {
@@ -86,22 +93,62 @@ struct Args {
     const uint16_t *ks;
     const uint16_t *vs;
     float *out;
+    float *part;      // partials [pair][split][tile][row][PART_ROW]
+    int *tickets;     // [pair]
     Geom g;
-    int layer, pos0, n_rows, kv_len, n_head_q, group, n_qtiles;
+    int layer, pos0, C, kv_len, H_q, G, H_kv, n_qt, U, J, ST, smax, n_items;
     float scale_log2;
+    int cum[MAX_SPLITS + 1];   // items before split index s
+    int jmin[MAX_SPLITS];      // first pair index that reaches split s
 };
 
-// Byte offset of 16-byte chunk `c` (0..7) of row `row` in a 128-byte-swizzled
-// tile whose 8-row atoms are 1024 bytes.
+struct Item {
+    int g, j, s, ns, k0, k1;
+    int qt[2], h[2], tf[2], tl[2];
+    bool has[2];
+};
+
+__device__ __forceinline__ int unit_tl(const Args &a, int qt) {
+    return a.pos0 + min(qt * BM + BM, a.C) - 1;
+}
+
+__device__ __forceinline__ Item decode_item(const Args &a, int i) {
+    Item it;
+    int s = 0;
+    while (s + 1 < a.smax && a.cum[s + 1] <= i) ++s;
+    const int r = i - a.cum[s];
+    const int nj = a.J - a.jmin[s];
+    it.g = r / nj;
+    it.j = a.jmin[s] + r % nj;
+    it.s = s;
+    for (int x = 0; x < 2; ++x) {
+        const int e = 2 * it.j + x;
+        it.has[x] = e < a.U;
+        const int ee = it.has[x] ? e : 2 * it.j;
+        it.qt[x] = ee / a.G;
+        it.h[x] = it.g * a.G + ee % a.G;
+        it.tf[x] = a.pos0 + it.qt[x] * BM;
+        it.tl[x] = unit_tl(a, it.qt[x]);
+    }
+    const int T = it.tl[it.has[1] ? 1 : 0] / BN + 1;
+    it.ns = (T + a.ST - 1) / a.ST;
+    it.k0 = s * a.ST;
+    it.k1 = min(T, (s + 1) * a.ST);
+    return it;
+}
+
+__device__ __forceinline__ bool tile_active(const Item &it, int x, int k) {
+    return it.has[x] && k * BN <= it.tl[x];
+}
+
 __device__ __forceinline__ uint32_t sw128(int row, int c) {
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4));
 }
-// Same for a 64-byte-swizzled tile of 64-byte rows.
 __device__ __forceinline__ uint32_t sw64(int row, int c) {
     return (uint32_t)(row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
 }
-// Chunk `cc` (8 halves) of row `row` in an fp16 operand tile of `rows` rows:
-// 64-half column blocks of rows*128 bytes each, 128-byte swizzle inside.
+// Chunk `cc` (8 halves) of row `row` of an fp16 operand tile of `rows` rows
+// (64-half column blocks of rows*128 bytes, 128-byte swizzle inside).
 __device__ __forceinline__ uint32_t op_off(int rows, int row, int cc) {
     return (uint32_t)((cc >> 3) * rows * 128) + sw128(row, cc & 7);
 }
@@ -111,54 +158,72 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
            ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
 
-// 4 int8 codes (one 32-bit word) times the fp16 scale, as two fp16x2 words.
+// 4 int8 codes times the fp16 scale, as two fp16x2 words (one rounding each).
 __device__ __forceinline__ void dequant4(uint32_t w, __half2 d2, uint32_t &lo, uint32_t &hi) {
-    // (byte ^ 0x80) in the low 8 bits of an fp16 with exponent bits 0x64 is 1024 + q + 128 exactly
-    const uint32_t a = (__byte_perm(w, 0, 0x0100) & 0x00FF00FFu) ^ 0x64806480u;
+    const uint32_t a = (__byte_perm(w, 0, 0x0100) & 0x00FF00FFu) ^ 0x64806480u;  // 1024 + q + 128
     const uint32_t b = (__byte_perm(w, 0, 0x0302) & 0x00FF00FFu) ^ 0x64806480u;
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    __half2 qa = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);  // exact integers
-    __half2 qb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
-    __half2 ra = __hmul2(qa, d2);  // one rounding: fp16(d * q)
-    __half2 rb = __hmul2(qb, d2);
+    __half2 ra = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&a), bias), d2);
+    __half2 rb = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b), bias), d2);
     lo = *reinterpret_cast<uint32_t *>(&ra);
     hi = *reinterpret_cast<uint32_t *>(&rb);
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 template <int D, bool Q8, int QDT>
-__global__ void __launch_bounds__(Layout<D, Q8>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Args a) {
-    using L = Layout<D, Q8>;
+    using L = Cfg<D, Q8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    volatile int *s_last = reinterpret_cast<volatile int *>(s_tmem + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qtile = a.n_qtiles - 1 - (int)blockIdx.x;  // the longest key ranges start first
-    const int h = blockIdx.y, hkv = h / a.group;
-    const int r0 = qtile * BM;
-    const int rows = min(BM, a.n_rows - r0);
-    const int t_first = a.pos0 + r0;
-    const int t_last = t_first + rows - 1;
-    const int n_tiles = t_last / BN + 1;
 
     if (threadIdx.x == 0) {
         *s_abort = 0;
         mbar_init(&bars[B_QFULL], 1);
-        mbar_init(&bars[B_QREADY], 128);
-        mbar_init(&bars[B_RAWFULL], 1);
-        mbar_init(&bars[B_RAWEMPTY], 128);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_KVFULL0 + s], Q8 ? 128 : 1);
-            mbar_init(&bars[B_KVEMPTY0 + s], 1);
-            mbar_init(&bars[B_SFULL0 + s], 1);
+        mbar_init(&bars[B_QREADY], 256);
+        mbar_init(&bars[B_QEMPTY], 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bars[B_SFULL0 + x], 1);
+            mbar_init(&bars[B_PFULL0 + x], 128);
+            mbar_init(&bars[B_ODONE0 + x], 1);
+            mbar_init(&bars[B_OFREE0 + x], 128);
         }
-        mbar_init(&bars[B_PFULL], 128);
-        mbar_init(&bars[B_ODONE], 1);
+        mbar_init(&bars[B_EPI], 256);
+        for (int s = 0; s < L::NS; ++s) {
+            mbar_init(&bars[B_RING_FULL + s], Q8 ? 128 : 1);
+            mbar_init(&bars[B_RING_EMPTY + s], 1);
+        }
+        for (int s = 0; s < L::NR; ++s) {
+            mbar_init(&bars[B_RAW_FULL + s], 1);
+            mbar_init(&bars[B_RAW_EMPTY + s], 128);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -168,269 +233,443 @@ __global__ void __launch_bounds__(Layout<D, Q8>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *s_tmem;
-    const uint32_t TM_S0 = tmem, TM_O = tmem + 256;
+    const uint32_t tmem = *s_tmem;  // S/P of tile x at column 128x, O of tile x at 256 + 128x
+    const int first_item = blockIdx.x, stride = gridDim.x;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- producer
+        // ------------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            if (QDT != KVC_IN_F32) {
-                mbar_arrive_expect_tx(&bars[B_QFULL], BM * D * 2);
-                for (int dh = 0; dh < D / 64; ++dh)
-                    tma_load_3d(sm + L::OFF_Q + dh * BM * 128, &tm_q, &bars[B_QFULL], dh * 64, h, r0);
-            }
-            for (int j = 0; j < n_tiles; ++j) {
-                if (Q8) {
-                    if (j > 0 && !mbar_wait(&bars[B_RAWEMPTY], (j - 1) & 1, s_abort)) break;
-                    mbar_arrive_expect_tx(&bars[B_RAWFULL], 2 * BN * D);
-                    tma_load_3d(sm + L::OFF_RAWK, &tm_k, &bars[B_RAWFULL], 0, j * BN, hkv);
-                    tma_load_3d(sm + L::OFF_RAWV, &tm_v, &bars[B_RAWFULL], 0, j * BN, hkv);
+            uint32_t ring_seq = 0, raw_seq = 0, q_seq = 0;
+            bool ok = true;
+            for (int i = first_item; ok && i < a.n_items; i += stride) {
+                const Item it = decode_item(a, i);
+                if (q_seq > 0 && !mbar_wait(&bars[B_QEMPTY], (q_seq - 1) & 1, s_abort)) break;
+                if (QDT != KVC_IN_F32) {
+                    mbar_arrive_expect_tx(&bars[B_QFULL], (it.has[1] ? 2 : 1) * L::QT_BYTES);
+                    for (int x = 0; x < 2; ++x) {
+                        if (!it.has[x]) continue;
+                        for (int dh = 0; dh < D / 64; ++dh)
+                            tma_load_3d(sm + L::OFF_Q + x * L::QT_BYTES + dh * BM * 128, &tm_q, &bars[B_QFULL],
+                                        dh * 64, it.h[x], it.qt[x] * BM);
+                    }
                 } else {
-                    const int st = j & 1;
-                    if (j >= 2 && !mbar_wait(&bars[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, s_abort)) break;
-                    mbar_arrive_expect_tx(&bars[B_KVFULL0 + st], 2 * BN * D * 2);
-                    for (int dh = 0; dh < D / 64; ++dh) {
-                        tma_load_3d(sm + L::OFF_K + st * L::KV_BYTES + dh * BN * 128, &tm_k,
-                                    &bars[B_KVFULL0 + st], dh * 64, j * BN, hkv);
-                        tma_load_3d(sm + L::OFF_V + st * L::KV_BYTES + dh * BN * 128, &tm_v,
-                                    &bars[B_KVFULL0 + st], dh * 64, j * BN, hkv);
+                    mbar_arrive(&bars[B_QFULL]);  // the softmax warps load f32 Q themselves
+                }
+                ++q_seq;
+                for (int k = it.k0; ok && k < it.k1; ++k) {
+                    for (int kv = 0; kv < 2 && ok; ++kv) {
+                        const CUtensorMap *m = kv ? &tm_v : &tm_k;
+                        if (Q8) {
+                            const int rs = raw_seq % L::NR;
+                            if (raw_seq >= (uint32_t)L::NR &&
+                                !mbar_wait(&bars[B_RAW_EMPTY + rs], ((raw_seq / L::NR) - 1) & 1, s_abort)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&bars[B_RAW_FULL + rs], L::RAW_BYTES);
+                            tma_load_3d(sm + L::OFF_RAW + rs * L::RAW_BYTES, m, &bars[B_RAW_FULL + rs], 0, k * BN,
+                                        it.g);
+                            ++raw_seq;
+                        } else {
+                            const int st = ring_seq % L::NS;
+                            if (ring_seq >= (uint32_t)L::NS &&
+                                !mbar_wait(&bars[B_RING_EMPTY + st], ((ring_seq / L::NS) - 1) & 1, s_abort)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&bars[B_RING_FULL + st], L::ST_BYTES);
+                            for (int dh = 0; dh < D / 64; ++dh)
+                                tma_load_3d(sm + L::OFF_RING + st * L::ST_BYTES + dh * BN * 128, m,
+                                            &bars[B_RING_FULL + st], dh * 64, k * BN, it.g);
+                            ++ring_seq;
+                        }
                     }
                 }
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
+        // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_f16(BM, BN, 0, 0);
             constexpr uint32_t IDESC_O = idesc_f16(BM, D, 0, 1);
-            const uint32_t sQ = smem_u32(sm + L::OFF_Q), sK = smem_u32(sm + L::OFF_K);
-            const uint32_t sV = smem_u32(sm + L::OFF_V), sP = smem_u32(sm + L::OFF_P);
-            auto issue_s = [&](int st) {
-                const uint32_t kb = sK + st * L::KV_BYTES;
+            const uint32_t sQ = smem_u32(sm + L::OFF_Q), sRing = smem_u32(sm + L::OFF_RING);
+            uint32_t ring_seq = 0, q_seq = 0, p_seq[2] = {0, 0}, ofree_seq[2] = {0, 0};
+            uint32_t pv_issued[2] = {0, 0}, pv_done[2] = {0, 0};
+            bool o_used[2] = {false, false};
+            bool ok = true;
+            auto ring_wait = [&](uint32_t seq) -> bool {
+                if (!mbar_wait(&bars[B_RING_FULL + seq % L::NS], (seq / L::NS) & 1, s_abort)) return false;
+                tc_fence_after();
+                return true;
+            };
+            // S_x and P_x share TMEM columns: before S_x overwrites them, the PV MMA that reads P_x must be
+            // complete (its o_done phase; the softmax group waits on the same phases independently)
+            auto pv_drain = [&](int x) -> bool {
+                while (pv_done[x] < pv_issued[x]) {
+                    if (!mbar_wait(&bars[B_ODONE0 + x], pv_done[x] & 1, s_abort)) return false;
+                    ++pv_done[x];
+                }
+                tc_fence_after();
+                return true;
+            };
+            auto issue_s = [&](int x, uint32_t seq) -> bool {
+                if (!pv_drain(x)) return false;
+                const uint32_t kb = sRing + (seq % L::NS) * L::ST_BYTES;
+                const uint32_t qb = sQ + x * L::QT_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-                    umma_f16_ss(TM_S0 + st * BN, sdesc_sw128(sQ + off, 16, 1024),
-                                sdesc_sw128(kb + off, 16, 1024), IDESC_S, ks > 0);
+                    umma_f16_ss(tmem + 128 * x, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                                IDESC_S, ks > 0);
                 }
+                umma_commit(&bars[B_SFULL0 + x]);
+                return true;
             };
-            auto issue_o = [&](int st, bool acc) {
-                const uint32_t vb = sV + st * L::KV_BYTES;
+            // O_x += P_x V: P_x from TMEM (fp16 packed in the S columns), V MN-major in the ring stage
+            auto issue_pv = [&](int x, uint32_t seq, bool acc) {
+                const uint32_t vb = sRing + (seq % L::NS) * L::ST_BYTES;
 #pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks) {
-                    const uint64_t ad = sdesc_sw128(sP + (ks >> 2) * (BM * 128) + (ks & 3) * 32, 16, 1024);
-                    // V tile [key][d]: MN-major; next 64 d's at +BN*128 bytes, next 8 keys at +1024
-                    const uint64_t bd = sdesc_sw128(vb + ks * 16 * 128, BN * 128, 1024);
-                    umma_f16_ss(TM_O, ad, bd, IDESC_O, (acc || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    umma_f16_ts(tmem + 256 + 128 * x, tmem + 128 * x + ks * 8,
+                                sdesc_sw128(vb + ks * 16 * 128, BN * 128, 1024), IDESC_O, (acc || ks > 0) ? 1u : 0u);
+                umma_commit(&bars[B_ODONE0 + x]);
+                ++pv_issued[x];
             };
-            bool ok = mbar_wait(&bars[B_QREADY], 0, s_abort) && mbar_wait(&bars[B_KVFULL0], 0, s_abort);
-            if (ok) {
+            for (int i = first_item; ok && i < a.n_items; i += stride) {
+                const Item it = decode_item(a, i);
+                if (!mbar_wait(&bars[B_QREADY], q_seq & 1, s_abort)) break;
+                ++q_seq;
                 tc_fence_after();
-                issue_s(0);
-                umma_commit(&bars[B_SFULL0]);
-                for (int j = 0; j < n_tiles; ++j) {
-                    if (j + 1 < n_tiles) {
-                        const int st = (j + 1) & 1;
-                        if (!mbar_wait(&bars[B_KVFULL0 + st], ((j + 1) >> 1) & 1, s_abort)) break;
-                        tc_fence_after();
-                        issue_s(st);
-                        umma_commit(&bars[B_SFULL0 + st]);
+                bool first_pv[2] = {true, true};
+                const uint32_t kseq = ring_seq++;
+                if (!ring_wait(kseq)) break;
+                for (int x = 0; x < 2 && ok; ++x)
+                    if (tile_active(it, x, it.k0) && !issue_s(x, kseq)) ok = false;
+                if (!ok) break;
+                umma_commit(&bars[B_RING_EMPTY + kseq % L::NS]);
+                // per key tile: PV_A(k), S_A(k+1), PV_B(k), S_B(k+1)
+                for (int k = it.k0; ok && k < it.k1; ++k) {
+                    const uint32_t vseq = ring_seq++;
+                    if (!ring_wait(vseq)) { ok = false; break; }
+                    const bool more = k + 1 < it.k1;
+                    uint32_t kseq_next = 0;
+                    if (more) kseq_next = ring_seq++;
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (tile_active(it, x, k)) {
+                            if (first_pv[x] && o_used[x]) {
+                                if (!mbar_wait(&bars[B_OFREE0 + x], ofree_seq[x] & 1, s_abort)) { ok = false; break; }
+                                ++ofree_seq[x];
+                            }
+                            if (!mbar_wait(&bars[B_PFULL0 + x], p_seq[x] & 1, s_abort)) { ok = false; break; }
+                            ++p_seq[x];
+                            tc_fence_after();
+                            issue_pv(x, vseq, !first_pv[x]);
+                            first_pv[x] = false;
+                            o_used[x] = true;
+                        }
+                        if (more) {
+                            if (x == 0 && !ring_wait(kseq_next)) { ok = false; break; }
+                            if (tile_active(it, x, k + 1) && !issue_s(x, kseq_next)) { ok = false; break; }
+                        }
                     }
-                    if (!mbar_wait(&bars[B_PFULL], j & 1, s_abort)) break;
-                    tc_fence_after();
-                    issue_o(j & 1, j > 0);
-                    umma_commit(&bars[B_KVEMPTY0 + (j & 1)]);
-                    umma_commit(&bars[B_ODONE]);
+                    if (!ok) break;
+                    umma_commit(&bars[B_RING_EMPTY + vseq % L::NS]);
+                    if (more) umma_commit(&bars[B_RING_EMPTY + kseq_next % L::NS]);
                 }
+                umma_commit(&bars[B_QEMPTY]);
             }
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------------------------------------- softmax
-        const int r = threadIdx.x - 128;                 // query row in the tile = TMEM lane
-        const int t = t_first + r;                       // its absolute position
-        const bool valid = r < rows;
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------------ softmax (tile x = A or B)
+        const int x = (warp - 4) >> 2;
+        const int r = threadIdx.x - 128 - 128 * x;  // row in the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        uint8_t *sQp = sm + L::OFF_Q;
+        const uint32_t tS = tmem + 128 * x + lane_base, tO = tmem + 256 + 128 * x + lane_base;
+        uint8_t *sQx = sm + L::OFF_Q + x * L::QT_BYTES;
+        uint32_t q_seq = 0, s_seq = 0, o_seq = 0, epi_seq = 0;
         bool ok = true;
-        if (QDT == KVC_IN_F32) {
-            const float *src = a.q_f32 + ((int64_t)(r0 + r) * a.n_head_q + h) * D;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 8; ++cc) {
-                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-                if (valid) {
-                    x0 = __ldg(reinterpret_cast<const float4 *>(src + cc * 8));
-                    x1 = __ldg(reinterpret_cast<const float4 *>(src + cc * 8 + 4));
-                }
-                uint4 o = make_uint4(pack_half2(x0.x, x0.y), pack_half2(x0.z, x0.w),
-                                     pack_half2(x1.x, x1.y), pack_half2(x1.z, x1.w));
-                *reinterpret_cast<uint4 *>(sQp + op_off(BM, r, cc)) = o;
-            }
-        } else {
-            ok = mbar_wait(&bars[B_QFULL], 0, s_abort);
-            if (ok && QDT == KVC_IN_BF16) {
-#pragma unroll 1
-                for (int cc = 0; cc < D / 8; ++cc) {
-                    uint4 *p = reinterpret_cast<uint4 *>(sQp + op_off(BM, r, cc));
-                    uint4 v = *p;
-                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w[i] = pack_half2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-                    *p = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[B_QREADY]);
-
-        float m_ref = -INFINITY, l = 0.f;
         const float sl2 = a.scale_log2;
-        uint8_t *sPp = sm + L::OFF_P;
+        // rendezvous of the 256 softmax threads (bounded, unlike bar.sync)
+        auto meet = [&]() -> bool {
+            mbar_arrive(&bars[B_EPI]);
+            const bool r = mbar_wait(&bars[B_EPI], epi_seq & 1, s_abort);
+            ++epi_seq;
+            return r;
+        };
+        for (int i = first_item; ok && i < a.n_items; i += stride) {
+            const Item it = decode_item(a, i);
+            if (!mbar_wait(&bars[B_QFULL], q_seq & 1, s_abort)) break;
+            ++q_seq;
+            const int row = it.qt[x] * BM + r;   // row within the chunk
+            const bool valid = it.has[x] && row < a.C;
+            const int t = it.tf[x] + r;          // absolute position
+            if (it.has[x]) {
+                if (QDT == KVC_IN_F32) {
+                    const float *src = a.q_f32 + ((int64_t)row * a.H_q + it.h[x]) * D;
 #pragma unroll 1
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            const int st = j & 1;
-            if (!mbar_wait(&bars[B_SFULL0 + st], (j >> 1) & 1, s_abort)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t s_addr = TM_S0 + st * BN + lane_base;
-            const int key0 = j * BN;
-            const bool need_mask = key0 + BN - 1 > t_first;
-            // pass 1: row max of the scaled, masked scores
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t s[32];
-                tmem_ld32(s_addr + c * 32, s);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float x = __uint_as_float(s[i]) * sl2;
-                    if (need_mask && key0 + c * 32 + i > t) x = -INFINITY;
-                    mx = fmaxf(mx, x);
-                }
-            }
-            const float m_new = fmaxf(m_ref, mx);
-            float m_use = m_ref, alpha = 1.f;
-            if (j == 0) {
-                m_use = m_new;  // key 0 is visible to every row, so m_new is finite
-            } else if (m_new > m_ref + RESCALE_LOG2) {
-                m_use = m_new;
-                alpha = ex2(m_ref - m_new);
-            }
-            // pass 2: probabilities (fp16) and their sum
-            uint32_t pk[BN / 2];
-            float rs = 0.f;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t s[32];
-                tmem_ld32(s_addr + c * 32, s);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float x0 = __uint_as_float(s[i]) * sl2, x1 = __uint_as_float(s[i + 1]) * sl2;
-                    if (need_mask && key0 + c * 32 + i > t) x0 = -INFINITY;
-                    if (need_mask && key0 + c * 32 + i + 1 > t) x1 = -INFINITY;
-                    const float p0 = ex2(x0 - m_use), p1 = ex2(x1 - m_use);
-                    rs += p0 + p1;
-                    pk[c * 16 + i / 2] = pack_half2(p0, p1);
-                }
-            }
-            l = l * alpha + rs;
-            if (j > 0) {
-                // the PV MMA of the previous tile must be done: O is rescaled and P rewritten
-                if (!mbar_wait(&bars[B_ODONE], (j - 1) & 1, s_abort)) { ok = false; break; }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(TM_O + lane_base + c * 32, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(TM_O + lane_base + c * 32, o);
+                    for (int cc = 0; cc < D / 8; ++cc) {
+                        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+                        if (valid) {
+                            x0 = __ldg(reinterpret_cast<const float4 *>(src + cc * 8));
+                            x1 = __ldg(reinterpret_cast<const float4 *>(src + cc * 8 + 4));
+                        }
+                        *reinterpret_cast<uint4 *>(sQx + op_off(BM, r, cc)) =
+                            make_uint4(pack_half2(x0.x, x0.y), pack_half2(x0.z, x0.w), pack_half2(x1.x, x1.y),
+                                       pack_half2(x1.z, x1.w));
                     }
-                    tmem_st_wait();
+                } else if (QDT == KVC_IN_BF16) {
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 8; ++cc) {
+                        uint4 *p = reinterpret_cast<uint4 *>(sQx + op_off(BM, r, cc));
+                        uint4 v = *p;
+                        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+                        *p = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
                 }
             }
-#pragma unroll
-            for (int cc = 0; cc < BN / 8; ++cc)
-                *reinterpret_cast<uint4 *>(sPp + op_off(BM, r, cc)) =
-                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars[B_PFULL]);
-            m_ref = m_use;
-        }
-        if (ok && mbar_wait(&bars[B_ODONE], (n_tiles - 1) & 1, s_abort)) {
-            tc_fence_after();
+            mbar_arrive(&bars[B_QREADY]);
+
+            float m_ref = -INFINITY, l = 0.f;
+            bool any = false;
+            for (int k = it.k0; k < it.k1; ++k) {
+                if (!tile_active(it, x, k)) continue;
+                if (!mbar_wait(&bars[B_SFULL0 + x], s_seq & 1, s_abort)) { ok = false; break; }
+                ++s_seq;
+                tc_fence_after();
+                const int key0 = k * BN;
+                const bool need_mask = key0 + BN - 1 > it.tf[x];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t s[32];
+                    tmem_ld32(tS + c * 32, s);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float v = (need_mask && key0 + c * 32 + e > t) ? -INFINITY : __uint_as_float(s[e]);
+                        mx = fmaxf(mx, v);
+                    }
+                }
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                float m_use = m_ref, alpha = 1.f;
+                if (!any) {
+                    m_use = m_new;  // the first visible tile of a row holds a visible key
+                } else if (m_new > m_ref + RESCALE_LOG2) {
+                    m_use = m_new;
+                    alpha = ex2(m_ref - m_new);
+                }
+                // a row that sees no key in this tile keeps m_use = -inf only if it saw none before either
+                const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t s[32];
+                    tmem_ld32(tS + c * 32, s);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -m_sub));
+                        float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -m_sub));
+                        if (need_mask && key0 + c * 32 + e > t) p0 = 0.f;
+                        if (need_mask && key0 + c * 32 + e + 1 > t) p1 = 0.f;
+                        rs += p0 + p1;
+                        pk[e / 2] = pack_half2(p0, p1);
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                l = l * alpha + rs;
+                if (any) {
+                    if (!mbar_wait(&bars[B_ODONE0 + x], o_seq & 1, s_abort)) { ok = false; break; }
+                    ++o_seq;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c * 32, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + c * 32, o);
+                        }
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars[B_PFULL0 + x]);
+                any = true;
+                m_ref = m_use;
+            }
+            if (!ok) break;
+            // ---- epilogue: this item's O for my row (or zeros when no tile of the item reached it)
+            if (any) {
+                if (!mbar_wait(&bars[B_ODONE0 + x], o_seq & 1, s_abort)) { ok = false; break; }
+                ++o_seq;
+                tc_fence_after();
+            }
+            const int pg = it.g * a.J + it.j;
+            float *part_row = a.part + ((((int64_t)pg * a.smax + it.s) * 2 + x) * BM + r) * PART_ROW(D);
+            float *out_row = a.out + ((int64_t)row * a.H_q + it.h[x]) * D;
             const float inv = 1.f / l;
-            float *dst = a.out + ((int64_t)(r0 + r) * a.n_head_q + h) * D;
+            if (it.has[x]) {
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(TM_O + lane_base + c * 32, o);
-                tmem_ld_wait();
-                if (valid) {
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    if (any) {
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_ld_wait();
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4 *>(dst + c * 32 + i) =
-                            make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                                        __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
+                    if (it.ns == 1) {
+                        if (valid) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                *reinterpret_cast<float4 *>(out_row + c * 32 + e) =
+                                    make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                                __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4 *>(part_row + c * 32 + e) =
+                                make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
+                                            __uint_as_float(o[e + 3]));
+                    }
+                }
+                if (it.ns > 1) {
+                    part_row[D] = any ? m_ref : -INFINITY;
+                    part_row[D + 1] = l;
+                }
+            }
+            if (any) {
+                tc_fence_before();
+                mbar_arrive(&bars[B_OFREE0 + x]);
+            }
+            if (it.ns > 1) {
+                // the last item of the pair to finish merges the splits in split order
+                __threadfence();
+                if (!meet()) { ok = false; break; }
+                if (threadIdx.x == 128) {
+                    const int old = atomicAdd(&a.tickets[pg], 1);
+                    *s_last = (old == it.ns - 1) ? 1 : 0;
+                }
+                if (!meet()) { ok = false; break; }
+                if (*s_last) {
+                    __threadfence();
+                    if (it.has[x]) {
+                        const float *base = a.part + (((int64_t)pg * a.smax) * 2 + x) * BM * PART_ROW(D) + (int64_t)r * PART_ROW(D);
+                        const int64_t sstride = 2 * BM * PART_ROW(D);
+                        float M = -INFINITY;
+                        for (int s = 0; s < it.ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride + D));
+                        float Lsum = 0.f;
+                        for (int s = 0; s < it.ns; ++s) {
+                            const float ms = __ldcg(base + s * sstride + D);
+                            const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
+                            Lsum += w * __ldcg(base + s * sstride + D + 1);
+                        }
+                        const float inv_l = 1.f / Lsum;
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            float acc[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                            for (int s = 0; s < it.ns; ++s) {
+                                const float ms = __ldcg(base + s * sstride + D);
+                                const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
+                                const float4 *src = reinterpret_cast<const float4 *>(base + s * sstride + c * 32);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float4 v = __ldcg(src + e);
+                                    acc[4 * e] += w * v.x;
+                                    acc[4 * e + 1] += w * v.y;
+                                    acc[4 * e + 2] += w * v.z;
+                                    acc[4 * e + 3] += w * v.w;
+                                }
+                            }
+                            if (valid) {
+#pragma unroll
+                                for (int e = 0; e < 32; e += 4)
+                                    *reinterpret_cast<float4 *>(out_row + c * 32 + e) =
+                                        make_float4(acc[e] * inv_l, acc[e + 1] * inv_l, acc[e + 2] * inv_l,
+                                                    acc[e + 3] * inv_l);
+                            }
+                        }
+                    }
+                    if (threadIdx.x == 128) atomicExch(&a.tickets[pg], 0);
                 }
             }
         }
-    } else if (Q8 && warp >= 8) {
-        // ---------------------------------------------------------------- dequantise
-        const int r = threadIdx.x - 256;  // key row in the tile
+    } else if (Q8 && warp >= 12) {
+        // ------------------------------------------------------------------ dequantise
+        const int r = threadIdx.x - 384;  // key row in the tile
         constexpr int NB = D / 32;
-        const uint8_t *rawk = sm + L::OFF_RAWK, *rawv = sm + L::OFF_RAWV;
-#pragma unroll 1
-        for (int j = 0; j < n_tiles; ++j) {
-            const int key = j * BN + r;
-            uint16_t sk[NB], sv[NB];
-            const int64_t soff = a.layer * a.g.s_layer + (int64_t)key * a.g.s_tok + hkv * a.g.s_head;
+        uint32_t raw_seq = 0, ring_seq = 0;
+        bool ok = true;
+        for (int i = first_item; ok && i < a.n_items; i += stride) {
+            const Item it = decode_item(a, i);
+            for (int k = it.k0; ok && k < it.k1; ++k) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int key = k * BN + r;
+                    const uint16_t *sp = (kv ? a.vs : a.ks) + a.layer * a.g.s_layer + (int64_t)key * a.g.s_tok +
+                                         it.g * a.g.s_head;
+                    uint32_t sw[NB / 2];
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                sk[b] = key < a.kv_len ? __ldg(a.ks + soff + b) : (uint16_t)0;
-                sv[b] = key < a.kv_len ? __ldg(a.vs + soff + b) : (uint16_t)0;
-            }
-            if (!mbar_wait(&bars[B_RAWFULL], j & 1, s_abort)) break;
-            uint4 rk[D / 16], rv[D / 16];
+                    for (int b = 0; b < NB / 2; ++b) sw[b] = 0u;
+                    if (key < a.kv_len) {
+                        if (NB == 4) {
+                            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(sp));
+                            sw[0] = u.x;
+                            sw[NB / 2 - 1] = u.y;
+                        } else {
+                            sw[0] = __ldg(reinterpret_cast<const uint32_t *>(sp));
+                        }
+                    }
+                    const int rs = raw_seq % L::NR;
+                    if (!mbar_wait(&bars[B_RAW_FULL + rs], (raw_seq / L::NR) & 1, s_abort)) { ok = false; break; }
+                    const uint8_t *raw = sm + L::OFF_RAW + rs * L::RAW_BYTES;
+                    uint4 rr[D / 16];
 #pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-                const uint32_t off = (D == 128) ? sw128(r, c) : sw64(r, c);
-                rk[c] = *reinterpret_cast<const uint4 *>(rawk + off);
-                rv[c] = *reinterpret_cast<const uint4 *>(rawv + off);
-            }
-            mbar_arrive(&bars[B_RAWEMPTY]);
-            const int st = j & 1;
-            if (j >= 2 && !mbar_wait(&bars[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, s_abort)) break;
-            uint8_t *dk = sm + L::OFF_K + st * L::KV_BYTES;
-            uint8_t *dv = sm + L::OFF_V + st * L::KV_BYTES;
+                    for (int c = 0; c < D / 16; ++c)
+                        rr[c] = *reinterpret_cast<const uint4 *>(raw + ((D == 128) ? sw128(r, c) : sw64(r, c)));
+                    // order these generic-proxy reads before the TMA (async proxy) that refills the stage
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+                    ++raw_seq;
+                    const int st = ring_seq % L::NS;
+                    if (ring_seq >= (uint32_t)L::NS &&
+                        !mbar_wait(&bars[B_RING_EMPTY + st], ((ring_seq / L::NS) - 1) & 1, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = sm + L::OFF_RING + st * L::ST_BYTES;
 #pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-                const __half2 k2 = __halves2half2(__ushort_as_half(sk[c >> 1]), __ushort_as_half(sk[c >> 1]));
-                const __half2 v2 = __halves2half2(__ushort_as_half(sv[c >> 1]), __ushort_as_half(sv[c >> 1]));
-                uint32_t ko[8], vo[8];
-                dequant4(rk[c].x, k2, ko[0], ko[1]);
-                dequant4(rk[c].y, k2, ko[2], ko[3]);
-                dequant4(rk[c].z, k2, ko[4], ko[5]);
-                dequant4(rk[c].w, k2, ko[6], ko[7]);
-                dequant4(rv[c].x, v2, vo[0], vo[1]);
-                dequant4(rv[c].y, v2, vo[2], vo[3]);
-                dequant4(rv[c].z, v2, vo[4], vo[5]);
-                dequant4(rv[c].w, v2, vo[6], vo[7]);
-                *reinterpret_cast<uint4 *>(dk + op_off(BN, r, 2 * c)) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
-                *reinterpret_cast<uint4 *>(dk + op_off(BN, r, 2 * c + 1)) = make_uint4(ko[4], ko[5], ko[6], ko[7]);
-                *reinterpret_cast<uint4 *>(dv + op_off(BN, r, 2 * c)) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
-                *reinterpret_cast<uint4 *>(dv + op_off(BN, r, 2 * c + 1)) = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+                    for (int c = 0; c < D / 16; ++c) {
+                        const int b = c >> 1;
+                        const unsigned short sb = (unsigned short)(sw[b >> 1] >> (16 * (b & 1)));
+                        const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
+                        uint32_t o[8];
+                        dequant4(rr[c].x, d2, o[0], o[1]);
+                        dequant4(rr[c].y, d2, o[2], o[3]);
+                        dequant4(rr[c].z, d2, o[4], o[5]);
+                        dequant4(rr[c].w, d2, o[6], o[7]);
+                        *reinterpret_cast<uint4 *>(dst + op_off(BN, r, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(dst + op_off(BN, r, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[B_RING_FULL + st]);
+                    ++ring_seq;
+                }
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars[B_KVFULL0 + st]);
         }
     }
 
@@ -450,7 +689,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     std::call_once(once, [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     });
@@ -470,10 +710,64 @@ bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
                sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 148;
+    });
+    return n;
+}
+
+// The work decomposition of one call (see the file comment).
+struct Plan {
+    int G, n_qt, U, J, ST, smax, n_items;
+    int cum[MAX_SPLITS + 1], jmin[MAX_SPLITS];
+    size_t ticket_bytes, part_bytes;
+};
+
+int split_tiles(int n_ctx) {
+    int keys = 1;
+    while (keys * 2 <= n_ctx / 4) keys *= 2;
+    if (keys < 4096) keys = 4096;
+    if (keys > 16384) keys = 16384;
+    return keys / BN;
+}
+
+bool make_plan(const kvc_desc &d, int n_head_q, int pos0, int C, Plan &p) {
+    p.G = n_head_q / d.n_head_kv;
+    p.n_qt = (C + BM - 1) / BM;
+    p.U = p.n_qt * p.G;
+    p.J = (p.U + 1) / 2;
+    p.ST = split_tiles(d.n_ctx);
+    auto T = [&](int j) {
+        const int e = (2 * j + 1 < p.U) ? 2 * j + 1 : p.U - 1;
+        const int qt = e / p.G;
+        const int tl = pos0 + ((qt * BM + BM < C) ? qt * BM + BM : C) - 1;
+        return tl / BN + 1;
+    };
+    p.smax = (T(p.J - 1) + p.ST - 1) / p.ST;
+    if (p.smax > MAX_SPLITS) return false;
+    p.cum[0] = 0;
+    int j = 0;
+    for (int s = 0; s < p.smax; ++s) {
+        while (j < p.J && T(j) <= s * p.ST) ++j;
+        p.jmin[s] = j;
+        p.cum[s + 1] = p.cum[s] + (p.J - j) * d.n_head_kv;
+    }
+    p.n_items = p.cum[p.smax];
+    p.ticket_bytes = ((size_t)d.n_head_kv * p.J * sizeof(int) + 255) / 256 * 256;
+    p.part_bytes = (p.smax > 1) ? (size_t)d.n_head_kv * p.J * p.smax * 2 * BM * PART_ROW(d.head_dim) * sizeof(float) : 0;
+    return true;
+}
+
 template <int D, bool Q8, int QDT>
 int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int n_head_q, float *out,
-             cudaStream_t s) {
-    using L = Layout<D, Q8>;
+             void *scratch, const Plan &p, cudaStream_t s) {
+    using L = Cfg<D, Q8>;
     const Geom g = geom_of(c.d);
     const int H = c.d.n_head_kv, kv_len = pos0 + n;
     CUtensorMap tq, tk, tv;
@@ -506,15 +800,25 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     a.ks = static_cast<const uint16_t *>(c.k_s);
     a.vs = static_cast<const uint16_t *>(c.v_s);
     a.out = out;
+    a.tickets = static_cast<int *>(scratch);
+    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + p.ticket_bytes);
     a.g = g;
     a.layer = layer;
     a.pos0 = pos0;
-    a.n_rows = n;
+    a.C = n;
     a.kv_len = kv_len;
-    a.n_head_q = n_head_q;
-    a.group = n_head_q / H;
-    a.n_qtiles = (n + BM - 1) / BM;
+    a.H_q = n_head_q;
+    a.G = p.G;
+    a.H_kv = H;
+    a.n_qt = p.n_qt;
+    a.U = p.U;
+    a.J = p.J;
+    a.ST = p.ST;
+    a.smax = p.smax;
+    a.n_items = p.n_items;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
+    for (int i = 0; i <= MAX_SPLITS; ++i) a.cum[i] = i <= p.smax ? p.cum[i] : p.n_items;
+    for (int i = 0; i < MAX_SPLITS; ++i) a.jmin[i] = i < p.smax ? p.jmin[i] : p.J;
     auto kern = prefill_kernel<D, Q8, QDT>;
     static bool attr_set = false;  // per instantiation
     if (!attr_set) {
@@ -522,32 +826,42 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
             return KVC_ECUDA;
         attr_set = true;
     }
-    dim3 grid(a.n_qtiles, n_head_q);
+    const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
     kern<<<grid, L::THREADS, L::ALLOC, s>>>(tq, tk, tv, a);
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 
 template <int D, bool Q8>
 int launch_d(const kvc_cache &c, int layer, int pos0, int n, const void *q, int dtype, int n_head_q,
-             float *out, cudaStream_t s) {
+             float *out, void *scratch, const Plan &p, cudaStream_t s) {
     switch (dtype) {
-        case KVC_IN_F32: return launch_t<D, Q8, KVC_IN_F32>(c, layer, pos0, n, q, n_head_q, out, s);
-        case KVC_IN_BF16: return launch_t<D, Q8, KVC_IN_BF16>(c, layer, pos0, n, q, n_head_q, out, s);
-        default: return launch_t<D, Q8, KVC_IN_F16>(c, layer, pos0, n, q, n_head_q, out, s);
+        case KVC_IN_F32: return launch_t<D, Q8, KVC_IN_F32>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s);
+        case KVC_IN_BF16: return launch_t<D, Q8, KVC_IN_BF16>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s);
+        default: return launch_t<D, Q8, KVC_IN_F16>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s);
     }
 }
 
 }  // namespace
 
+size_t prefill_scratch_bytes(const kvc_desc &d, int n_head_q, int max_tokens) {
+    // the largest plan over chunk positions: pairs grow with the chunk, splits with the context
+    Plan p;
+    if (!make_plan(d, n_head_q, d.n_ctx - max_tokens, max_tokens, p)) return 0;
+    return p.ticket_bytes + p.part_bytes;
+}
+
 int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, int dtype,
-                   int n_head_q, float *out, cudaStream_t s) {
+                   int n_head_q, float *out, void *scratch, size_t scratch_bytes, cudaStream_t s) {
     if (n_tokens == 0) return KVC_OK;
+    Plan p;
+    if (!make_plan(c.d, n_head_q, pos0, n_tokens, p)) return KVC_EINVAL;
+    if (p.ticket_bytes + p.part_bytes > scratch_bytes) return KVC_ENOSPC;
     const bool q8 = c.d.type == KVC_Q8_0;
     if (c.d.head_dim == 128)
-        return q8 ? launch_d<128, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, s)
-                  : launch_d<128, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, s);
-    return q8 ? launch_d<64, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, s)
-              : launch_d<64, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, s);
+        return q8 ? launch_d<128, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s)
+                  : launch_d<128, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s);
+    return q8 ? launch_d<64, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s)
+              : launch_d<64, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s);
 }
 
 int read_and_clear_device_status(int32_t *status) {

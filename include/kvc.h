@@ -127,18 +127,32 @@ int kvc_cache_init(kvc_cache *out, const kvc_desc *desc, void *k_q, void *k_s, v
 int kv_cache_append(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens,
                     const void *k, const void *v, int32_t dtype, kvc_stream_t stream);
 
+/* Bytes of the scratch buffer prefill_chunk_attn needs for chunks of up to
+ * max_tokens rows anywhere in this cache: a ticket per work pair and float32
+ * partial results of the key splits.  The buffer must be zero-filled once
+ * before its first use; every call leaves its tickets at zero again (after a
+ * call whose kernel gave up a bounded wait, zero it again). */
+int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t max_tokens, size_t *bytes);
+
 /* Causal attention of a chunk's query rows over the cache:
  *   out[i][h] = sum_{j <= pos0+i} softmax_j(q[i][h] . khat[j][h/G] / sqrt(head_dim)) vhat[j][h/G]
  * for i in [0, n_tokens), G = n_head_q / n_head_kv, khat/vhat the values the
  * cache holds for `layer` at positions [0, pos0 + n_tokens).  The chunk's own
  * K/V must have been appended (kv_cache_append earlier on the same stream).
- * Rows are independent of how the prompt is cut into chunks.  Computed with
- * fp16 tensor-core products and float32 accumulation and softmax.
+ * Keys are processed in tiles of 128 and splits whose boundaries sit at
+ * absolute positions (a size fixed by n_ctx); partial results of a row are
+ * merged in split order, so a row's output is bitwise independent of how the
+ * prompt is cut into chunks.  Computed with fp16 tensor-core products and
+ * float32 accumulation and softmax.
  * q: [n_tokens][n_head_q][head_dim] in dtype (f32, bf16 or f16); out float32.
- * Errors: KVC_EINVAL (null, dtype, head_dim not 64/128, heads), KVC_ERANGE. */
+ * scratch: device buffer of scratch_bytes >= kvc_prefill_scratch_bytes(desc,
+ * n_head_q, n_tokens), zero-filled before its first use; calls on one scratch
+ * buffer must not overlap on the GPU.
+ * Errors: KVC_EINVAL (null, dtype, head_dim not 64/128, heads), KVC_ERANGE,
+ * KVC_ENOSPC (scratch too small). */
 int prefill_chunk_attn(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens,
-                       const void *q, int32_t dtype, int32_t n_head_q, float *out,
-                       kvc_stream_t stream);
+                       const void *q, int32_t dtype, int32_t n_head_q, float *out, void *scratch,
+                       size_t scratch_bytes, kvc_stream_t stream);
 
 /* Single-token decode attention at position pos: the formula above with one
  * query row at pos, keys [0, pos].  The token's K/V must have been appended.

@@ -33,8 +33,8 @@ def declared_functions():
 def test_header_declares_the_path():
     names = declared_functions()
     for n in ["kv_cache_append", "prefill_chunk_attn", "decode_attn", "kv_state_get", "kv_state_set",
-              "kv_state_size", "kvc_cache_bytes", "kvc_scratch_bytes", "kvc_cache_init", "kvc_strerror",
-              "kvc_device_status"]:
+              "kv_state_size", "kvc_cache_bytes", "kvc_scratch_bytes", "kvc_prefill_scratch_bytes",
+              "kvc_cache_init", "kvc_strerror", "kvc_device_status"]:
         assert n in names
 
 
@@ -106,9 +106,11 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, 0, 4, k, k, 9, S) == kvc.KVC_EINVAL
     assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, 0, 4, None, k, 1, S) == kvc.KVC_EINVAL
     assert kvc.lib.kv_cache_append(ctypes.byref(c), 0, 10, 0, None, None, 1, S) == kvc.KVC_OK  # empty: no-op
-    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 60, 5, k, 1, 4, k, S) == kvc.KVC_ERANGE
-    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 0, 5, k, 1, 3, k, S) == kvc.KVC_EINVAL
-    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 3, 0, None, 1, 4, None, S) == kvc.KVC_OK
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 60, 5, k, 1, 4, k, k, 1 << 30, S) == kvc.KVC_ERANGE
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 0, 5, k, 1, 3, k, k, 1 << 30, S) == kvc.KVC_EINVAL
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 0, 5, k, 1, 4, k, None, 1 << 30, S) == kvc.KVC_EINVAL
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 0, 5, k, 1, 4, k, k, 16, S) == kvc.KVC_ENOSPC
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 3, 0, None, 1, 4, None, None, 0, S) == kvc.KVC_OK
     assert kvc.lib.decode_attn(ctypes.byref(c), 0, 64, k, 1, 4, k, k, 1 << 20, S) == kvc.KVC_ERANGE
     assert kvc.lib.decode_attn(ctypes.byref(c), 0, 5, k, 1, 4, k, k, 100, S) == kvc.KVC_ENOSPC
     assert kvc.lib.decode_attn(ctypes.byref(c), 0, 5, k, 1, 36, k, k, 1 << 24, S) == kvc.KVC_EINVAL  # G = 18 > 16
@@ -119,7 +121,23 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     c96 = kvc.kvc_cache()
     d96 = kvc.make_desc(1, 64, 2, 96, "f16")
     assert kvc.lib.kvc_cache_init(ctypes.byref(c96), ctypes.byref(d96), k, None, k, None) == kvc.KVC_OK
-    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c96), 0, 0, 5, k, 1, 4, k, S) == kvc.KVC_EINVAL
+    assert kvc.lib.prefill_chunk_attn(ctypes.byref(c96), 0, 0, 5, k, 1, 4, k, k, 1 << 30, S) == kvc.KVC_EINVAL
+
+
+def test_prefill_scratch_query(kvc):
+    out = ctypes.c_size_t()
+    d = kvc.make_desc(1, 65536, 8, 128, "q8_0")
+    assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(d), 40, 2048, ctypes.byref(out)) == kvc.KVC_OK
+    big = out.value
+    # 8 kv groups x 40 pairs x 4 splits x 2 tiles x 128 rows x 130 floats, plus tickets
+    assert big >= 8 * 40 * 4 * 2 * 128 * 130 * 4
+    assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(d), 40, 512, ctypes.byref(out)) == kvc.KVC_OK
+    assert out.value < big
+    small = kvc.make_desc(1, 512, 2, 64, "q8_0")
+    assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 4, 64, ctypes.byref(out)) == kvc.KVC_OK
+    assert 0 < out.value <= 4096   # one split: tickets only
+    assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 4, 513, ctypes.byref(out)) == kvc.KVC_ERANGE
+    assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 3, 64, ctypes.byref(out)) == kvc.KVC_EINVAL
 
 
 def test_strerror(kvc):

@@ -23,9 +23,10 @@ def gpu_prefill(kvc, w, layout, chunk, layer=0, qkv=None):
     q, k, v = qkv if qkv is not None else si.layer_qkv(w, layer)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     out = torch.empty(w.n_prompt, w.n_head_q, w.head_dim, device="cuda")
+    scratch = g.prefill_scratch(w.n_head_q, chunk if chunk > 0 else w.n_prompt)  # reused by every chunk
     for p, c in w.chunks(chunk):
         kvc.kv_cache_append(g, layer, p, kd[p:p + c], vd[p:p + c])
-        kvc.prefill_chunk_attn(g, layer, p, qd[p:p + c], out=out[p:p + c])
+        kvc.prefill_chunk_attn(g, layer, p, qd[p:p + c], out=out[p:p + c], scratch=scratch)
     torch.cuda.synchronize()
     return g, out
 
@@ -66,6 +67,8 @@ def test_prefill_chunk_and_layout_invariance(kvc):
     w = si.small_workload("inv", 10, 2, 128, "q8_0", "bf16", n_prompt=700, chunk=0, n_decode=0, seed=21)
     qkv = si.layer_qkv(w, 0)
     _, whole = gpu_prefill(kvc, w, "head_major", 0, qkv=qkv)
+    for _ in range(3):  # repeat runs: the result must be deterministic
+        assert torch.equal(gpu_prefill(kvc, w, "layer_major", 0, qkv=qkv)[1], whole)
     for chunk in (1, 37, 128, 300):
         for layout in ("head_major", "layer_major"):
             if chunk == 1 and layout == "layer_major":
@@ -92,4 +95,25 @@ def test_prefill_other_layer_and_repeatability(kvc):
     assert torch.equal(a, b)
     _, ref = oracle_prefill(w, 150, layer=1, qkv=qkv)
     assert_close(a.cpu().numpy(), ref)
+    assert kvc.kvc_device_status() == 0
+
+
+def test_prefill_key_splits_merge_and_stay_chunk_invariant(kvc):
+    # 9,000 keys: the splits (4,096 keys at this context size) are merged in split order; rows of one
+    # chunking and another must agree bit for bit, and sampled rows must match the oracle
+    w = si.small_workload("split", 10, 2, 128, "q8_0", "bf16", n_prompt=9000, chunk=1024, n_decode=0, seed=31,
+                          k_outlier_frac=0.01)
+    qkv = si.layer_qkv(w, 0)
+    _, a = gpu_prefill(kvc, w, "head_major", 1024, qkv=qkv)
+    for chunk, layout in ((3000, "layer_major"), (1024, "head_major"), (0, "head_major"), (257, "layer_major")):
+        _, b = gpu_prefill(kvc, w, layout, chunk, qkv=qkv)
+        assert torch.equal(a, b), "chunk %d %s" % (chunk, layout)
+    o = OracleCache(1, w.n_ctx, w.n_head_kv, w.head_dim, w.cache)
+    q, k, v = qkv
+    o.append(0, 0, np32(k[:w.n_prompt]), np32(v[:w.n_prompt]))
+    rows = si.sample_rows(5, w.chunks(1024))
+    kh, vh = o.dequantized(0, w.n_prompt)
+    from oracle.attention import attend
+    ref = attend(np32(q[rows]), rows, kh, vh)
+    assert_close(a[rows].cpu().numpy(), ref, "sampled rows")
     assert kvc.kvc_device_status() == 0
