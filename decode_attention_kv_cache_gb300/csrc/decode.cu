@@ -348,26 +348,56 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodeAr
     }
 }
 
+// One CTA per query head, one thread per output value.  The split maxima and
+// weights are computed once per CTA in shared memory; each thread then sums its
+// value over the splits in split order (independent loads, unrolled).
 template <int D>
-__global__ void decode_combine_kernel(const float *__restrict__ part, int n_split, int group,
-                                      int n_head_kv, float *__restrict__ out) {
+__global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ part, int n_split,
+                                                           int group, int n_head_kv, float *__restrict__ out) {
+    __shared__ float s_w[MAX_SPLIT];
+    __shared__ float s_red[D / 32];
+    __shared__ float s_M, s_L;
     const int h = blockIdx.x, d = threadIdx.x;
     const int hkv = h / group, row = h % group;
     const float *part_o = part;
     const float *part_ml = part + (int64_t)n_head_kv * MAX_SPLIT * group * D;
-    float M = -INFINITY;
-    for (int i = 0; i < n_split; ++i)
-        M = fmaxf(M, part_ml[(((int64_t)hkv * MAX_SPLIT + i) * group + row) * 2]);
-    float acc = 0.f, l = 0.f;
-    for (int i = 0; i < n_split; ++i) {
-        const int64_t pi = ((int64_t)hkv * MAX_SPLIT + i) * group + row;
-        const float m = part_ml[pi * 2];
-        if (m == -INFINITY) continue;
-        const float f = ptx::ex2(m - M);
-        acc += f * part_o[pi * D + d];
-        l += f * part_ml[pi * 2 + 1];
+    const int64_t p0 = ((int64_t)hkv * MAX_SPLIT) * group + row;   // partial index of split 0
+    // maximum over splits
+    float m = -INFINITY;
+    for (int i = d; i < n_split; i += D) m = fmaxf(m, part_ml[(p0 + (int64_t)i * group) * 2]);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((d & 31) == 0) s_red[d >> 5] = m;
+    __syncthreads();
+    if (d == 0) {
+        float M = s_red[0];
+        for (int w = 1; w < D / 32; ++w) M = fmaxf(M, s_red[w]);
+        s_M = M;
     }
-    out[(int64_t)h * D + d] = acc / l;
+    __syncthreads();
+    const float M = s_M;
+    // split weights; the sum of weighted softmax denominators in split order
+    for (int i = d; i < n_split; i += D) {
+        const float mi = part_ml[(p0 + (int64_t)i * group) * 2];
+        s_w[i] = (mi == -INFINITY) ? 0.f : ptx::ex2(mi - M);
+    }
+    __syncthreads();
+    if (d == 0) {
+        float L = 0.f;
+        for (int i = 0; i < n_split; ++i) L += s_w[i] * part_ml[(p0 + (int64_t)i * group) * 2 + 1];
+        s_L = L;
+    }
+    float acc = 0.f;
+    int i = 0;
+    for (; i + 8 <= n_split; i += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = part_o[(p0 + (int64_t)(i + u) * group) * D + d];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc += s_w[i + u] * v[u];
+    }
+    for (; i < n_split; ++i) acc += s_w[i] * part_o[(p0 + (int64_t)i * group) * D + d];
+    __syncthreads();
+    out[(int64_t)h * D + d] = acc / s_L;
 }
 
 int sm_count() {

@@ -80,6 +80,14 @@ struct Cfg {
     static constexpr int USED = OFF_BAR + 512;
     static constexpr int ALLOC = (USED + 1024 > 122880) ? USED + 1024 : 122880;  // one CTA per SM
     static constexpr int THREADS = Q8 ? 512 : 384;
+    // registers per thread: at launch (65536 / THREADS, multiple of 8), then per warpgroup after
+    // setmaxnreg; sum over warpgroups of 128 * regs must not exceed THREADS * LAUNCH_REGS
+    static constexpr int LAUNCH_REGS = Q8 ? 128 : 168;
+    static constexpr int WG0_REGS = 112;                    // producer, MMA issuer, two idle warps
+    static constexpr int DQ_REGS = 88;                      // dequantising warpgroup (q8_0)
+    static constexpr int SM_REGS = Q8 ? 152 : 192;          // each softmax warpgroup
+    static_assert(128 * WG0_REGS + 256 * SM_REGS + (Q8 ? 128 * DQ_REGS : 0) <= THREADS * LAUNCH_REGS,
+                  "register split exceeds the launch allocation");
 };
 
 enum Bar {
@@ -236,6 +244,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     const uint32_t tmem = *s_tmem;  // S/P of tile x at column 128x, O of tile x at 256 + 128x
     const int first_item = blockIdx.x, stride = gridDim.x;
 
+    if (warp < 4) setmaxnreg_dec<L::WG0_REGS>();  // producer, MMA issuer and two idle warps
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
         if (lane == 0) {
@@ -314,15 +323,17 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 tc_fence_after();
                 return true;
             };
+            // S_x = Q_x K^T.  P_x (fp16, packed) occupies the first 64 columns of the S_x region, so the PV
+            // MMA that reads P_x must be complete before S_x is overwritten.
             auto issue_s = [&](int x, uint32_t seq) -> bool {
-                if (!pv_drain(x)) return false;
                 const uint32_t kb = sRing + (seq % L::NS) * L::ST_BYTES;
                 const uint32_t qb = sQ + x * L::QT_BYTES;
+                if (!pv_drain(x)) return false;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-                    umma_f16_ss(tmem + 128 * x, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                                IDESC_S, ks > 0);
+                    umma_f16_ss(tmem + 128 * x, sdesc_sw128(qb + off, 16, 1024),
+                                sdesc_sw128(kb + off, 16, 1024), IDESC_S, ks > 0);
                 }
                 umma_commit(&bars[B_SFULL0 + x]);
                 return true;
@@ -384,6 +395,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         __syncwarp();
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------------ softmax (tile x = A or B)
+        setmaxnreg_inc<L::SM_REGS>();
         const int x = (warp - 4) >> 2;
         const int r = threadIdx.x - 128 - 128 * x;  // row in the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -403,12 +415,15 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             const Item it = decode_item(a, i);
             if (!mbar_wait(&bars[B_QFULL], q_seq & 1, s_abort)) break;
             ++q_seq;
-            const int row = it.qt[x] * BM + r;   // row within the chunk
-            const bool valid = it.has[x] && row < a.C;
-            const int t = it.tf[x] + r;          // absolute position
-            if (it.has[x]) {
+            const bool has_x = x ? it.has[1] : it.has[0];
+            const int qt_x = x ? it.qt[1] : it.qt[0], h_x = x ? it.h[1] : it.h[0];
+            const int tf_x = x ? it.tf[1] : it.tf[0], tl_x = x ? it.tl[1] : it.tl[0];
+            const int row = qt_x * BM + r;       // row within the chunk
+            const bool valid = has_x && row < a.C;
+            const int t = tf_x + r;              // absolute position
+            if (has_x) {
                 if (QDT == KVC_IN_F32) {
-                    const float *src = a.q_f32 + ((int64_t)row * a.H_q + it.h[x]) * D;
+                    const float *src = a.q_f32 + ((int64_t)row * a.H_q + h_x) * D;
 #pragma unroll 1
                     for (int cc = 0; cc < D / 8; ++cc) {
                         float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
@@ -439,24 +454,30 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             float m_ref = -INFINITY, l = 0.f;
             bool any = false;
             for (int k = it.k0; k < it.k1; ++k) {
-                if (!tile_active(it, x, k)) continue;
+                if (!has_x || k * BN > tl_x) continue;  // tile_active(it, x, k)
                 if (!mbar_wait(&bars[B_SFULL0 + x], s_seq & 1, s_abort)) { ok = false; break; }
                 ++s_seq;
                 tc_fence_after();
                 const int key0 = k * BN;
-                const bool need_mask = key0 + BN - 1 > it.tf[x];
-                float mx = -INFINITY;
+                const bool need_mask = key0 + BN - 1 > tf_x;
+                // the whole S row in registers (one TMEM round trip), masked keys set to -inf
+                uint32_t s[BN];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t s[32];
-                    tmem_ld32(tS + c * 32, s);
-                    tmem_ld_wait();
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32p(tS + c * 32, s + c * 32);
+                tmem_ld_wait();
+                if (need_mask) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float v = (need_mask && key0 + c * 32 + e > t) ? -INFINITY : __uint_as_float(s[e]);
-                        mx = fmaxf(mx, v);
-                    }
+                    for (int e = 0; e < BN; ++e)
+                        if (key0 + e > t) s[e] = 0xFF800000u;
                 }
+                // row max: 8 independent chains, then a tree (max is exact in any order)
+                float mx8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+#pragma unroll
+                for (int e = 8; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(s[e]));
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 float m_use = m_ref, alpha = 1.f;
                 if (!any) {
@@ -465,26 +486,23 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                     m_use = m_new;
                     alpha = ex2(m_ref - m_new);
                 }
-                // a row that sees no key in this tile keeps m_use = -inf only if it saw none before either
+                // -inf scores give p = 0 exactly; a row with no visible key so far uses 0 as its offset
                 const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-                float rs = 0.f;
+                // probabilities; the row sum in 8 independent partial sums, added in a fixed order
+                float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t s[32];
-                    tmem_ld32(tS + c * 32, s);
-                    tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -m_sub));
-                        float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -m_sub));
-                        if (need_mask && key0 + c * 32 + e > t) p0 = 0.f;
-                        if (need_mask && key0 + c * 32 + e + 1 > t) p1 = 0.f;
-                        rs += p0 + p1;
+                        const float p0 = ex2(fmaf(__uint_as_float(s[c * 32 + e]), sl2, -m_sub));
+                        const float p1 = ex2(fmaf(__uint_as_float(s[c * 32 + e + 1]), sl2, -m_sub));
+                        rs8[(e >> 1) & 7] += p0 + p1;
                         pk[e / 2] = pack_half2(p0, p1);
                     }
                     tmem_st16(tS + c * 16, pk);
                 }
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
                 l = l * alpha + rs;
                 if (any) {
                     if (!mbar_wait(&bars[B_ODONE0 + x], o_seq & 1, s_abort)) { ok = false; break; }
@@ -517,9 +535,9 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             }
             const int pg = it.g * a.J + it.j;
             float *part_row = a.part + ((((int64_t)pg * a.smax + it.s) * 2 + x) * BM + r) * PART_ROW(D);
-            float *out_row = a.out + ((int64_t)row * a.H_q + it.h[x]) * D;
+            float *out_row = a.out + ((int64_t)row * a.H_q + h_x) * D;
             const float inv = 1.f / l;
-            if (it.has[x]) {
+            if (has_x) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -566,7 +584,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 if (!meet()) { ok = false; break; }
                 if (*s_last) {
                     __threadfence();
-                    if (it.has[x]) {
+                    if (has_x) {
                         const float *base = a.part + (((int64_t)pg * a.smax) * 2 + x) * BM * PART_ROW(D) + (int64_t)r * PART_ROW(D);
                         const int64_t sstride = 2 * BM * PART_ROW(D);
                         float M = -INFINITY;
@@ -611,6 +629,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         }
     } else if (Q8 && warp >= 12) {
         // ------------------------------------------------------------------ dequantise
+        setmaxnreg_dec<L::DQ_REGS>();
         const int r = threadIdx.x - 384;  // key row in the tile
         constexpr int NB = D / 32;
         uint32_t raw_seq = 0, ring_seq = 0;
@@ -729,6 +748,8 @@ struct Plan {
     size_t ticket_bytes, part_bytes;
 };
 
+// Keys per split: a power of two near n_ctx/4, between 4096 and 16384.  It depends on the cache
+// only, never on the chunk, so a row meets the same split boundaries however the prompt is cut.
 int split_tiles(int n_ctx) {
     int keys = 1;
     while (keys * 2 <= n_ctx / 4) keys *= 2;
