@@ -150,32 +150,53 @@ def dist_max(x, world):
 
 # --------------------------------------------------------------------------- GPU arm
 class GpuRequest:
-    """Inputs resident in HBM (and pinned host copies for the end-to-end run), two caches, output buffers."""
+    """Inputs resident in HBM (and pinned host copies for the end-to-end run), two caches, output buffers.
 
-    def __init__(self, kvc, w, device, seed_offset):
+    Multi-layer stacks draw their inputs on the device (seeded_inputs.layer_qkv_device) and reuse one
+    prefill/decode output buffer for every layer (the layers of the attention-only stack share no data).
+    """
+
+    def __init__(self, kvc, w, device, seed_offset=0, device_inputs=None, host_copies=True, extra_rows=0,
+                 inputs=None):
         import torch
         self.torch, self.kvc, self.w, self.dev = torch, kvc, w, device
         wl = w if seed_offset == 0 else si.Workload(**{**w.__dict__, "seed": w.seed + 1000 * seed_offset})
         self.wl = wl
+        self.device_inputs = (w.n_layer > 1) if device_inputs is None else device_inputs
+        n_rows = w.n_tokens + extra_rows
         self.host, self.dev_in = [], []
         for layer in range(w.n_layer):
-            q, k, v = si.layer_qkv(wl, layer)
-            hq, hk, hv = (t.pin_memory() for t in (q, k, v))
-            self.host.append((hq, hk, hv))
-            self.dev_in.append(tuple(t.to(device) for t in (hq, hk, hv)))
+            if inputs is not None:           # caller-provided device tensors (one tuple per layer)
+                self.dev_in.append(inputs[layer])
+            elif self.device_inputs:
+                dq, dk, dv = si.layer_qkv_device(wl, layer, device, n_rows=n_rows)
+                self.dev_in.append((dq, dk, dv))
+                if host_copies:
+                    self.host.append(tuple(t.cpu().pin_memory() for t in (dq, dk, dv)))
+            else:
+                q, k, v = si.layer_qkv(wl, layer, n_rows=n_rows)
+                hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+                if host_copies:
+                    self.host.append((hq, hk, hv))
+                self.dev_in.append(tuple(t.to(device) for t in (hq, hk, hv)))
         self.src = kvc.KVCache(w.n_layer, w.n_ctx, w.n_head_kv, w.head_dim, w.cache, "head_major", device)
         self.dst = kvc.KVCache(w.n_layer, w.n_ctx, w.n_head_kv, w.head_dim, w.cache, "layer_major", device)
-        self.out_p = torch.empty(w.n_layer, w.n_prompt, w.n_head_q, w.head_dim, device=device)
-        self.out_d = torch.empty(w.n_layer, max(w.n_decode, 1), w.n_head_q, w.head_dim, device=device)
+        n_out = w.n_layer if w.n_layer == 1 else 1
+        self.out_p = torch.empty(n_out, w.n_prompt, w.n_head_q, w.head_dim, device=device)
+        self.out_d = torch.empty(n_out, max(w.n_decode, 1), w.n_head_q, w.head_dim, device=device)
         self.scratch = torch.empty(self.src.scratch_bytes(w.n_head_q), dtype=torch.uint8, device=device)
         self.pscratch = self.src.prefill_scratch(w.n_head_q, w.chunk if w.chunk > 0 else w.n_prompt)
         self.state = torch.empty(self.src.state_size(w.n_tokens), dtype=torch.uint8, device=device)
-        self.host_out_p = torch.empty(self.out_p.shape, dtype=torch.float32).pin_memory()
-        self.host_out_d = torch.empty(self.out_d.shape, dtype=torch.float32).pin_memory()
-        self.host_state = torch.empty(self.state.shape, dtype=torch.uint8).pin_memory()
+        if host_copies:
+            self.host_out_p = torch.empty(self.out_p.shape, dtype=torch.float32).pin_memory()
+            self.host_out_d = torch.empty(self.out_d.shape, dtype=torch.float32).pin_memory()
+            self.host_state = torch.empty(self.state.shape, dtype=torch.uint8).pin_memory()
         self.chunks = w.chunks()
         self.graphs = []
         self.flops = prefill_flops(w)
+
+    def out_slot(self, layer):
+        return layer if self.w.n_layer == 1 else 0
 
     def launches_per_step(self):
         w = self.w
@@ -187,7 +208,8 @@ class GpuRequest:
         for i in range(w.n_decode):
             pos = w.n_prompt + i
             kvc.kv_cache_append(self.src, layer, pos, k[pos:pos + 1], v[pos:pos + 1])
-            kvc.decode_attn(self.src, layer, pos, q[pos], out=self.out_d[layer, i], scratch=self.scratch)
+            kvc.decode_attn(self.src, layer, pos, q[pos], out=self.out_d[self.out_slot(layer), i],
+                            scratch=self.scratch)
 
     def capture(self):
         """Capture each layer's decode loop in a CUDA graph (after one eager run)."""
@@ -203,8 +225,9 @@ class GpuRequest:
             self.graphs.append(g)
         torch.cuda.synchronize()
 
-    def step(self, ev=None):
-        """One request on every layer.  ev: dict of event lists to record phase/launch times."""
+    def step(self, ev=None, on_layer=None):
+        """One request on every layer.  ev: dict of event lists to record phase/launch times;
+        on_layer(layer): called after each layer's prefill and decode (checks only, never timed)."""
         kvc, w, torch = self.kvc, self.w, self.torch
         E = torch.cuda.Event
         for layer in range(w.n_layer):
@@ -215,7 +238,7 @@ class GpuRequest:
                 kvc.kv_cache_append(self.src, layer, p, k[p:p + c], v[p:p + c])
                 if ev is not None:
                     a = E(enable_timing=True); a.record()
-                kvc.prefill_chunk_attn(self.src, layer, p, q[p:p + c], out=self.out_p[layer, p:p + c],
+                kvc.prefill_chunk_attn(self.src, layer, p, q[p:p + c], out=self.out_p[self.out_slot(layer), p:p + c],
                                        scratch=self.pscratch)
                 if ev is not None:
                     b = E(enable_timing=True); b.record(); ev["attn"].append((a, b, self.flops[ci]))
@@ -228,6 +251,8 @@ class GpuRequest:
                     self._decode_loop(layer)
             if ev is not None:
                 e2 = E(enable_timing=True); e2.record(); ev["decode"].append((e1, e2))
+            if on_layer is not None:
+                on_layer(layer)
         if ev is not None:
             e3 = E(enable_timing=True); e3.record()
         kvc.kv_state_get(self.src, w.n_tokens, dst=self.state)
@@ -238,6 +263,8 @@ class GpuRequest:
 
     def h2d(self):
         for (hq, hk, hv), (dq, dk, dv) in zip(self.host, self.dev_in):
+            # host inputs hold exactly the request's rows
+
             dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
 
     def d2h(self):
@@ -362,7 +389,7 @@ def run_gpu(args, rank, world, local):
 
 
 # --------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
-def oracle_sample(w, max_chunks=6, rows_per_chunk=4, decode_samples=3):
+def oracle_sample(w, max_chunks=16, rows_per_chunk=64, decode_samples=32):
     """Time the oracle on a bounded sample of one layer's request; extrapolate to the whole request.
 
     Appends (quantisation) of every token and the state pack/unpack are timed

@@ -142,6 +142,31 @@ def layer_qkv(w: Workload, layer: int, n_rows: Optional[int] = None):
     return to_input_dtype(q, w.in_dtype), to_input_dtype(k, w.in_dtype), to_input_dtype(v, w.in_dtype)
 
 
+def layer_qkv_device(w: Workload, layer: int, device, n_rows: Optional[int] = None):
+    """Q, K, V of one layer drawn on a CUDA device (torch's counter-based Philox generator), in w.in_dtype.
+
+    For large stacks where drawing on the host would take minutes.  The values
+    differ from layer_qkv's (another generator) but are just as seeded: the
+    same (seed, layer) always gives the same tensors, and a CPU copy of them is
+    what the oracle receives.  K outliers follow the same seeded channel choice.
+    """
+    import hashlib
+    n = w.n_tokens if n_rows is None else n_rows
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.in_dtype]
+    out = []
+    for tid, heads in ((Q_ID, w.n_head_q), (K_ID, w.n_head_kv), (V_ID, w.n_head_kv)):
+        key = int.from_bytes(hashlib.sha256(b"%d/%d/%d" % (w.seed, layer, tid)).digest()[:8], "little") >> 1
+        g = torch.Generator(device=device)
+        g.manual_seed(key)
+        x = torch.randn((n, heads, w.head_dim), generator=g, device=device, dtype=torch.float32)
+        if tid == K_ID:
+            ch = outlier_channels(w, layer)
+            if ch.size:
+                x.view(n, -1)[:, torch.from_numpy(ch).to(device)] *= 4.0
+        out.append(x.to(dt))
+    return tuple(out)
+
+
 def small_workload(name: str, n_head_q: int, n_head_kv: int, head_dim: int, cache: str,
                    in_dtype: str, n_prompt: int, chunk: int, n_decode: int, seed: int,
                    n_ctx: Optional[int] = None, n_layer: int = 1,
