@@ -780,7 +780,11 @@ bool make_plan(const kvc_desc &d, int n_head_q, int pos0, int C, Plan &p) {
         p.cum[s + 1] = p.cum[s] + (p.J - j) * d.n_head_kv;
     }
     p.n_items = p.cum[p.smax];
-    p.ticket_bytes = ((size_t)d.n_head_kv * p.J * sizeof(int) + 255) / 256 * 256;
+    // The ticket region is sized for the largest chunk the cache admits, not for this call: every call
+    // on one scratch buffer must agree on where the tickets end and the partials begin, or a short
+    // chunk's partials would overwrite the (zeroed) tickets of a longer one.
+    const int j_max = ((d.n_ctx + BM - 1) / BM * p.G + 1) / 2;
+    p.ticket_bytes = ((size_t)d.n_head_kv * j_max * sizeof(int) + 255) / 256 * 256;
     p.part_bytes = (p.smax > 1) ? (size_t)d.n_head_kv * p.J * p.smax * 2 * BM * PART_ROW(d.head_dim) * sizeof(float) : 0;
     return true;
 }
