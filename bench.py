@@ -199,8 +199,17 @@ class GpuRequest:
         return layer if self.w.n_layer == 1 else 0
 
     def launches_per_step(self):
+        """Kernels one step launches: per chunk an append and the attention, plus the split merge when
+        the chunk's last row reaches past the first key split (keys per split: the power of two near
+        n_ctx/4, clamped to [4096, 16384]); per decode step append, split pass and combine; the state
+        header, pack and unpack."""
         w = self.w
-        return w.n_layer * (2 * len(self.chunks) + 3 * w.n_decode) + 3
+        keys = 1
+        while keys * 2 <= w.n_ctx // 4:
+            keys *= 2
+        keys = min(max(keys, 4096), 16384)
+        merges = sum(1 for p, c in self.chunks if p + c - 1 >= keys)
+        return w.n_layer * (2 * len(self.chunks) + merges + 3 * w.n_decode) + 3
 
     def _decode_loop(self, layer):
         kvc, w = self.kvc, self.w

@@ -165,8 +165,8 @@ class KVCache:
         return n.value
 
     def prefill_scratch(self, n_head_q, max_tokens):
-        """A zero-filled prefill scratch buffer for chunks of up to max_tokens rows."""
-        return torch.zeros(max(self.prefill_scratch_bytes(n_head_q, max_tokens), 16), dtype=torch.uint8,
+        """A prefill scratch buffer for chunks of up to max_tokens rows (needs no initialisation)."""
+        return torch.empty(max(self.prefill_scratch_bytes(n_head_q, max_tokens), 16), dtype=torch.uint8,
                            device=self.device)
 
     def state_size(self, n_tokens):
@@ -184,7 +184,7 @@ def kv_cache_append(cache, layer, pos0, k, v, stream=None):
 def prefill_chunk_attn(cache, layer, pos0, q, out=None, scratch=None, stream=None):
     """Causal attention of chunk rows q [C, H_q, D] at positions [pos0, pos0 + C); returns out [C, H_q, D] f32.
 
-    scratch: a zero-filled uint8 CUDA buffer (KVCache.prefill_scratch); one is made when None.
+    scratch: a uint8 CUDA buffer (KVCache.prefill_scratch); one is made when None.
     """
     _need(q, "q")
     if out is None:

@@ -16,10 +16,12 @@
 // are cut at ABSOLUTE split boundaries of ST tiles (ST is fixed by the cache
 // size): an item is (pair, split).  Persistent CTAs (one per SM) take items
 // round-robin.  An item whose pair has one split writes the output directly;
-// otherwise it writes its partial (O, running max, sum) and the last item of
-// the pair to finish merges the partials in split order.  Because tiles and
-// splits sit at absolute positions and every merge runs in split order, a
-// row's result does not depend on how the prompt is cut into chunks.
+// otherwise it writes its partial (O, running max, sum), and a second, fully
+// parallel kernel merges the partials of each row in split order (merging
+// inside the persistent kernel left the merging SM's tensor pipe idle).
+// Because tiles and splits sit at absolute positions and every merge runs in
+// split order, a row's result does not depend on how the prompt is cut into
+// chunks.
 //
 // One CTA:
 //   warp 0      TMA producer: the two Q tiles of an item, then K and V tiles
@@ -92,7 +94,7 @@ struct Cfg {
 
 enum Bar {
     B_QFULL, B_QREADY, B_QEMPTY, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ODONE0, B_ODONE1,
-    B_OFREE0, B_OFREE1, B_EPI, B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
+    B_OFREE0, B_OFREE1, B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
     B_RAW_EMPTY = B_RAW_FULL + 8, NBAR = B_RAW_EMPTY + 8
 };
 
@@ -102,7 +104,6 @@ struct Args {
     const uint16_t *vs;
     float *out;
     float *part;      // partials [pair][split][tile][row][PART_ROW]
-    int *tickets;     // [pair]
     Geom g;
     int layer, pos0, C, kv_len, H_q, G, H_kv, n_qt, U, J, ST, smax, n_items;
     float scale_log2;
@@ -208,7 +209,6 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
-    volatile int *s_last = reinterpret_cast<volatile int *>(s_tmem + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -223,7 +223,6 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             mbar_init(&bars[B_ODONE0 + x], 1);
             mbar_init(&bars[B_OFREE0 + x], 128);
         }
-        mbar_init(&bars[B_EPI], 256);
         for (int s = 0; s < L::NS; ++s) {
             mbar_init(&bars[B_RING_FULL + s], Q8 ? 128 : 1);
             mbar_init(&bars[B_RING_EMPTY + s], 1);
@@ -401,16 +400,9 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + 128 * x + lane_base, tO = tmem + 256 + 128 * x + lane_base;
         uint8_t *sQx = sm + L::OFF_Q + x * L::QT_BYTES;
-        uint32_t q_seq = 0, s_seq = 0, o_seq = 0, epi_seq = 0;
+        uint32_t q_seq = 0, s_seq = 0, o_seq = 0;
         bool ok = true;
         const float sl2 = a.scale_log2;
-        // rendezvous of the 256 softmax threads (bounded, unlike bar.sync)
-        auto meet = [&]() -> bool {
-            mbar_arrive(&bars[B_EPI]);
-            const bool r = mbar_wait(&bars[B_EPI], epi_seq & 1, s_abort);
-            ++epi_seq;
-            return r;
-        };
         for (int i = first_item; ok && i < a.n_items; i += stride) {
             const Item it = decode_item(a, i);
             if (!mbar_wait(&bars[B_QFULL], q_seq & 1, s_abort)) break;
@@ -573,59 +565,6 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(&bars[B_OFREE0 + x]);
             }
-            if (it.ns > 1) {
-                // the last item of the pair to finish merges the splits in split order
-                __threadfence();
-                if (!meet()) { ok = false; break; }
-                if (threadIdx.x == 128) {
-                    const int old = atomicAdd(&a.tickets[pg], 1);
-                    *s_last = (old == it.ns - 1) ? 1 : 0;
-                }
-                if (!meet()) { ok = false; break; }
-                if (*s_last) {
-                    __threadfence();
-                    if (has_x) {
-                        const float *base = a.part + (((int64_t)pg * a.smax) * 2 + x) * BM * PART_ROW(D) + (int64_t)r * PART_ROW(D);
-                        const int64_t sstride = 2 * BM * PART_ROW(D);
-                        float M = -INFINITY;
-                        for (int s = 0; s < it.ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride + D));
-                        float Lsum = 0.f;
-                        for (int s = 0; s < it.ns; ++s) {
-                            const float ms = __ldcg(base + s * sstride + D);
-                            const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
-                            Lsum += w * __ldcg(base + s * sstride + D + 1);
-                        }
-                        const float inv_l = 1.f / Lsum;
-#pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            float acc[32];
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-                            for (int s = 0; s < it.ns; ++s) {
-                                const float ms = __ldcg(base + s * sstride + D);
-                                const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
-                                const float4 *src = reinterpret_cast<const float4 *>(base + s * sstride + c * 32);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const float4 v = __ldcg(src + e);
-                                    acc[4 * e] += w * v.x;
-                                    acc[4 * e + 1] += w * v.y;
-                                    acc[4 * e + 2] += w * v.z;
-                                    acc[4 * e + 3] += w * v.w;
-                                }
-                            }
-                            if (valid) {
-#pragma unroll
-                                for (int e = 0; e < 32; e += 4)
-                                    *reinterpret_cast<float4 *>(out_row + c * 32 + e) =
-                                        make_float4(acc[e] * inv_l, acc[e + 1] * inv_l, acc[e + 2] * inv_l,
-                                                    acc[e + 3] * inv_l);
-                            }
-                        }
-                    }
-                    if (threadIdx.x == 128) atomicExch(&a.tickets[pg], 0);
-                }
-            }
         }
     } else if (Q8 && warp >= 12) {
         // ------------------------------------------------------------------ dequantise
@@ -701,6 +640,49 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     }
 }
 
+// Merge of the key splits: out = sum_s w_s O_s / sum_s w_s l_s, w_s = 2^(m_s - max_s m_s), the
+// splits taken in split order (a split with no visible key has m_s = -inf and weight 0).  A group
+// of D/4 threads per row, 4 columns each; a block covers 256 / (D/4) rows of one Q tile of a pair.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
+    constexpr int TPR = D / 4, RPB = 256 / TPR, BPT = BM / RPB;
+    const int rb = blockIdx.x % BPT, x = (blockIdx.x / BPT) & 1, pg = blockIdx.x / (2 * BPT);
+    const int g = pg / a.J, j = pg % a.J;
+    const int e = 2 * j + x;
+    if (e >= a.U) return;
+    // the pair's split count, as decode_item computes it
+    const int e_last = (2 * j + 1 < a.U) ? 2 * j + 1 : 2 * j;
+    const int T = unit_tl(a, e_last / a.G) / BN + 1;
+    const int ns = (T + a.ST - 1) / a.ST;
+    if (ns <= 1) return;
+    const int qt = e / a.G, h = g * a.G + e % a.G;
+    const int r = rb * RPB + threadIdx.x / TPR, c4 = (threadIdx.x % TPR) * 4;
+    const int row = qt * BM + r;
+    if (row >= a.C) return;
+    const int64_t sstride = 2 * BM * PART_ROW(D);
+    const float *base = a.part + (((int64_t)pg * a.smax * 2 + x) * BM + r) * PART_ROW(D);
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcs(base + s * sstride + D));
+    float Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) {
+        const float *ps = base + s * sstride;
+        const float ms = __ldcs(ps + D), ls = __ldcs(ps + D + 1);
+        const float4 v = __ldcs(reinterpret_cast<const float4 *>(ps + c4));
+        const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
+        Lsum += w * ls;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+    }
+    const float inv_l = 1.f / Lsum;
+    *reinterpret_cast<float4 *>(a.out + ((int64_t)row * a.H_q + h) * D + c4) =
+        make_float4(acc.x * inv_l, acc.y * inv_l, acc.z * inv_l, acc.w * inv_l);
+}
+
 // ---- host side ----------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -745,7 +727,7 @@ int sm_count() {
 struct Plan {
     int G, n_qt, U, J, ST, smax, n_items;
     int cum[MAX_SPLITS + 1], jmin[MAX_SPLITS];
-    size_t ticket_bytes, part_bytes;
+    size_t part_bytes;
 };
 
 // Keys per split: a power of two near n_ctx/4, between 4096 and 16384.  It depends on the cache
@@ -780,14 +762,12 @@ bool make_plan(const kvc_desc &d, int n_head_q, int pos0, int C, Plan &p) {
         p.cum[s + 1] = p.cum[s] + (p.J - j) * d.n_head_kv;
     }
     p.n_items = p.cum[p.smax];
-    // The ticket region is sized for the largest chunk the cache admits, not for this call: every call
-    // on one scratch buffer must agree on where the tickets end and the partials begin, or a short
-    // chunk's partials would overwrite the (zeroed) tickets of a longer one.
-    const int j_max = ((d.n_ctx + BM - 1) / BM * p.G + 1) / 2;
-    p.ticket_bytes = ((size_t)d.n_head_kv * j_max * sizeof(int) + 255) / 256 * 256;
     p.part_bytes = (p.smax > 1) ? (size_t)d.n_head_kv * p.J * p.smax * 2 * BM * PART_ROW(d.head_dim) * sizeof(float) : 0;
     return true;
 }
+
+// the documented scratch size: the partials, at least 256 bytes
+size_t scratch_need(const Plan &p) { return p.part_bytes > 256 ? p.part_bytes : 256; }
 
 template <int D, bool Q8, int QDT>
 int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int n_head_q, float *out,
@@ -825,8 +805,7 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     a.ks = static_cast<const uint16_t *>(c.k_s);
     a.vs = static_cast<const uint16_t *>(c.v_s);
     a.out = out;
-    a.tickets = static_cast<int *>(scratch);
-    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + p.ticket_bytes);
+    a.part = static_cast<float *>(scratch);
     a.g = g;
     a.layer = layer;
     a.pos0 = pos0;
@@ -853,6 +832,10 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     }
     const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
     kern<<<grid, L::THREADS, L::ALLOC, s>>>(tq, tk, tv, a);
+    if (p.smax > 1) {
+        constexpr int BPT = BM / (256 / (D / 4));
+        prefill_merge_kernel<D><<<H * p.J * 2 * BPT, 256, 0, s>>>(a);
+    }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 
@@ -872,7 +855,7 @@ size_t prefill_scratch_bytes(const kvc_desc &d, int n_head_q, int max_tokens) {
     // the largest plan over chunk positions: pairs grow with the chunk, splits with the context
     Plan p;
     if (!make_plan(d, n_head_q, d.n_ctx - max_tokens, max_tokens, p)) return 0;
-    return p.ticket_bytes + p.part_bytes;
+    return scratch_need(p);
 }
 
 int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, int dtype,
@@ -880,7 +863,7 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
     if (n_tokens == 0) return KVC_OK;
     Plan p;
     if (!make_plan(c.d, n_head_q, pos0, n_tokens, p)) return KVC_EINVAL;
-    if (p.ticket_bytes + p.part_bytes > scratch_bytes) return KVC_ENOSPC;
+    if (scratch_need(p) > scratch_bytes) return KVC_ENOSPC;
     const bool q8 = c.d.type == KVC_Q8_0;
     if (c.d.head_dim == 128)
         return q8 ? launch_d<128, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s)

@@ -128,10 +128,9 @@ int kv_cache_append(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t
                     const void *k, const void *v, int32_t dtype, kvc_stream_t stream);
 
 /* Bytes of the scratch buffer prefill_chunk_attn needs for chunks of up to
- * max_tokens rows anywhere in this cache: a ticket per work pair and float32
- * partial results of the key splits.  The buffer must be zero-filled once
- * before its first use; every call leaves its tickets at zero again (after a
- * call whose kernel gave up a bounded wait, zero it again). */
+ * max_tokens rows anywhere in this cache: the float32 partial results
+ * (output row, running max, sum) of the key splits, at least 256 bytes.  The
+ * contents need no initialisation; every call writes what it reads. */
 int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t max_tokens, size_t *bytes);
 
 /* Causal attention of a chunk's query rows over the cache:
@@ -145,8 +144,10 @@ int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t ma
  * prompt is cut into chunks.  Computed with fp16 tensor-core products and
  * float32 accumulation and softmax.
  * q: [n_tokens][n_head_q][head_dim] in dtype (f32, bf16 or f16); out float32.
- * scratch: device buffer of scratch_bytes >= kvc_prefill_scratch_bytes(desc,
- * n_head_q, n_tokens), zero-filled before its first use; calls on one scratch
+ * Two kernels on `stream`: the attention (partials of rows whose keys span
+ * several splits go to scratch) and, when any row has several splits, the
+ * merge.  scratch: device buffer of scratch_bytes >=
+ * kvc_prefill_scratch_bytes(desc, n_head_q, n_tokens); calls on one scratch
  * buffer must not overlap on the GPU.
  * Errors: KVC_EINVAL (null, dtype, head_dim not 64/128, heads), KVC_ERANGE,
  * KVC_ENOSPC (scratch too small). */

@@ -129,13 +129,13 @@ def test_prefill_scratch_query(kvc):
     d = kvc.make_desc(1, 65536, 8, 128, "q8_0")
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(d), 40, 2048, ctypes.byref(out)) == kvc.KVC_OK
     big = out.value
-    # 8 kv groups x 40 pairs x 4 splits x 2 tiles x 128 rows x 130 floats, plus tickets
+    # 8 kv groups x 40 pairs x 4 splits x 2 tiles x 128 rows x 130 floats
     assert big >= 8 * 40 * 4 * 2 * 128 * 130 * 4
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(d), 40, 512, ctypes.byref(out)) == kvc.KVC_OK
     assert out.value < big
     small = kvc.make_desc(1, 512, 2, 64, "q8_0")
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 4, 64, ctypes.byref(out)) == kvc.KVC_OK
-    assert 0 < out.value <= 4096   # one split: tickets only
+    assert out.value == 256        # one split: no partials, the minimum size
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 4, 513, ctypes.byref(out)) == kvc.KVC_ERANGE
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 3, 64, ctypes.byref(out)) == kvc.KVC_EINVAL
 

@@ -120,8 +120,8 @@ def test_prefill_key_splits_merge_and_stay_chunk_invariant(kvc):
 
 
 def test_scratch_reused_after_a_short_chunk(kvc):
-    # the tickets of a scratch buffer must survive a call with fewer work pairs: run a short chunk,
-    # then long chunks with key splits on the same scratch, and compare with a fresh scratch
+    # a scratch buffer reused across calls with different work shapes (a short chunk, then long
+    # chunks with key splits) gives the results of a fresh buffer filled with garbage
     w = si.small_workload("reuse", 10, 2, 128, "f16", "bf16", n_prompt=9000, chunk=1024, n_decode=0, seed=41)
     q, k, v = (t.cuda() for t in si.layer_qkv(w, 0))
     g = kvc.KVCache(1, w.n_ctx, w.n_head_kv, w.head_dim, w.cache, "head_major")
@@ -130,5 +130,6 @@ def test_scratch_reused_after_a_short_chunk(kvc):
     kvc.prefill_chunk_attn(g, 0, 8900, q[8900:9000], scratch=shared)          # short chunk, key splits
     for p in (6000, 7000, 7976):
         a = kvc.prefill_chunk_attn(g, 0, p, q[p:p + 1024], scratch=shared)
-        b = kvc.prefill_chunk_attn(g, 0, p, q[p:p + 1024], scratch=g.prefill_scratch(w.n_head_q, 1024))
+        fresh = g.prefill_scratch(w.n_head_q, 1024).fill_(0xA5)
+        b = kvc.prefill_chunk_attn(g, 0, p, q[p:p + 1024], scratch=fresh)
         assert torch.equal(a, b), "chunk at %d" % p
