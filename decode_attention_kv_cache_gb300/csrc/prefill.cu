@@ -33,6 +33,9 @@
 //               shared-memory operand), interleaved as
 //               PV_A(k), S_A(k+1), PV_B(k), S_B(k+1) so each softmax has two
 //               MMAs' time to turn S into P.
+//   warps 2-3   put the two Q tiles in fp16 (bf16 converted in place, f32 read
+//               from global memory); Q is released after the item's last S MMAs,
+//               so the next item's Q is loaded and converted during this one's tail.
 //   warps 4-7   softmax of Q tile A, warps 8-11 of Q tile B: thread r owns row r
 //               (TMEM lane r): row max, exp2, fp16 P written back over S in
 //               tensor memory, O rescaled in TMEM only when the running max
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     if (threadIdx.x == 0) {
         *s_abort = 0;
         mbar_init(&bars[B_QFULL], 1);
-        mbar_init(&bars[B_QREADY], 256);
+        mbar_init(&bars[B_QREADY], 64);
         mbar_init(&bars[B_QEMPTY], 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&bars[B_SFULL0 + x], 1);
@@ -359,6 +362,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                     if (tile_active(it, x, it.k0) && !issue_s(x, kseq)) ok = false;
                 if (!ok) break;
                 umma_commit(&bars[B_RING_EMPTY + kseq % L::NS]);
+                // Q is free once the item's last S MMAs complete: the next item's Q loads during this one's tail
+                if (it.k0 + 1 == it.k1) umma_commit(&bars[B_QEMPTY]);
                 // per key tile: PV_A(k), S_A(k+1), PV_B(k), S_B(k+1)
                 for (int k = it.k0; ok && k < it.k1; ++k) {
                     const uint32_t vseq = ring_seq++;
@@ -387,11 +392,52 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                     if (!ok) break;
                     umma_commit(&bars[B_RING_EMPTY + vseq % L::NS]);
                     if (more) umma_commit(&bars[B_RING_EMPTY + kseq_next % L::NS]);
+                    if (more && k + 2 == it.k1) umma_commit(&bars[B_QEMPTY]);
                 }
-                umma_commit(&bars[B_QEMPTY]);
             }
         }
         __syncwarp();
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------------------------ Q operand (fp16, swizzled)
+        // bf16 Q (TMA-loaded) is converted in place; f32 Q is read from global memory; f16 needs nothing.
+        constexpr int CPR = D / 8;             // 16-byte chunks per row
+        constexpr int RPI = 32 / CPR;          // rows per warp and iteration
+        const int cc = lane % CPR, r_off = (warp - 2) * RPI + lane / CPR;
+        uint32_t q_seq = 0;
+        for (int i = first_item; i < a.n_items; i += stride) {
+            const Item it = decode_item(a, i);
+            if (!mbar_wait(&bars[B_QFULL], q_seq & 1, s_abort)) break;
+            ++q_seq;
+            for (int x = 0; x < 2; ++x) {
+                if (!it.has[x] || QDT == KVC_IN_F16) continue;
+                uint8_t *sQx = sm + L::OFF_Q + x * L::QT_BYTES;
+#pragma unroll 4
+                for (int r = r_off; r < BM; r += 2 * RPI) {
+                    uint4 *p = reinterpret_cast<uint4 *>(sQx + op_off(BM, r, cc));
+                    if (QDT == KVC_IN_F32) {
+                        const int row = it.qt[x] * BM + r;
+                        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+                        if (row < a.C) {
+                            const float *src = a.q_f32 + ((int64_t)row * a.H_q + it.h[x]) * D + cc * 8;
+                            x0 = __ldg(reinterpret_cast<const float4 *>(src));
+                            x1 = __ldg(reinterpret_cast<const float4 *>(src + 4));
+                        }
+                        *p = make_uint4(pack_half2(x0.x, x0.y), pack_half2(x0.z, x0.w), pack_half2(x1.x, x1.y),
+                                        pack_half2(x1.z, x1.w));
+                    } else {
+                        const uint4 v = *p;
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            o[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+                        *p = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[B_QREADY]);
+        }
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------------ softmax (tile x = A or B)
         setmaxnreg_inc<L::SM_REGS>();
@@ -399,49 +445,17 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         const int r = threadIdx.x - 128 - 128 * x;  // row in the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + 128 * x + lane_base, tO = tmem + 256 + 128 * x + lane_base;
-        uint8_t *sQx = sm + L::OFF_Q + x * L::QT_BYTES;
-        uint32_t q_seq = 0, s_seq = 0, o_seq = 0;
+        uint32_t s_seq = 0, o_seq = 0;
         bool ok = true;
         const float sl2 = a.scale_log2;
         for (int i = first_item; ok && i < a.n_items; i += stride) {
             const Item it = decode_item(a, i);
-            if (!mbar_wait(&bars[B_QFULL], q_seq & 1, s_abort)) break;
-            ++q_seq;
             const bool has_x = x ? it.has[1] : it.has[0];
             const int qt_x = x ? it.qt[1] : it.qt[0], h_x = x ? it.h[1] : it.h[0];
             const int tf_x = x ? it.tf[1] : it.tf[0], tl_x = x ? it.tl[1] : it.tl[0];
             const int row = qt_x * BM + r;       // row within the chunk
             const bool valid = has_x && row < a.C;
             const int t = tf_x + r;              // absolute position
-            if (has_x) {
-                if (QDT == KVC_IN_F32) {
-                    const float *src = a.q_f32 + ((int64_t)row * a.H_q + h_x) * D;
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 8; ++cc) {
-                        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-                        if (valid) {
-                            x0 = __ldg(reinterpret_cast<const float4 *>(src + cc * 8));
-                            x1 = __ldg(reinterpret_cast<const float4 *>(src + cc * 8 + 4));
-                        }
-                        *reinterpret_cast<uint4 *>(sQx + op_off(BM, r, cc)) =
-                            make_uint4(pack_half2(x0.x, x0.y), pack_half2(x0.z, x0.w), pack_half2(x1.x, x1.y),
-                                       pack_half2(x1.z, x1.w));
-                    }
-                } else if (QDT == KVC_IN_BF16) {
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 8; ++cc) {
-                        uint4 *p = reinterpret_cast<uint4 *>(sQx + op_off(BM, r, cc));
-                        uint4 v = *p;
-                        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
-                        *p = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars[B_QREADY]);
 
             float m_ref = -INFINITY, l = 0.f;
             bool any = false;
@@ -730,14 +744,15 @@ struct Plan {
     size_t part_bytes;
 };
 
-// Keys per split: a power of two near n_ctx/4, between 4096 and 16384.  It depends on the cache
-// only, never on the chunk, so a row meets the same split boundaries however the prompt is cut.
+// Tiles per split: about a tenth of the cache in steps of 1024 keys, at least 2048 keys, and at
+// most MAX_SPLITS splits.  It depends on the cache only, never on the chunk, so a row meets the same
+// split boundaries however the prompt is cut.  Shorter splits balance the persistent CTAs better but
+// write more partials for the merge.
 int split_tiles(int n_ctx) {
-    int keys = 1;
-    while (keys * 2 <= n_ctx / 4) keys *= 2;
-    if (keys < 4096) keys = 4096;
-    if (keys > 16384) keys = 16384;
-    return keys / BN;
+    int tiles = (n_ctx / 10 + 512) / 1024 * (1024 / BN);
+    if (tiles < 2048 / BN) tiles = 2048 / BN;
+    const int min_tiles = (n_ctx + MAX_SPLITS * BN - 1) / (MAX_SPLITS * BN);
+    return tiles > min_tiles ? tiles : min_tiles;
 }
 
 bool make_plan(const kvc_desc &d, int n_head_q, int pos0, int C, Plan &p) {
