@@ -59,6 +59,13 @@ def prefill_flops(w, chunks=None):
     return out
 
 
+def prefill_split_keys(n_ctx):
+    """Keys per prefill split as the library chooses them: about a tenth of the cache in steps of
+    1024 keys, at least 2048, and at most 64 splits (in 256-key tiles)."""
+    keys = max((n_ctx // 10 + 512) // 1024 * 1024, 2048)
+    return max(keys, -(-n_ctx // (64 * 256)) * 256)
+
+
 def cache_bytes_per_token(w):
     if w.cache == "q8_0":
         return 2 * w.n_head_kv * w.head_dim * 34 // 32
@@ -200,14 +207,10 @@ class GpuRequest:
 
     def launches_per_step(self):
         """Kernels one step launches: per chunk an append and the attention, plus the split merge when
-        the chunk's last row reaches past the first key split (keys per split: the power of two near
-        n_ctx/4, clamped to [4096, 16384]); per decode step append, split pass and combine; the state
-        header, pack and unpack."""
+        the chunk's last row reaches past the first key split; per decode step append, split pass and
+        combine; the state header, pack and unpack."""
         w = self.w
-        keys = 1
-        while keys * 2 <= w.n_ctx // 4:
-            keys *= 2
-        keys = min(max(keys, 4096), 16384)
+        keys = prefill_split_keys(w.n_ctx)
         merges = sum(1 for p, c in self.chunks if p + c - 1 >= keys)
         return w.n_layer * (2 * len(self.chunks) + merges + 3 * w.n_decode) + 3
 

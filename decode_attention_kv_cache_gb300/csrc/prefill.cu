@@ -9,37 +9,39 @@
 // llama.cpp PR #58 "completion : allow the prompt to be processed under its
 // own split mode", section "Why").
 //
-// Work decomposition.  A unit is 128 query rows of one query head.  The units
-// of one kv group are listed q-tile-major and taken in pairs, so a CTA works on
-// two Q tiles that read the same K/V tiles (two query heads of the group, or
-// the last head of one q-tile with the first of the next).  The keys of a pair
-// are cut at ABSOLUTE split boundaries of ST tiles (ST is fixed by the cache
-// size): an item is (pair, split).  Persistent CTAs (one per SM) take items
-// round-robin.  An item whose pair has one split writes the output directly;
-// otherwise it writes its partial (O, running max, sum), and a second, fully
-// parallel kernel merges the partials of each row in split order (merging
-// inside the persistent kernel left the merging SM's tensor pipe idle).
-// Because tiles and splits sit at absolute positions and every merge runs in
-// split order, a row's result does not depend on how the prompt is cut into
-// chunks.
+// Work decomposition.  A unit is 128 query rows of one query head.  Keys are
+// taken in tiles of 256 and cut at ABSOLUTE split boundaries of ST tiles (ST
+// is fixed by the cache size): an item is (unit, split).  Persistent CTAs (one
+// per SM) take items round-robin, split-major and kv-group-major so that the
+// CTAs running at one time read the same K/V tiles.  An item whose unit has
+// one split writes the output directly; otherwise it writes its partial (O,
+// running max, sum), and a second, fully parallel kernel merges each row's
+// partials in split order.  Because tiles and splits sit at absolute
+// positions and every merge runs in split order, a row's result does not
+// depend on how the prompt is cut into chunks.
+//
+// Tensor memory (512 columns): S = Q K^T of one key tile (256 fp32 columns),
+// P = softmax numerators as fp16 (128 columns), O (D columns).  S, P and O
+// are separate, so S of the next tile is computed while the softmax of this
+// one runs, and the MMA issue order per tile is S(k+1), PV(k).  Both are
+// M=128 MMAs; S has N=256, the shape at which the tensor core reaches its
+// full rate (N=128 runs at about 60% of it on this part).
 //
 // One CTA:
-//   warp 0      TMA producer: the two Q tiles of an item, then K and V tiles
+//   warp 0      TMA producer: the Q tile of an item, then K and V tiles in
+//               the MMA's order K(k0), K(k0+1), V(k0), K(k0+2), V(k0+1), ...
 //               (int8 codes into a raw ring for q8_0; fp16 values straight into
 //               the operand ring for f16).
-//   warp 1      allocates all 512 TMEM columns (S/P and O for both Q tiles);
-//               one lane issues tcgen05.mma: S = Q K^T (both operands in shared
-//               memory) and O += P V (P from tensor memory, V as an MN-major
-//               shared-memory operand), interleaved as
-//               PV_A(k), S_A(k+1), PV_B(k), S_B(k+1) so each softmax has two
-//               MMAs' time to turn S into P.
-//   warps 2-3   put the two Q tiles in fp16 (bf16 converted in place, f32 read
-//               from global memory); Q is released after the item's last S MMAs,
-//               so the next item's Q is loaded and converted during this one's tail.
-//   warps 4-7   softmax of Q tile A, warps 8-11 of Q tile B: thread r owns row r
-//               (TMEM lane r): row max, exp2, fp16 P written back over S in
-//               tensor memory, O rescaled in TMEM only when the running max
-//               grows by more than 2^8; epilogue O / l.
+//   warp 1      allocates the 512 TMEM columns; one lane issues tcgen05.mma.
+//   warps 2-3   put the Q tile in fp16 (bf16 converted in place, f32 read from
+//               global memory); Q is released after the item's last S MMA, so
+//               the next item's Q loads during this one's tail.
+//   warps 4-11  softmax: two warpgroups, each owns 128 of the tile's 256 key
+//               columns for all 128 rows (thread = TMEM lane = row).  Row maxima
+//               are exchanged through shared memory, so both groups use the
+//               same running max; each group writes its half of P and
+//               rescales its half of O (only when the running max grows by
+//               more than 2^8).
 //   warps 12-15 (q8_0) dequantise int8 rows into fp16 d*q in the 128-byte
 //               swizzled operand layout.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
@@ -63,41 +65,45 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = 128;           // query rows per Q tile
-constexpr int BN = 128;           // keys per tile
+constexpr int BM = 128;           // query rows per unit
+constexpr int BN = 256;           // keys per tile
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0, COL_P = 256, COL_O = 384;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr int MAX_SPLITS = 64;
+constexpr int MAX_DYN_SMEM = 232448;   // 227 KB per CTA
 // a partial row: D values, the running max, the sum, two pad floats (keeps rows 16-byte aligned)
 #define PART_ROW(D) ((D) + 4)
 
 template <int D, bool Q8>
 struct Cfg {
-    static constexpr int QT_BYTES = BM * D * 2;    // one fp16 Q tile
+    static constexpr int QT_BYTES = BM * D * 2;    // the fp16 Q tile
     static constexpr int ST_BYTES = BN * D * 2;    // one ring stage: a fp16 K or V tile
     static constexpr int RAW_BYTES = BN * D;       // one int8 K or V tile
-    static constexpr int NS = Q8 ? 3 : 5;          // fp16 operand ring stages
-    static constexpr int NR = Q8 ? 4 : 1;          // int8 raw ring stages
+    static constexpr int NS = Q8 ? (D == 128 ? 2 : 4) : (D == 128 ? 3 : 6);  // fp16 operand ring stages
+    static constexpr int NR = Q8 ? (D == 128 ? 2 : 4) : 1;                   // int8 raw ring stages
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_RING = OFF_Q + 2 * QT_BYTES;
+    static constexpr int OFF_RING = OFF_Q + QT_BYTES;
     static constexpr int OFF_RAW = OFF_RING + NS * ST_BYTES;
     static constexpr int OFF_BAR = OFF_RAW + (Q8 ? NR * RAW_BYTES : 0);
-    static constexpr int USED = OFF_BAR + 512;
-    static constexpr int ALLOC = (USED + 1024 > 122880) ? USED + 1024 : 122880;  // one CTA per SM
+    static constexpr int OFF_RED = OFF_BAR + 512;             // [parity][group][row] floats
+    static constexpr int USED = OFF_RED + 2 * 2 * BM * 4;
+    static constexpr int ALLOC = (USED + 1024 <= MAX_DYN_SMEM) ? USED + 1024 : MAX_DYN_SMEM;
+    static_assert(USED <= MAX_DYN_SMEM, "shared memory plan too large");
     static constexpr int THREADS = Q8 ? 512 : 384;
     // registers per thread: at launch (65536 / THREADS, multiple of 8), then per warpgroup after
     // setmaxnreg; sum over warpgroups of 128 * regs must not exceed THREADS * LAUNCH_REGS
     static constexpr int LAUNCH_REGS = Q8 ? 128 : 168;
-    static constexpr int WG0_REGS = 112;                    // producer, MMA issuer, two idle warps
+    static constexpr int WG0_REGS = Q8 ? 72 : 152;          // producer, MMA issuer, Q warps
     static constexpr int DQ_REGS = 88;                      // dequantising warpgroup (q8_0)
-    static constexpr int SM_REGS = Q8 ? 152 : 192;          // each softmax warpgroup
+    static constexpr int SM_REGS = 176;                     // each softmax warpgroup
     static_assert(128 * WG0_REGS + 256 * SM_REGS + (Q8 ? 128 * DQ_REGS : 0) <= THREADS * LAUNCH_REGS,
                   "register split exceeds the launch allocation");
 };
 
 enum Bar {
-    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ODONE0, B_ODONE1,
-    B_OFREE0, B_OFREE1, B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
+    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_OFREE, B_XCHG, B_DRAIN,
+    B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
     B_RAW_EMPTY = B_RAW_FULL + 8, NBAR = B_RAW_EMPTY + 8
 };
 
@@ -106,51 +112,42 @@ struct Args {
     const uint16_t *ks;
     const uint16_t *vs;
     float *out;
-    float *part;      // partials [pair][split][tile][row][PART_ROW]
+    float *part;      // partials [q-tile][head][split][row][PART_ROW]
     Geom g;
-    int layer, pos0, C, kv_len, H_q, G, H_kv, n_qt, U, J, ST, smax, n_items;
+    int layer, pos0, C, kv_len, H_q, G, H_kv, n_qt, ST, smax, n_items;
     float scale_log2;
     int cum[MAX_SPLITS + 1];   // items before split index s
-    int jmin[MAX_SPLITS];      // first pair index that reaches split s
+    int qtmin[MAX_SPLITS];     // first q-tile whose keys reach split s
 };
 
 struct Item {
-    int g, j, s, ns, k0, k1;
-    int qt[2], h[2], tf[2], tl[2];
-    bool has[2];
+    int g, h, qt, s, ns, k0, k1, tf, tl;
 };
 
+// last absolute position of q-tile qt
 __device__ __forceinline__ int unit_tl(const Args &a, int qt) {
     return a.pos0 + min(qt * BM + BM, a.C) - 1;
 }
 
+// Items are ordered by split, then kv group, then q-tile, then head within the group.
 __device__ __forceinline__ Item decode_item(const Args &a, int i) {
     Item it;
     int s = 0;
     while (s + 1 < a.smax && a.cum[s + 1] <= i) ++s;
     const int r = i - a.cum[s];
-    const int nj = a.J - a.jmin[s];
-    it.g = r / nj;
-    it.j = a.jmin[s] + r % nj;
+    const int per_g = (a.n_qt - a.qtmin[s]) * a.G;
+    it.g = r / per_g;
+    const int rem = r - it.g * per_g;
+    it.qt = a.qtmin[s] + rem / a.G;
+    it.h = it.g * a.G + rem % a.G;
     it.s = s;
-    for (int x = 0; x < 2; ++x) {
-        const int e = 2 * it.j + x;
-        it.has[x] = e < a.U;
-        const int ee = it.has[x] ? e : 2 * it.j;
-        it.qt[x] = ee / a.G;
-        it.h[x] = it.g * a.G + ee % a.G;
-        it.tf[x] = a.pos0 + it.qt[x] * BM;
-        it.tl[x] = unit_tl(a, it.qt[x]);
-    }
-    const int T = it.tl[it.has[1] ? 1 : 0] / BN + 1;
+    it.tf = a.pos0 + it.qt * BM;
+    it.tl = unit_tl(a, it.qt);
+    const int T = it.tl / BN + 1;
     it.ns = (T + a.ST - 1) / a.ST;
     it.k0 = s * a.ST;
     it.k1 = min(T, (s + 1) * a.ST);
     return it;
-}
-
-__device__ __forceinline__ bool tile_active(const Item &it, int x, int k) {
-    return it.has[x] && k * BN <= it.tl[x];
 }
 
 __device__ __forceinline__ uint32_t sw128(int row, int c) {
@@ -170,10 +167,13 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
            ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
 
-// 4 int8 codes times the fp16 scale, as two fp16x2 words (one rounding each).
+// 4 int8 codes times the fp16 scale, as two fp16x2 words (one rounding each).  Flipping the sign
+// bit makes each code q + 128 as an unsigned byte; under the high byte 0x64 that is the fp16 value
+// 1024 + q + 128, exact, and subtracting 1152 leaves q.
 __device__ __forceinline__ void dequant4(uint32_t w, __half2 d2, uint32_t &lo, uint32_t &hi) {
-    const uint32_t a = (__byte_perm(w, 0, 0x0100) & 0x00FF00FFu) ^ 0x64806480u;  // 1024 + q + 128
-    const uint32_t b = (__byte_perm(w, 0, 0x0302) & 0x00FF00FFu) ^ 0x64806480u;
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
     __half2 ra = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&a), bias), d2);
     __half2 rb = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b), bias), d2);
@@ -206,12 +206,17 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Args a) {
     using L = Cfg<D, Q8>;
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
+    if (sm + L::USED > smem_raw + L::ALLOC) {  // the operand tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicExch(&g_device_status, 2);
+        return;
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    float *s_red = reinterpret_cast<float *>(sm + L::OFF_RED);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -220,12 +225,13 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_QREADY], 64);
         mbar_init(&bars[B_QEMPTY], 1);
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(&bars[B_SFULL0 + x], 1);
-            mbar_init(&bars[B_PFULL0 + x], 128);
-            mbar_init(&bars[B_ODONE0 + x], 1);
-            mbar_init(&bars[B_OFREE0 + x], 128);
-        }
+        mbar_init(&bars[B_SFULL], 1);
+        mbar_init(&bars[B_SFREE], 256);
+        mbar_init(&bars[B_PFULL], 256);
+        mbar_init(&bars[B_ODONE], 1);
+        mbar_init(&bars[B_OFREE], 256);
+        mbar_init(&bars[B_XCHG], 256);
+        mbar_init(&bars[B_DRAIN], 1);
         for (int s = 0; s < L::NS; ++s) {
             mbar_init(&bars[B_RING_FULL + s], Q8 ? 128 : 1);
             mbar_init(&bars[B_RING_EMPTY + s], 1);
@@ -243,10 +249,10 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *s_tmem;  // S/P of tile x at column 128x, O of tile x at 256 + 128x
+    const uint32_t tmem = *s_tmem;
     const int first_item = blockIdx.x, stride = gridDim.x;
 
-    if (warp < 4) setmaxnreg_dec<L::WG0_REGS>();  // producer, MMA issuer and two idle warps
+    if (warp < 4) setmaxnreg_dec<L::WG0_REGS>();  // producer, MMA issuer and the Q warps
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
         if (lane == 0) {
@@ -254,50 +260,56 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             tma_prefetch_desc(&tm_v);
             uint32_t ring_seq = 0, raw_seq = 0, q_seq = 0;
             bool ok = true;
+            // the next K or V tile of kv group g into the raw (q8_0) or operand (f16) ring
+            auto load_kv = [&](int kv, int k, int g) -> bool {
+                const CUtensorMap *m = kv ? &tm_v : &tm_k;
+                if (Q8) {
+                    const int rs = raw_seq % L::NR;
+                    if (raw_seq >= (uint32_t)L::NR &&
+                        !mbar_wait(&bars[B_RAW_EMPTY + rs], ((raw_seq / L::NR) - 1) & 1, s_abort))
+                        return false;
+                    mbar_arrive_expect_tx(&bars[B_RAW_FULL + rs], L::RAW_BYTES);
+                    tma_load_3d(sm + L::OFF_RAW + rs * L::RAW_BYTES, m, &bars[B_RAW_FULL + rs], 0, k * BN, g);
+                    ++raw_seq;
+                } else {
+                    const int st = ring_seq % L::NS;
+                    if (ring_seq >= (uint32_t)L::NS &&
+                        !mbar_wait(&bars[B_RING_EMPTY + st], ((ring_seq / L::NS) - 1) & 1, s_abort))
+                        return false;
+                    mbar_arrive_expect_tx(&bars[B_RING_FULL + st], L::ST_BYTES);
+                    for (int dh = 0; dh < D / 64; ++dh)
+                        tma_load_3d(sm + L::OFF_RING + st * L::ST_BYTES + dh * BN * 128, m, &bars[B_RING_FULL + st],
+                                    dh * 64, k * BN, g);
+                    ++ring_seq;
+                }
+                return true;
+            };
             for (int i = first_item; ok && i < a.n_items; i += stride) {
                 const Item it = decode_item(a, i);
                 if (q_seq > 0 && !mbar_wait(&bars[B_QEMPTY], (q_seq - 1) & 1, s_abort)) break;
                 if (QDT != KVC_IN_F32) {
-                    mbar_arrive_expect_tx(&bars[B_QFULL], (it.has[1] ? 2 : 1) * L::QT_BYTES);
-                    for (int x = 0; x < 2; ++x) {
-                        if (!it.has[x]) continue;
-                        for (int dh = 0; dh < D / 64; ++dh)
-                            tma_load_3d(sm + L::OFF_Q + x * L::QT_BYTES + dh * BM * 128, &tm_q, &bars[B_QFULL],
-                                        dh * 64, it.h[x], it.qt[x] * BM);
-                    }
+                    mbar_arrive_expect_tx(&bars[B_QFULL], L::QT_BYTES);
+                    for (int dh = 0; dh < D / 64; ++dh)
+                        tma_load_3d(sm + L::OFF_Q + dh * BM * 128, &tm_q, &bars[B_QFULL], dh * 64, it.h, it.qt * BM);
                 } else {
-                    mbar_arrive(&bars[B_QFULL]);  // the softmax warps load f32 Q themselves
+                    mbar_arrive(&bars[B_QFULL]);  // the Q warps load f32 Q themselves
                 }
                 ++q_seq;
+                ok = load_kv(0, it.k0, it.g);
                 for (int k = it.k0; ok && k < it.k1; ++k) {
-                    for (int kv = 0; kv < 2 && ok; ++kv) {
-                        const CUtensorMap *m = kv ? &tm_v : &tm_k;
-                        if (Q8) {
-                            const int rs = raw_seq % L::NR;
-                            if (raw_seq >= (uint32_t)L::NR &&
-                                !mbar_wait(&bars[B_RAW_EMPTY + rs], ((raw_seq / L::NR) - 1) & 1, s_abort)) {
-                                ok = false;
-                                break;
-                            }
-                            mbar_arrive_expect_tx(&bars[B_RAW_FULL + rs], L::RAW_BYTES);
-                            tma_load_3d(sm + L::OFF_RAW + rs * L::RAW_BYTES, m, &bars[B_RAW_FULL + rs], 0, k * BN,
-                                        it.g);
-                            ++raw_seq;
-                        } else {
-                            const int st = ring_seq % L::NS;
-                            if (ring_seq >= (uint32_t)L::NS &&
-                                !mbar_wait(&bars[B_RING_EMPTY + st], ((ring_seq / L::NS) - 1) & 1, s_abort)) {
-                                ok = false;
-                                break;
-                            }
-                            mbar_arrive_expect_tx(&bars[B_RING_FULL + st], L::ST_BYTES);
-                            for (int dh = 0; dh < D / 64; ++dh)
-                                tma_load_3d(sm + L::OFF_RING + st * L::ST_BYTES + dh * BN * 128, m,
-                                            &bars[B_RING_FULL + st], dh * 64, k * BN, it.g);
-                            ++ring_seq;
-                        }
-                    }
+                    if (k + 1 < it.k1) ok = load_kv(0, k + 1, it.g);
+                    if (ok) ok = load_kv(1, k, it.g);
                 }
+            }
+            if (*s_abort) {
+                // after a wait gave up: let the copies still in flight land before the CTA exits
+                volatile int never = 0;
+                const uint32_t n = Q8 ? raw_seq : ring_seq, stages = Q8 ? L::NR : L::NS;
+                for (uint32_t st = 0; st < stages && st < n; ++st) {
+                    const uint32_t last = st + ((n - 1 - st) / stages) * stages;
+                    mbar_wait(&bars[(Q8 ? B_RAW_FULL : B_RING_FULL) + st], (last / stages) & 1, &never, 200000000ull);
+                }
+                if (QDT != KVC_IN_F32 && q_seq > 0) mbar_wait(&bars[B_QFULL], (q_seq - 1) & 1, &never, 200000000ull);
             }
         }
     } else if (warp == 1) {
@@ -306,94 +318,74 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             constexpr uint32_t IDESC_S = idesc_f16(BM, BN, 0, 0);
             constexpr uint32_t IDESC_O = idesc_f16(BM, D, 0, 1);
             const uint32_t sQ = smem_u32(sm + L::OFF_Q), sRing = smem_u32(sm + L::OFF_RING);
-            uint32_t ring_seq = 0, q_seq = 0, p_seq[2] = {0, 0}, ofree_seq[2] = {0, 0};
-            uint32_t pv_issued[2] = {0, 0}, pv_done[2] = {0, 0};
-            bool o_used[2] = {false, false};
-            bool ok = true;
+            uint32_t ring_seq = 0, q_seq = 0, s_issued = 0, p_seq = 0, ofree_seq = 0;
+            bool o_used = false, ok = true;
             auto ring_wait = [&](uint32_t seq) -> bool {
                 if (!mbar_wait(&bars[B_RING_FULL + seq % L::NS], (seq / L::NS) & 1, s_abort)) return false;
                 tc_fence_after();
                 return true;
             };
-            // S_x and P_x share TMEM columns: before S_x overwrites them, the PV MMA that reads P_x must be
-            // complete (its o_done phase; the softmax group waits on the same phases independently)
-            auto pv_drain = [&](int x) -> bool {
-                while (pv_done[x] < pv_issued[x]) {
-                    if (!mbar_wait(&bars[B_ODONE0 + x], pv_done[x] & 1, s_abort)) return false;
-                    ++pv_done[x];
-                }
-                tc_fence_after();
-                return true;
-            };
-            // S_x = Q_x K^T.  P_x (fp16, packed) occupies the first 64 columns of the S_x region, so the PV
-            // MMA that reads P_x must be complete before S_x is overwritten.
-            auto issue_s = [&](int x, uint32_t seq) -> bool {
+            // S = Q K^T of the next K tile in the ring.  It overwrites the previous S, which the
+            // softmax must have read out (s_free).
+            auto issue_s = [&]() -> bool {
+                if (s_issued > 0 && !mbar_wait(&bars[B_SFREE], (s_issued - 1) & 1, s_abort)) return false;
+                const uint32_t seq = ring_seq++;
+                if (!ring_wait(seq)) return false;
                 const uint32_t kb = sRing + (seq % L::NS) * L::ST_BYTES;
-                const uint32_t qb = sQ + x * L::QT_BYTES;
-                if (!pv_drain(x)) return false;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-                    umma_f16_ss(tmem + 128 * x, sdesc_sw128(qb + off, 16, 1024),
-                                sdesc_sw128(kb + off, 16, 1024), IDESC_S, ks > 0);
+                    const uint32_t kk = (ks & 3) * 32;
+                    umma_f16_ss(tmem + COL_S, sdesc_sw128(sQ + (ks >> 2) * (BM * 128) + kk, 16, 1024),
+                                sdesc_sw128(kb + (ks >> 2) * (BN * 128) + kk, 16, 1024), IDESC_S, ks > 0);
                 }
-                umma_commit(&bars[B_SFULL0 + x]);
+                umma_commit(&bars[B_SFULL]);
+                umma_commit(&bars[B_RING_EMPTY + seq % L::NS]);
+                ++s_issued;
                 return true;
             };
-            // O_x += P_x V: P_x from TMEM (fp16 packed in the S columns), V MN-major in the ring stage
-            auto issue_pv = [&](int x, uint32_t seq, bool acc) {
+            // O (+)= P V: P fp16 from TMEM, V MN-major in the ring stage
+            auto issue_pv = [&](bool acc) -> bool {
+                const uint32_t seq = ring_seq++;
+                if (!ring_wait(seq)) return false;
                 const uint32_t vb = sRing + (seq % L::NS) * L::ST_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
-                    umma_f16_ts(tmem + 256 + 128 * x, tmem + 128 * x + ks * 8,
-                                sdesc_sw128(vb + ks * 16 * 128, BN * 128, 1024), IDESC_O, (acc || ks > 0) ? 1u : 0u);
-                umma_commit(&bars[B_ODONE0 + x]);
-                ++pv_issued[x];
+                    umma_f16_ts(tmem + COL_O, tmem + COL_P + ks * 8, sdesc_sw128(vb + ks * 16 * 128, BN * 128, 1024),
+                                IDESC_O, (acc || ks > 0) ? 1u : 0u);
+                umma_commit(&bars[B_ODONE]);
+                umma_commit(&bars[B_RING_EMPTY + seq % L::NS]);
+                return true;
             };
             for (int i = first_item; ok && i < a.n_items; i += stride) {
                 const Item it = decode_item(a, i);
                 if (!mbar_wait(&bars[B_QREADY], q_seq & 1, s_abort)) break;
                 ++q_seq;
                 tc_fence_after();
-                bool first_pv[2] = {true, true};
-                const uint32_t kseq = ring_seq++;
-                if (!ring_wait(kseq)) break;
-                for (int x = 0; x < 2 && ok; ++x)
-                    if (tile_active(it, x, it.k0) && !issue_s(x, kseq)) ok = false;
-                if (!ok) break;
-                umma_commit(&bars[B_RING_EMPTY + kseq % L::NS]);
-                // Q is free once the item's last S MMAs complete: the next item's Q loads during this one's tail
+                if (!issue_s()) break;
+                // Q is free once the item's last S MMA completes: the next item's Q loads during this one's tail
                 if (it.k0 + 1 == it.k1) umma_commit(&bars[B_QEMPTY]);
-                // per key tile: PV_A(k), S_A(k+1), PV_B(k), S_B(k+1)
+                // per key tile: S(k+1), then PV(k)
                 for (int k = it.k0; ok && k < it.k1; ++k) {
-                    const uint32_t vseq = ring_seq++;
-                    if (!ring_wait(vseq)) { ok = false; break; }
-                    const bool more = k + 1 < it.k1;
-                    uint32_t kseq_next = 0;
-                    if (more) kseq_next = ring_seq++;
-                    for (int x = 0; x < 2 && ok; ++x) {
-                        if (tile_active(it, x, k)) {
-                            if (first_pv[x] && o_used[x]) {
-                                if (!mbar_wait(&bars[B_OFREE0 + x], ofree_seq[x] & 1, s_abort)) { ok = false; break; }
-                                ++ofree_seq[x];
-                            }
-                            if (!mbar_wait(&bars[B_PFULL0 + x], p_seq[x] & 1, s_abort)) { ok = false; break; }
-                            ++p_seq[x];
-                            tc_fence_after();
-                            issue_pv(x, vseq, !first_pv[x]);
-                            first_pv[x] = false;
-                            o_used[x] = true;
-                        }
-                        if (more) {
-                            if (x == 0 && !ring_wait(kseq_next)) { ok = false; break; }
-                            if (tile_active(it, x, k + 1) && !issue_s(x, kseq_next)) { ok = false; break; }
-                        }
+                    if (k + 1 < it.k1) {
+                        if (!issue_s()) { ok = false; break; }
+                        if (k + 2 == it.k1) umma_commit(&bars[B_QEMPTY]);
                     }
-                    if (!ok) break;
-                    umma_commit(&bars[B_RING_EMPTY + vseq % L::NS]);
-                    if (more) umma_commit(&bars[B_RING_EMPTY + kseq_next % L::NS]);
-                    if (more && k + 2 == it.k1) umma_commit(&bars[B_QEMPTY]);
+                    if (k == it.k0 && o_used) {  // the previous item's epilogue has read O
+                        if (!mbar_wait(&bars[B_OFREE], ofree_seq & 1, s_abort)) { ok = false; break; }
+                        ++ofree_seq;
+                    }
+                    if (!mbar_wait(&bars[B_PFULL], p_seq & 1, s_abort)) { ok = false; break; }
+                    ++p_seq;
+                    tc_fence_after();
+                    if (!issue_pv(k > it.k0)) { ok = false; break; }
+                    o_used = true;
                 }
+            }
+            if (*s_abort) {
+                // after a wait gave up: let the MMAs in flight finish before TMEM is freed
+                volatile int never = 0;
+                umma_commit(&bars[B_DRAIN]);
+                mbar_wait(&bars[B_DRAIN], 0, &never, 200000000ull);
             }
         }
         __syncwarp();
@@ -408,17 +400,16 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             const Item it = decode_item(a, i);
             if (!mbar_wait(&bars[B_QFULL], q_seq & 1, s_abort)) break;
             ++q_seq;
-            for (int x = 0; x < 2; ++x) {
-                if (!it.has[x] || QDT == KVC_IN_F16) continue;
-                uint8_t *sQx = sm + L::OFF_Q + x * L::QT_BYTES;
+            if (QDT != KVC_IN_F16) {
+                uint8_t *sQ = sm + L::OFF_Q;
 #pragma unroll 4
                 for (int r = r_off; r < BM; r += 2 * RPI) {
-                    uint4 *p = reinterpret_cast<uint4 *>(sQx + op_off(BM, r, cc));
+                    uint4 *p = reinterpret_cast<uint4 *>(sQ + op_off(BM, r, cc));
                     if (QDT == KVC_IN_F32) {
-                        const int row = it.qt[x] * BM + r;
+                        const int row = it.qt * BM + r;
                         float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
                         if (row < a.C) {
-                            const float *src = a.q_f32 + ((int64_t)row * a.H_q + it.h[x]) * D + cc * 8;
+                            const float *src = a.q_f32 + ((int64_t)row * a.H_q + it.h) * D + cc * 8;
                             x0 = __ldg(reinterpret_cast<const float4 *>(src));
                             x1 = __ldg(reinterpret_cast<const float4 *>(src + 4));
                         }
@@ -438,85 +429,103 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             fence_proxy_async_smem();
             mbar_arrive(&bars[B_QREADY]);
         }
-    } else if (warp >= 4 && warp < 12) {
-        // ------------------------------------------------------------------ softmax (tile x = A or B)
+    } else if (warp < 12) {
+        // ------------------------------------------------------------------ softmax
         setmaxnreg_inc<L::SM_REGS>();
-        const int x = (warp - 4) >> 2;
-        const int r = threadIdx.x - 128 - 128 * x;  // row in the tile = TMEM lane
+        const int grp = (warp - 4) >> 2;              // key columns [128 grp, 128 grp + 128) of each tile
+        const int r = (warp & 3) * 32 + lane;         // row in the unit = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + 128 * x + lane_base, tO = tmem + 256 + 128 * x + lane_base;
-        uint32_t s_seq = 0, o_seq = 0;
+        const uint32_t tS = tmem + COL_S + 128 * grp + lane_base;
+        const uint32_t tP = tmem + COL_P + 64 * grp + lane_base;
+        const uint32_t tO = tmem + COL_O + (D / 2) * grp + lane_base;
+        uint32_t s_seq = 0, o_seq = 0, x_seq = 0;
         bool ok = true;
         const float sl2 = a.scale_log2;
+        // the other group's value for my row, through shared memory (bounded rendezvous of both groups)
+        auto exchange = [&](float mine, float &theirs) -> bool {
+            float *slot = s_red + (x_seq & 1) * 2 * BM;
+            slot[grp * BM + r] = mine;
+            mbar_arrive(&bars[B_XCHG]);
+            if (!mbar_wait(&bars[B_XCHG], x_seq & 1, s_abort)) return false;
+            ++x_seq;
+            theirs = slot[(grp ^ 1) * BM + r];
+            return true;
+        };
         for (int i = first_item; ok && i < a.n_items; i += stride) {
             const Item it = decode_item(a, i);
-            const bool has_x = x ? it.has[1] : it.has[0];
-            const int qt_x = x ? it.qt[1] : it.qt[0], h_x = x ? it.h[1] : it.h[0];
-            const int tf_x = x ? it.tf[1] : it.tf[0], tl_x = x ? it.tl[1] : it.tl[0];
-            const int row = qt_x * BM + r;       // row within the chunk
-            const bool valid = has_x && row < a.C;
-            const int t = tf_x + r;              // absolute position
-
+            const int row = it.qt * BM + r;       // row within the chunk
+            const bool valid = row < a.C;
+            const int t = it.tf + r;              // absolute position
             float m_ref = -INFINITY, l = 0.f;
-            bool any = false;
             for (int k = it.k0; k < it.k1; ++k) {
-                if (!has_x || k * BN > tl_x) continue;  // tile_active(it, x, k)
-                if (!mbar_wait(&bars[B_SFULL0 + x], s_seq & 1, s_abort)) { ok = false; break; }
+                if (!mbar_wait(&bars[B_SFULL], s_seq & 1, s_abort)) { ok = false; break; }
                 ++s_seq;
                 tc_fence_after();
-                const int key0 = k * BN;
-                const bool need_mask = key0 + BN - 1 > tf_x;
-                // the whole S row in registers (one TMEM round trip), masked keys set to -inf
-                uint32_t s[BN];
+                // my half of the S row in registers (one TMEM round trip), then S may be overwritten
+                uint32_t s[128];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) tmem_ld32p(tS + c * 32, s + c * 32);
+                for (int c = 0; c < 4; ++c) tmem_ld32p(tS + c * 32, s + c * 32);
                 tmem_ld_wait();
-                if (need_mask) {
+                tc_fence_before();
+                mbar_arrive(&bars[B_SFREE]);
+                const int key0 = k * BN + 128 * grp;
+                if (key0 + 127 > it.tf) {
 #pragma unroll
-                    for (int e = 0; e < BN; ++e)
-                        if (key0 + e > t) s[e] = 0xFF800000u;
+                    for (int e = 0; e < 128; ++e)
+                        if (key0 + e > t) s[e] = 0xFF800000u;  // -inf: a key after the query
                 }
-                // row max: 8 independent chains, then a tree (max is exact in any order)
+                // row max: 8 independent chains of three-input maxima, then a tree (max is exact in any order)
                 float mx8[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
 #pragma unroll
-                for (int e = 8; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(s[e]));
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int e = 8; e < 120; e += 16) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        mx8[u] = fmax3(mx8[u], __uint_as_float(s[e + u]), __uint_as_float(s[e + 8 + u]));
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], __uint_as_float(s[120 + u]));
+                float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                float mx_other;
+                if (!exchange(mx, mx_other)) { ok = false; break; }
+                mx = fmaxf(mx, mx_other);
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 float m_use = m_ref, alpha = 1.f;
-                if (!any) {
-                    m_use = m_new;  // the first visible tile of a row holds a visible key
+                if (k == it.k0) {
+                    m_use = m_new;
                 } else if (m_new > m_ref + RESCALE_LOG2) {
                     m_use = m_new;
                     alpha = ex2(m_ref - m_new);
                 }
                 // -inf scores give p = 0 exactly; a row with no visible key so far uses 0 as its offset
                 const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-                // probabilities; the row sum in 8 independent partial sums, added in a fixed order
-                float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // probabilities as fp16 pairs (exponents by packed fma); the row sum in 4 packed partial
+                // sums, added in a fixed order
+                uint32_t pk[64];
+                const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_sub, -m_sub);
+                uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(s[c * 32 + e]), sl2, -m_sub));
-                        const float p1 = ex2(fmaf(__uint_as_float(s[c * 32 + e + 1]), sl2, -m_sub));
-                        rs8[(e >> 1) & 7] += p0 + p1;
-                        pk[e / 2] = pack_half2(p0, p1);
-                    }
-                    tmem_st16(tS + c * 16, pk);
+                for (int e = 0; e < 128; e += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2x2, nm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    rs4[(e >> 1) & 3] = f2_add(rs4[(e >> 1) & 3], f2_pack(p0, p1));
+                    pk[e >> 1] = pack_half2(p0, p1);
                 }
-                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                float r8[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) f2_unpack(rs4[u], r8[2 * u], r8[2 * u + 1]);
+                const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
                 l = l * alpha + rs;
-                if (any) {
-                    if (!mbar_wait(&bars[B_ODONE0 + x], o_seq & 1, s_abort)) { ok = false; break; }
+                if (k > it.k0) {
+                    // P and O are free once PV(k-1) is complete
+                    if (!mbar_wait(&bars[B_ODONE], o_seq & 1, s_abort)) { ok = false; break; }
                     ++o_seq;
                     tc_fence_after();
                     if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
+                        for (int c = 0; c < D / 64; ++c) {
                             uint32_t o[32];
                             tmem_ld32(tO + c * 32, o);
                             tmem_ld_wait();
@@ -526,121 +535,125 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                         }
                     }
                 }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, pk + c * 16);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars[B_PFULL0 + x]);
-                any = true;
+                mbar_arrive(&bars[B_PFULL]);
                 m_ref = m_use;
             }
             if (!ok) break;
-            // ---- epilogue: this item's O for my row (or zeros when no tile of the item reached it)
-            if (any) {
-                if (!mbar_wait(&bars[B_ODONE0 + x], o_seq & 1, s_abort)) { ok = false; break; }
-                ++o_seq;
-                tc_fence_after();
-            }
-            const int pg = it.g * a.J + it.j;
-            float *part_row = a.part + ((((int64_t)pg * a.smax + it.s) * 2 + x) * BM + r) * PART_ROW(D);
-            float *out_row = a.out + ((int64_t)row * a.H_q + h_x) * D;
-            const float inv = 1.f / l;
-            if (has_x) {
+            // ---- epilogue: the row sum over both halves, then O / l or the partial (O, m, l)
+            if (!mbar_wait(&bars[B_ODONE], o_seq & 1, s_abort)) { ok = false; break; }
+            ++o_seq;
+            tc_fence_after();
+            float l_other;
+            if (!exchange(l, l_other)) { ok = false; break; }
+            const float l_row = grp == 0 ? l + l_other : l_other + l;
+            const int unit = it.qt * a.H_q + it.h;
+            float *part_row = a.part + (((int64_t)unit * a.smax + it.s) * BM + r) * PART_ROW(D);
+            float *out_row = a.out + ((int64_t)row * a.H_q + it.h) * D;
+            const float inv = 1.f / l_row;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    if (any) {
-                        tmem_ld32(tO + c * 32, o);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = 0u;
-                    }
-                    if (it.ns == 1) {
-                        if (valid) {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 4)
-                                *reinterpret_cast<float4 *>(out_row + c * 32 + e) =
-                                    make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                                                __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        }
-                    } else {
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_ld_wait();
+                const int col = (D / 2) * grp + c * 32;
+                if (it.ns == 1) {
+                    if (valid) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4 *>(part_row + c * 32 + e) =
-                                make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
-                                            __uint_as_float(o[e + 3]));
+                            *reinterpret_cast<float4 *>(out_row + col + e) =
+                                make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                            __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
                     }
-                }
-                if (it.ns > 1) {
-                    part_row[D] = any ? m_ref : -INFINITY;
-                    part_row[D + 1] = l;
+                } else if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(part_row + col + e) =
+                            make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
+                                        __uint_as_float(o[e + 3]));
                 }
             }
-            if (any) {
-                tc_fence_before();
-                mbar_arrive(&bars[B_OFREE0 + x]);
+            if (it.ns > 1 && valid && grp == 0) {
+                part_row[D] = m_ref;
+                part_row[D + 1] = l_row;
             }
+            tc_fence_before();
+            mbar_arrive(&bars[B_OFREE]);
         }
-    } else if (Q8 && warp >= 12) {
+    } else if (Q8) {
         // ------------------------------------------------------------------ dequantise
         setmaxnreg_dec<L::DQ_REGS>();
-        const int r = threadIdx.x - 384;  // key row in the tile
+        const int r0 = threadIdx.x - 384;  // key rows r0 and r0 + 128 of each tile
         constexpr int NB = D / 32;
         uint32_t raw_seq = 0, ring_seq = 0;
         bool ok = true;
+        auto convert = [&](int kv, int k, int g) -> bool {
+            // the scales of my two rows (zero beyond the cache end: TMA zero-fills those codes)
+            uint32_t sw[2][NB / 2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int key = k * BN + r0 + 128 * h;
+                const uint16_t *sp = (kv ? a.vs : a.ks) + a.layer * a.g.s_layer + (int64_t)key * a.g.s_tok +
+                                     g * a.g.s_head;
+#pragma unroll
+                for (int b = 0; b < NB / 2; ++b) sw[h][b] = 0u;
+                if (key < a.kv_len) {
+                    if (NB == 4) {
+                        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(sp));
+                        sw[h][0] = u.x;
+                        sw[h][NB / 2 - 1] = u.y;
+                    } else {
+                        sw[h][0] = __ldg(reinterpret_cast<const uint32_t *>(sp));
+                    }
+                }
+            }
+            const int st = ring_seq % L::NS;
+            if (ring_seq >= (uint32_t)L::NS &&
+                !mbar_wait(&bars[B_RING_EMPTY + st], ((ring_seq / L::NS) - 1) & 1, s_abort))
+                return false;
+            const int rs = raw_seq % L::NR;
+            if (!mbar_wait(&bars[B_RAW_FULL + rs], (raw_seq / L::NR) & 1, s_abort)) return false;
+            const uint8_t *raw = sm + L::OFF_RAW + rs * L::RAW_BYTES;
+            uint8_t *dst = sm + L::OFF_RING + st * L::ST_BYTES;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rr = r0 + 128 * h;
+                uint4 q[D / 16];
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c)
+                    q[c] = *reinterpret_cast<const uint4 *>(raw + ((D == 128) ? sw128(rr, c) : sw64(rr, c)));
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    const int b = c >> 1;
+                    const unsigned short sb = (unsigned short)(sw[h][b >> 1] >> (16 * (b & 1)));
+                    const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
+                    uint32_t o[8];
+                    dequant4(q[c].x, d2, o[0], o[1]);
+                    dequant4(q[c].y, d2, o[2], o[3]);
+                    dequant4(q[c].z, d2, o[4], o[5]);
+                    dequant4(q[c].w, d2, o[6], o[7]);
+                    *reinterpret_cast<uint4 *>(dst + op_off(BN, rr, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(dst + op_off(BN, rr, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+            // order the generic-proxy reads of the raw stage and writes of the operand stage before the
+            // async-proxy accesses that follow (the TMA refill, the MMA)
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+            ++raw_seq;
+            mbar_arrive(&bars[B_RING_FULL + st]);
+            ++ring_seq;
+            return true;
+        };
         for (int i = first_item; ok && i < a.n_items; i += stride) {
             const Item it = decode_item(a, i);
+            ok = convert(0, it.k0, it.g);
             for (int k = it.k0; ok && k < it.k1; ++k) {
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int key = k * BN + r;
-                    const uint16_t *sp = (kv ? a.vs : a.ks) + a.layer * a.g.s_layer + (int64_t)key * a.g.s_tok +
-                                         it.g * a.g.s_head;
-                    uint32_t sw[NB / 2];
-#pragma unroll
-                    for (int b = 0; b < NB / 2; ++b) sw[b] = 0u;
-                    if (key < a.kv_len) {
-                        if (NB == 4) {
-                            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(sp));
-                            sw[0] = u.x;
-                            sw[NB / 2 - 1] = u.y;
-                        } else {
-                            sw[0] = __ldg(reinterpret_cast<const uint32_t *>(sp));
-                        }
-                    }
-                    const int rs = raw_seq % L::NR;
-                    if (!mbar_wait(&bars[B_RAW_FULL + rs], (raw_seq / L::NR) & 1, s_abort)) { ok = false; break; }
-                    const uint8_t *raw = sm + L::OFF_RAW + rs * L::RAW_BYTES;
-                    uint4 rr[D / 16];
-#pragma unroll
-                    for (int c = 0; c < D / 16; ++c)
-                        rr[c] = *reinterpret_cast<const uint4 *>(raw + ((D == 128) ? sw128(r, c) : sw64(r, c)));
-                    // order these generic-proxy reads before the TMA (async proxy) that refills the stage
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bars[B_RAW_EMPTY + rs]);
-                    ++raw_seq;
-                    const int st = ring_seq % L::NS;
-                    if (ring_seq >= (uint32_t)L::NS &&
-                        !mbar_wait(&bars[B_RING_EMPTY + st], ((ring_seq / L::NS) - 1) & 1, s_abort)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *dst = sm + L::OFF_RING + st * L::ST_BYTES;
-#pragma unroll
-                    for (int c = 0; c < D / 16; ++c) {
-                        const int b = c >> 1;
-                        const unsigned short sb = (unsigned short)(sw[b >> 1] >> (16 * (b & 1)));
-                        const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
-                        uint32_t o[8];
-                        dequant4(rr[c].x, d2, o[0], o[1]);
-                        dequant4(rr[c].y, d2, o[2], o[3]);
-                        dequant4(rr[c].z, d2, o[4], o[5]);
-                        dequant4(rr[c].w, d2, o[6], o[7]);
-                        *reinterpret_cast<uint4 *>(dst + op_off(BN, r, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(dst + op_off(BN, r, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bars[B_RING_FULL + st]);
-                    ++ring_seq;
-                }
+                if (k + 1 < it.k1) ok = convert(0, k + 1, it.g);
+                if (ok) ok = convert(1, k, it.g);
             }
         }
     }
@@ -655,26 +668,21 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
 }
 
 // Merge of the key splits: out = sum_s w_s O_s / sum_s w_s l_s, w_s = 2^(m_s - max_s m_s), the
-// splits taken in split order (a split with no visible key has m_s = -inf and weight 0).  A group
-// of D/4 threads per row, 4 columns each; a block covers 256 / (D/4) rows of one Q tile of a pair.
+// splits taken in split order.  A group of D/4 threads per row, 4 columns each; a block covers
+// 256 / (D/4) rows of one unit.
 template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
-    constexpr int TPR = D / 4, RPB = 256 / TPR, BPT = BM / RPB;
-    const int rb = blockIdx.x % BPT, x = (blockIdx.x / BPT) & 1, pg = blockIdx.x / (2 * BPT);
-    const int g = pg / a.J, j = pg % a.J;
-    const int e = 2 * j + x;
-    if (e >= a.U) return;
-    // the pair's split count, as decode_item computes it
-    const int e_last = (2 * j + 1 < a.U) ? 2 * j + 1 : 2 * j;
-    const int T = unit_tl(a, e_last / a.G) / BN + 1;
+    constexpr int TPR = D / 4, RPB = 256 / TPR, BPU = BM / RPB;
+    const int rb = blockIdx.x % BPU, unit = blockIdx.x / BPU;
+    const int qt = unit / a.H_q, h = unit % a.H_q;
+    const int T = unit_tl(a, qt) / BN + 1;
     const int ns = (T + a.ST - 1) / a.ST;
     if (ns <= 1) return;
-    const int qt = e / a.G, h = g * a.G + e % a.G;
     const int r = rb * RPB + threadIdx.x / TPR, c4 = (threadIdx.x % TPR) * 4;
     const int row = qt * BM + r;
     if (row >= a.C) return;
-    const int64_t sstride = 2 * BM * PART_ROW(D);
-    const float *base = a.part + (((int64_t)pg * a.smax * 2 + x) * BM + r) * PART_ROW(D);
+    const int64_t sstride = BM * PART_ROW(D);
+    const float *base = a.part + ((int64_t)unit * a.smax * BM + r) * PART_ROW(D);
     float M = -INFINITY;
 #pragma unroll 4
     for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcs(base + s * sstride + D));
@@ -739,8 +747,8 @@ int sm_count() {
 
 // The work decomposition of one call (see the file comment).
 struct Plan {
-    int G, n_qt, U, J, ST, smax, n_items;
-    int cum[MAX_SPLITS + 1], jmin[MAX_SPLITS];
+    int G, n_qt, ST, smax, n_items;
+    int cum[MAX_SPLITS + 1], qtmin[MAX_SPLITS];
     size_t part_bytes;
 };
 
@@ -758,26 +766,22 @@ int split_tiles(int n_ctx) {
 bool make_plan(const kvc_desc &d, int n_head_q, int pos0, int C, Plan &p) {
     p.G = n_head_q / d.n_head_kv;
     p.n_qt = (C + BM - 1) / BM;
-    p.U = p.n_qt * p.G;
-    p.J = (p.U + 1) / 2;
     p.ST = split_tiles(d.n_ctx);
-    auto T = [&](int j) {
-        const int e = (2 * j + 1 < p.U) ? 2 * j + 1 : p.U - 1;
-        const int qt = e / p.G;
+    auto T = [&](int qt) {
         const int tl = pos0 + ((qt * BM + BM < C) ? qt * BM + BM : C) - 1;
         return tl / BN + 1;
     };
-    p.smax = (T(p.J - 1) + p.ST - 1) / p.ST;
+    p.smax = (T(p.n_qt - 1) + p.ST - 1) / p.ST;
     if (p.smax > MAX_SPLITS) return false;
     p.cum[0] = 0;
-    int j = 0;
+    int qt = 0;
     for (int s = 0; s < p.smax; ++s) {
-        while (j < p.J && T(j) <= s * p.ST) ++j;
-        p.jmin[s] = j;
-        p.cum[s + 1] = p.cum[s] + (p.J - j) * d.n_head_kv;
+        while (qt < p.n_qt && T(qt) <= s * p.ST) ++qt;
+        p.qtmin[s] = qt;
+        p.cum[s + 1] = p.cum[s] + (p.n_qt - qt) * n_head_q;
     }
     p.n_items = p.cum[p.smax];
-    p.part_bytes = (p.smax > 1) ? (size_t)d.n_head_kv * p.J * p.smax * 2 * BM * PART_ROW(d.head_dim) * sizeof(float) : 0;
+    p.part_bytes = (p.smax > 1) ? (size_t)p.n_qt * n_head_q * p.smax * BM * PART_ROW(d.head_dim) * sizeof(float) : 0;
     return true;
 }
 
@@ -830,14 +834,12 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     a.G = p.G;
     a.H_kv = H;
     a.n_qt = p.n_qt;
-    a.U = p.U;
-    a.J = p.J;
     a.ST = p.ST;
     a.smax = p.smax;
     a.n_items = p.n_items;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
     for (int i = 0; i <= MAX_SPLITS; ++i) a.cum[i] = i <= p.smax ? p.cum[i] : p.n_items;
-    for (int i = 0; i < MAX_SPLITS; ++i) a.jmin[i] = i < p.smax ? p.jmin[i] : p.J;
+    for (int i = 0; i < MAX_SPLITS; ++i) a.qtmin[i] = i < p.smax ? p.qtmin[i] : p.n_qt;
     auto kern = prefill_kernel<D, Q8, QDT>;
     static bool attr_set = false;  // per instantiation
     if (!attr_set) {
@@ -848,8 +850,8 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
     kern<<<grid, L::THREADS, L::ALLOC, s>>>(tq, tk, tv, a);
     if (p.smax > 1) {
-        constexpr int BPT = BM / (256 / (D / 4));
-        prefill_merge_kernel<D><<<H * p.J * 2 * BPT, 256, 0, s>>>(a);
+        constexpr int BPU = BM / (256 / (D / 4));
+        prefill_merge_kernel<D><<<p.n_qt * n_head_q * BPU, 256, 0, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
@@ -867,7 +869,7 @@ int launch_d(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
 }  // namespace
 
 size_t prefill_scratch_bytes(const kvc_desc &d, int n_head_q, int max_tokens) {
-    // the largest plan over chunk positions: pairs grow with the chunk, splits with the context
+    // the largest plan over chunk positions: q-tiles grow with the chunk, splits with the context
     Plan p;
     if (!make_plan(d, n_head_q, d.n_ctx - max_tokens, max_tokens, p)) return 0;
     return scratch_need(p);
