@@ -461,35 +461,35 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 if (!mbar_wait(&bars[B_SFULL], s_seq & 1, s_abort)) { ok = false; break; }
                 ++s_seq;
                 tc_fence_after();
-                // my half of the S row in registers (one TMEM round trip), then S may be overwritten
+                // the row max over the whole tile: the other group's half first (read only for the max),
+                // then my half, kept in registers; both groups reach the same max (max is exact in any
+                // order).  Then S may be overwritten.
                 uint32_t s[128];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32p(tS + c * 32, s + c * 32);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&bars[B_SFREE]);
-                const int key0 = k * BN + 128 * grp;
-                if (key0 + 127 > it.tf) {
-#pragma unroll
-                    for (int e = 0; e < 128; ++e)
-                        if (key0 + e > t) s[e] = 0xFF800000u;  // -inf: a key after the query
-                }
-                // row max: 8 independent chains of three-input maxima, then a tree (max is exact in any order)
                 float mx8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+                for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+#pragma unroll 1
+                for (int half = 1; half >= 0; --half) {
+                    const int hg = grp ^ half;
 #pragma unroll
-                for (int e = 8; e < 120; e += 16) {
+                    for (int c = 0; c < 4; ++c) tmem_ld32p(tmem + COL_S + 128 * hg + lane_base + c * 32, s + c * 32);
+                    tmem_ld_wait();
+                    const int key0 = k * BN + 128 * hg;
+                    if (key0 + 127 > it.tf) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        mx8[u] = fmax3(mx8[u], __uint_as_float(s[e + u]), __uint_as_float(s[e + 8 + u]));
+                        for (int e = 0; e < 128; ++e)
+                            if (key0 + e > t) s[e] = 0xFF800000u;  // -inf: a key after the query
+                    }
+#pragma unroll
+                    for (int e = 0; e < 128; e += 16) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            mx8[u] = fmax3(mx8[u], __uint_as_float(s[e + u]), __uint_as_float(s[e + 8 + u]));
+                    }
                 }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], __uint_as_float(s[120 + u]));
-                float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-                float mx_other;
-                if (!exchange(mx, mx_other)) { ok = false; break; }
-                mx = fmaxf(mx, mx_other);
+                tc_fence_before();
+                mbar_arrive(&bars[B_SFREE]);
+                const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 float m_use = m_ref, alpha = 1.f;
                 if (k == it.k0) {
@@ -500,16 +500,24 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 }
                 // -inf scores give p = 0 exactly; a row with no visible key so far uses 0 as its offset
                 const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-                // probabilities as fp16 pairs (exponents by packed fma); the row sum in 4 packed partial
-                // sums, added in a fixed order
-                uint32_t pk[64];
+                // probabilities as fp16 pairs, in three passes over the row so that each pass is a long run
+                // of independent operations: exponents by packed fma (in place), 2^x on the MUFU unit (in
+                // place), then the row sum (4 packed partial sums, added in a fixed order) and fp16 packing
                 const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_sub, -m_sub);
-                uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int e = 0; e < 128; e += 2) {
                     float x0, x1;
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2x2, nm2), x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    s[e] = __float_as_uint(x0);
+                    s[e + 1] = __float_as_uint(x1);
+                }
+#pragma unroll
+                for (int e = 0; e < 128; ++e) s[e] = __float_as_uint(ex2(__uint_as_float(s[e])));
+                uint32_t pk[64];
+                uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int e = 0; e < 128; e += 2) {
+                    const float p0 = __uint_as_float(s[e]), p1 = __uint_as_float(s[e + 1]);
                     rs4[(e >> 1) & 3] = f2_add(rs4[(e >> 1) & 3], f2_pack(p0, p1));
                     pk[e >> 1] = pack_half2(p0, p1);
                 }
@@ -618,7 +626,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             if (!mbar_wait(&bars[B_RAW_FULL + rs], (raw_seq / L::NR) & 1, s_abort)) return false;
             const uint8_t *raw = sm + L::OFF_RAW + rs * L::RAW_BYTES;
             uint8_t *dst = sm + L::OFF_RING + st * L::ST_BYTES;
-#pragma unroll
+#pragma unroll 1  // unrolling both rows doubles the code and stalls on instruction fetch
             for (int h = 0; h < 2; ++h) {
                 const int rr = r0 + 128 * h;
                 uint4 q[D / 16];
