@@ -52,6 +52,9 @@ template <int DT, bool Q8>
 __global__ void __launch_bounds__(256) append_kernel(
     const void *__restrict__ k, const void *__restrict__ v, int64_t n_units, int units_per_tok,
     int units_per_head, void *kq, uint16_t *ks, void *vq, uint16_t *vs, Geom g, int layer, int pos0) {
+    // a kernel launched after this one as a programmatic dependent (the decode split pass) may be
+    // scheduled now; it waits for this grid's completion before it reads the cache
+    asm volatile("griddepcontrol.launch_dependents;");
     const bool is_v = blockIdx.y != 0;
     const void *src = is_v ? v : k;
     const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

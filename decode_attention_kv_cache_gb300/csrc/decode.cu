@@ -8,28 +8,35 @@
 // mode", section "Why"; llama.cpp PR #59 "llama : switch the split mode of a
 // live context", section "Why").
 //
-// Split pass: grid (split, kv head), 4 warps per CTA.  A CTA streams its key
-// range [split*len, (split+1)*len) of one kv head for all G query heads of the
-// group; each warp takes 16-key groups in turn.  The warp computes the group's
+// Split pass: one wave of CTAs, grid (split, kv head), two CTAs per SM.  A CTA
+// streams the key range [split*len, (split+1)*len) of one kv head: warp 0
+// issues TMA copies of 64-key K and V blocks into a ring of shared-memory
+// stages (128-byte swizzle; 64-byte for 64-byte rows), so many stages are in
+// flight at once; four consumer warps each take one 16-key group of a stage
+// for all G query heads of the group.  A consumer warp computes the group's
 // scores with mma.sync m16n8k16 (rows = query heads of the group, columns =
 // keys), keeps an online softmax per head, and accumulates P*V with a second
-// mma.sync (rows = heads, columns = head_dim).  K and V come straight from
-// global memory into registers in the fragment layouts:
+// mma.sync (rows = heads, columns = head_dim), reading its fragments from the
+// stage:
 //   - q8_0 codes are converted to exact fp16 integers with two byte permutes
 //     and one fp16 subtraction; the K scale is applied per 32-value block to
 //     the fp32 partial scores, the V scale is folded into P per block, so the
 //     only rounding besides fp32 accumulation is fp16(p*d);
 //   - f16 values feed the MMAs as stored.
 // Head-dim slots are permuted inside each MMA (the dot product does not care)
-// so that every thread reads 8 (K) or 4 (V) contiguous code bytes per row.
-// The four warps are merged in shared memory in a fixed order and the CTA
-// writes (m, l, O) for its range to the scratch buffer.
+// so that every thread reads 8 or 16 (K) and 4 or 8 (V) contiguous bytes per
+// row.  The four warps are merged in shared memory in a fixed order and the
+// CTA writes (m, l, O) for its range to the scratch buffer.
 //
-// Combine pass: one CTA per query head, one thread per output value; merges
-// the splits in split order (deterministic) and divides by the softmax sum.
+// Combine pass: launched with programmatic dependent launch, so its CTAs are
+// resident while the split pass runs and wait for it on the device
+// (griddepcontrol.wait); one CTA per query head merges the splits in split
+// order (deterministic) and divides by the softmax sum.
 //
 // Split boundaries are absolute key positions, so the result does not depend
-// on the cache layout.  No inter-CTA waits.
+// on the cache layout.  Every mbarrier wait is bounded (2 s); a wait that gives
+// up sets the device status word and the CTA skips its remaining work.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -41,9 +48,44 @@
 namespace kvc {
 namespace {
 
+// set by a split pass that gave up a bounded wait (read and cleared with the other kernels' status)
+__device__ int g_decode_status;
+
+using namespace ptx;
+
 constexpr int MAX_SPLIT = 256;
-constexpr int WARPS = 4;
-constexpr int GROUP_KEYS = 16;
+constexpr int CWARPS = 4;                          // consumer warps
+constexpr int GROUP_KEYS = 16;                     // keys per consumer warp and stage
+constexpr int STAGE_KEYS = CWARPS * GROUP_KEYS;    // keys per stage
+constexpr int CTAS_PER_SM = 2;
+
+template <int D, bool Q8>
+struct DCfg {
+    static constexpr int ROW = Q8 ? D : 2 * D;             // bytes of one key row
+    static constexpr int BLK_ROW = Q8 ? D : 128;            // bytes per row of one swizzled column block
+    static constexpr int NBLK = ROW / BLK_ROW;              // column blocks of a K or V tile
+    static constexpr int HALF = STAGE_KEYS * ROW;           // K (or V) bytes of a stage
+    static constexpr int STAGE = 2 * HALF;
+    static constexpr int NST = (96 * 1024) / STAGE;          // ring stages (two CTAs per SM)
+    static constexpr int OFF_BAR = NST * STAGE;
+    static constexpr int USED = OFF_BAR + 2 * NST * 8 + 16;
+    static constexpr int ALLOC = USED + 1024;                // room to align the ring to 1024 bytes
+    // the warps' partial results, merged at the end, reuse the ring
+    static constexpr int MERGE = CWARPS * 16 * (D + 2) * 4;
+    static_assert(MERGE <= OFF_BAR, "merge buffers must fit in the ring");
+    static_assert(NST >= 2, "ring too small");
+};
+
+// Byte offset, within one K or V tile of a stage, of byte c of key row r (TMA 128- or 64-byte swizzle).
+template <int D, bool Q8>
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+    using L = DCfg<D, Q8>;
+    const int blk = c / L::BLK_ROW, cb = c % L::BLK_ROW;
+    if constexpr (L::BLK_ROW == 128)
+        return (uint32_t)(blk * (STAGE_KEYS * 128) + r * 128 + ((((cb >> 4) ^ (r & 7))) << 4) + (cb & 15));
+    else
+        return (uint32_t)(blk * (STAGE_KEYS * 64) + r * 64 + ((((cb >> 4) ^ ((r >> 1) & 3))) << 4) + (cb & 15));
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -78,9 +120,7 @@ __device__ __forceinline__ float load_q(const void *q, int64_t i) {
 
 struct DecodeArgs {
     const void *q;
-    const void *kq;
     const uint16_t *ks;
-    const void *vq;
     const uint16_t *vs;
     float *part;       // scratch
     Geom g;
@@ -88,17 +128,22 @@ struct DecodeArgs {
     float scale_log2;
 };
 
-// Per-group register tiles loaded ahead of use.
+// One consumer warp's fragments of a 16-key group.
 template <int D, bool Q8>
 struct Tiles {
     static constexpr int NB = D / 32;
     // K: [n-tile t][block b] 8 code bytes (q8_0) or 8 halves (f16)
-    uint2 k8[2][NB];
+    uint2 k8[Q8 ? 2 : 1][Q8 ? NB : 1];
     uint4 k16[Q8 ? 1 : 2][Q8 ? 1 : NB];
     // V: [key r][block b] 4 code bytes (q8_0) or 4 halves (f16)
-    uint32_t v8[4][NB];
+    uint32_t v8[Q8 ? 4 : 1][Q8 ? NB : 1];
     uint2 v16[Q8 ? 1 : 4][Q8 ? 1 : NB];
-    // scales of keys j0+4c+r: NB fp16 values packed two per word
+};
+
+// scales of keys j0+4c+r: NB fp16 values packed two per word
+template <int D>
+struct Scales {
+    static constexpr int NB = D / 32;
     uint32_t sk[4][NB / 2], sv[4][NB / 2];
     __device__ __forceinline__ float kscale(int r, int b) const {
         return __half2float(__ushort_as_half((unsigned short)(sk[r][b >> 1] >> (16 * (b & 1)))));
@@ -108,218 +153,310 @@ struct Tiles {
     }
 };
 
-template <int D, bool Q8>
-__device__ __forceinline__ void load_group(const DecodeArgs &a, int hkv, int j0, int gq, int cq,
-                                           Tiles<D, Q8> &T) {
+template <int D>
+__device__ __forceinline__ void load_scales(const DecodeArgs &a, int hkv, int j0, int cq, Scales<D> &S) {
     constexpr int NB = D / 32;
     const int last = a.n_keys - 1;
-    const int64_t base_c = a.layer * a.g.c_layer + hkv * a.g.c_head;
     const int64_t base_s = a.layer * a.g.s_layer + hkv * a.g.s_head;
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int key = min(j0 + 4 * (gq >> 1) + 2 * t + (gq & 1), last);
-        const int64_t row = base_c + (int64_t)key * a.g.c_tok;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            if constexpr (Q8)
-                T.k8[t][b] = __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(a.kq) + row + 32 * b + 8 * cq));
-            else
-                T.k16[t][b] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.kq) + row + 32 * b + 8 * cq));
+    for (int r = 0; r < 4; ++r) {
+        // a key's NB scales are contiguous and 2*NB-byte aligned; keys past the end reuse the last
+        // key's (their codes are zero-filled and their scores masked)
+        const int key = min(j0 + 4 * cq + r, last);
+        const int64_t srow = base_s + (int64_t)key * a.g.s_tok;
+        if constexpr (NB == 4) {
+            const uint2 wk = __ldg(reinterpret_cast<const uint2 *>(a.ks + srow));
+            const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(a.vs + srow));
+            S.sk[r][0] = wk.x; S.sk[r][1] = wk.y;
+            S.sv[r][0] = wv.x; S.sv[r][1] = wv.y;
+        } else {
+            S.sk[r][0] = __ldg(reinterpret_cast<const uint32_t *>(a.ks + srow));
+            S.sv[r][0] = __ldg(reinterpret_cast<const uint32_t *>(a.vs + srow));
         }
     }
+}
+
+// The group's K fragments from stage `sb`: rows 16*cw .. 16*cw + 15 of its K tile.
+template <int D, bool Q8>
+__device__ __forceinline__ void load_group_k(const uint8_t *sb, int cw, int gq, int cq, Tiles<D, Q8> &T) {
+    constexpr int NB = D / 32;
+    const uint8_t *kb = sb;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int key = min(j0 + 4 * cq + r, last);
-        const int64_t row = base_c + (int64_t)key * a.g.c_tok;
+    for (int t = 0; t < 2; ++t) {
+        const int row = GROUP_KEYS * cw + 4 * (gq >> 1) + 2 * t + (gq & 1);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             if constexpr (Q8)
-                T.v8[r][b] = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const int8_t *>(a.vq) + row + 32 * b + 4 * gq));
+                T.k8[t][b] = *reinterpret_cast<const uint2 *>(kb + tile_off<D, Q8>(row, 32 * b + 8 * cq));
             else
-                T.v16[r][b] = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.vq) + row + 32 * b + 4 * gq));
+                T.k16[t][b] = *reinterpret_cast<const uint4 *>(kb + tile_off<D, Q8>(row, 2 * (32 * b + 8 * cq)));
         }
-        if constexpr (Q8) {
-            // a key's NB scales are contiguous and 2*NB-byte aligned
-            const int64_t srow = base_s + (int64_t)key * a.g.s_tok;
-            if constexpr (NB == 4) {
-                const uint2 wk = __ldg(reinterpret_cast<const uint2 *>(a.ks + srow));
-                const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(a.vs + srow));
-                T.sk[r][0] = wk.x; T.sk[r][1] = wk.y;
-                T.sv[r][0] = wv.x; T.sv[r][1] = wv.y;
-            } else {
-                T.sk[r][0] = __ldg(reinterpret_cast<const uint32_t *>(a.ks + srow));
-                T.sv[r][0] = __ldg(reinterpret_cast<const uint32_t *>(a.vs + srow));
-            }
+    }
+}
+
+// The group's V fragments from stage `sb`: rows 16*cw .. 16*cw + 15 of its V tile.
+template <int D, bool Q8>
+__device__ __forceinline__ void load_group_v(const uint8_t *sb, int cw, int gq, int cq, Tiles<D, Q8> &T) {
+    constexpr int NB = D / 32;
+    const uint8_t *vb = sb + DCfg<D, Q8>::HALF;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int row = GROUP_KEYS * cw + 4 * cq + r;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if constexpr (Q8)
+                T.v8[r][b] = *reinterpret_cast<const uint32_t *>(vb + tile_off<D, Q8>(row, 32 * b + 4 * gq));
+            else
+                T.v16[r][b] = *reinterpret_cast<const uint2 *>(vb + tile_off<D, Q8>(row, 2 * (32 * b + 4 * gq)));
         }
     }
 }
 
 template <int D, bool Q8, int DT>
-__global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodeArgs a) {
+__global__ void __maxnreg__(200)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const DecodeArgs a) {
+    using L = DCfg<D, Q8>;
     constexpr int NB = D / 32;
     constexpr int KS = D / 16;       // k-steps of the score MMA
     constexpr int NT = D / 8;        // n-tiles of the output MMA
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+    uint64_t *empty = full + L::NST;
+    volatile int *s_abort = reinterpret_cast<volatile int *>(empty + L::NST);
     const int split = blockIdx.x, hkv = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, cq = lane & 3;
     const int G = a.group;
     const int j_begin = split * a.split_len;
     const int j_end = min(a.n_keys, j_begin + a.split_len);
+    const int n_stages = (j_end - j_begin + STAGE_KEYS - 1) / STAGE_KEYS;
 
-    // Q as the A operand of the score MMA: rows = heads of the group; in k-step
-    // s = 2b + e this thread's four head-dim slots are d0..d0+3, d0 = 32b + 8c + 4e.
-    uint32_t qa[KS][4];
-#pragma unroll
-    for (int s = 0; s < KS; ++s) {
-        const int d0 = 32 * (s >> 1) + 8 * cq + 4 * (s & 1);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int row = gq + 8 * half;
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-            if (row < G) {
-                const int64_t base = ((int64_t)hkv * G + row) * D + d0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = load_q<DT>(a.q, base + i);
-            }
-            qa[s][half] = pack_half2(x[0], x[1]);       // a0a1 / a2a3: slots 2c, 2c+1
-            qa[s][2 + half] = pack_half2(x[2], x[3]);   // a4a5 / a6a7: slots 2c+8, 2c+9
+    if (threadIdx.x == 0) {
+        *s_abort = 0;
+        for (int i = 0; i < L::NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], CWARPS);
         }
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
     }
+    __syncthreads();
+    // inputs written by the kernels before this one are read only past this point; the combine
+    // pass may be scheduled from here on (it waits for this grid to finish)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float o[NT][4];
 #pragma unroll
     for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-    Tiles<D, Q8> cur, nxt;
-    int j0 = j_begin + warp * GROUP_KEYS;
-    if (j0 < j_end) load_group<D, Q8>(a, hkv, j0, gq, cq, cur);
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            int i = 0;
+            for (; i < n_stages; ++i) {
+                const int st = i % L::NST;
+                if (i >= L::NST && !mbar_wait(&empty[st], ((i / L::NST) - 1) & 1, s_abort)) break;
+                mbar_arrive_expect_tx(&full[st], L::STAGE);
+                const int j = j_begin + i * STAGE_KEYS;
+                uint8_t *dst = sm + st * L::STAGE;
+                constexpr int ELEMS = Q8 ? L::BLK_ROW : L::BLK_ROW / 2;  // elements per block row
+#pragma unroll
+                for (int blk = 0; blk < L::NBLK; ++blk) {
+                    tma_load_3d(dst + blk * (STAGE_KEYS * L::BLK_ROW), &tm_k, &full[st], blk * ELEMS, j, hkv);
+                    tma_load_3d(dst + L::HALF + blk * (STAGE_KEYS * L::BLK_ROW), &tm_v, &full[st], blk * ELEMS, j,
+                                hkv);
+                }
+            }
+            if (*s_abort) {
+                // after a wait gave up: let the copies still in flight land before the CTA exits
+                volatile int never = 0;
+                for (int st = 0; st < L::NST && st < i; ++st) {
+                    const int last = st + ((i - 1 - st) / L::NST) * L::NST;
+                    mbar_wait(&full[st], (last / L::NST) & 1, &never, 200000000ull);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ consumers
+        const int cw = warp - 1;
+        const int gq = lane >> 2, cq = lane & 3;
+        // Q as the A operand of the score MMA: rows = heads of the group; in k-step
+        // s = 2b + e this thread's four head-dim slots are d0..d0+3, d0 = 32b + 8c + 4e.
+        uint32_t qa[KS][4];
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            const int d0 = 32 * (s >> 1) + 8 * cq + 4 * (s & 1);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int row = gq + 8 * half;
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
+                if (row < G) {
+                    const int64_t base = ((int64_t)hkv * G + row) * D + d0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) x[i] = load_q<DT>(a.q, base + i);
+                }
+                qa[s][half] = pack_half2(x[0], x[1]);       // a0a1 / a2a3: slots 2c, 2c+1
+                qa[s][2 + half] = pack_half2(x[2], x[3]);   // a4a5 / a6a7: slots 2c+8, 2c+9
+            }
+        }
+        Scales<D> sc_cur, sc_nxt;
+        if (Q8 && n_stages > 0) load_scales<D>(a, hkv, j_begin + cw * GROUP_KEYS, cq, sc_cur);
 #pragma unroll 1
-    for (; j0 < j_end; j0 += WARPS * GROUP_KEYS) {
-        const int jn = j0 + WARPS * GROUP_KEYS;
-        if (jn < j_end) load_group<D, Q8>(a, hkv, jn, gq, cq, nxt);
-
-        // ---- scores: sc[t][i] for keys j0 + 4c + 2t + (i & 1), heads gq (i < 2) and gq + 8
-        float sc[2][4];
+        for (int i = 0; i < n_stages; ++i) {
+            const int st = i % L::NST;
+            const int j0 = j_begin + i * STAGE_KEYS + cw * GROUP_KEYS;
+            if (Q8 && i + 1 < n_stages) load_scales<D>(a, hkv, j0 + STAGE_KEYS, cq, sc_nxt);
+            if (!mbar_wait(&full[st], (i / L::NST) & 1, s_abort)) break;
+            Tiles<D, Q8> cur;
+            const uint8_t *sb = sm + st * L::STAGE;
+            // K fragments now, V fragments after the softmax (fewer live registers); the stage is
+            // released once both are read
+            load_group_k<D, Q8>(sb, cw, gq, cq, cur);
+            if (j0 < j_end) {
+                // ---- scores: sc[t][i] for keys j0 + 4c + 2t + (i & 1), heads gq (i < 2) and gq + 8
+                float sc[2][4];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-            if constexpr (Q8) {
+                for (int t = 0; t < 2; ++t) {
+                    sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+                    if constexpr (Q8) {
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    const uint32_t w0 = cur.k8[t][b].x, w1 = cur.k8[t][b].y;
-                    mma16816(acc, qa[2 * b], codes_to_half2(__byte_perm(w0, 0, 0x0100)),
-                             codes_to_half2(__byte_perm(w0, 0, 0x0302)));
-                    mma16816(acc, qa[2 * b + 1], codes_to_half2(__byte_perm(w1, 0, 0x0100)),
-                             codes_to_half2(__byte_perm(w1, 0, 0x0302)));
+                        for (int b = 0; b < NB; ++b) {
+                            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                            const uint32_t w0 = cur.k8[t][b].x, w1 = cur.k8[t][b].y;
+                            mma16816(acc, qa[2 * b], codes_to_half2(__byte_perm(w0, 0, 0x0100)),
+                                     codes_to_half2(__byte_perm(w0, 0, 0x0302)));
+                            mma16816(acc, qa[2 * b + 1], codes_to_half2(__byte_perm(w1, 0, 0x0100)),
+                                     codes_to_half2(__byte_perm(w1, 0, 0x0302)));
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        sc[t][i] += cur.kscale(2 * t + (i & 1), b) * acc[i];
+                            for (int e = 0; e < 4; ++e)
+                                sc[t][e] += sc_cur.kscale(2 * t + (e & 1), b) * acc[e];
+                        }
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            mma16816(sc[t], qa[2 * b], cur.k16[t][b].x, cur.k16[t][b].y);
+                            mma16816(sc[t], qa[2 * b + 1], cur.k16[t][b].z, cur.k16[t][b].w);
+                        }
+                    }
+                }
+                // ---- online softmax (log2 domain), rows gq and gq + 8
+                float p[2][4];
+                float alpha[2];
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    float x[4];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int key = j0 + 4 * cq + 2 * t + e;
+                            x[2 * t + e] = key < j_end ? sc[t][2 * hr + e] * a.scale_log2 : -INFINITY;
+                        }
+                    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_new = fmaxf(m_run[hr], mx);  // finite: key j0 < j_end is visible
+                    alpha[hr] = ex2(m_run[hr] - m_new);
+                    float rs = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        p[hr][e] = ex2(x[e] - m_new);
+                        rs += p[hr][e];
+                    }
+                    l_run[hr] = l_run[hr] * alpha[hr] + rs;
+                    m_run[hr] = m_new;
+                }
+                if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
+                        o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
+                    }
+                }
+                load_group_v<D, Q8>(sb, cw, gq, cq, cur);
+                // order the stage reads before the TMA (async proxy) that refills it
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+                // ---- O += P V.  A = P (rows heads, k-slots 2c, 2c+1 <- keys 4c, 4c+1; 2c+8, 2c+9 <- 4c+2, 4c+3)
+                //      B = V (k-slots as above, column n of n-tile 4b + s <- head-dim 32b + 4n + s)
+                if constexpr (Q8) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        float dv[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) dv[r] = sc_cur.vscale(r, b);
+                        uint32_t pa[4];
+                        pa[0] = pack_half2(p[0][0] * dv[0], p[0][1] * dv[1]);
+                        pa[1] = pack_half2(p[1][0] * dv[0], p[1][1] * dv[1]);
+                        pa[2] = pack_half2(p[0][2] * dv[2], p[0][3] * dv[3]);
+                        pa[3] = pack_half2(p[1][2] * dv[2], p[1][3] * dv[3]);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const uint32_t sel = (uint32_t)s | ((uint32_t)(4 + s) << 8);
+                            const uint32_t b0 = codes_to_half2(__byte_perm(cur.v8[0][b], cur.v8[1][b], sel));
+                            const uint32_t b1 = codes_to_half2(__byte_perm(cur.v8[2][b], cur.v8[3][b], sel));
+                            mma16816(o[4 * b + s], pa, b0, b1);
+                        }
+                    }
+                } else {
+                    uint32_t pa[4];
+                    pa[0] = pack_half2(p[0][0], p[0][1]);
+                    pa[1] = pack_half2(p[1][0], p[1][1]);
+                    pa[2] = pack_half2(p[0][2], p[0][3]);
+                    pa[3] = pack_half2(p[1][2], p[1][3]);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const uint32_t sel = (s & 1) ? 0x7632u : 0x5410u;
+                            const uint32_t w0 = (s < 2) ? cur.v16[0][b].x : cur.v16[0][b].y;
+                            const uint32_t w1 = (s < 2) ? cur.v16[1][b].x : cur.v16[1][b].y;
+                            const uint32_t w2 = (s < 2) ? cur.v16[2][b].x : cur.v16[2][b].y;
+                            const uint32_t w3 = (s < 2) ? cur.v16[3][b].x : cur.v16[3][b].y;
+                            mma16816(o[4 * b + s], pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
+                        }
+                    }
                 }
             } else {
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    mma16816(sc[t], qa[2 * b], cur.k16[t][b].x, cur.k16[t][b].y);
-                    mma16816(sc[t], qa[2 * b + 1], cur.k16[t][b].z, cur.k16[t][b].w);
-                }
+                // a group past the end of the range: release the stage without computing
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
             }
+            if (Q8) sc_cur = sc_nxt;
         }
-        // ---- online softmax (log2 domain), rows gq and gq + 8
-        float p[2][4];
-        float alpha[2];
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            float x[4];
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = j0 + 4 * cq + 2 * t + e;
-                    x[2 * t + e] = key < j_end ? sc[t][2 * hr + e] * a.scale_log2 : -INFINITY;
-                }
-            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run[hr], mx);  // finite: key j0 < j_end is visible
-            alpha[hr] = ptx::ex2(m_run[hr] - m_new);
-            float rs = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                p[hr][i] = ptx::ex2(x[i] - m_new);
-                rs += p[hr][i];
-            }
-            l_run[hr] = l_run[hr] * alpha[hr] + rs;
-            m_run[hr] = m_new;
-        }
-        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-            for (int i = 0; i < NT; ++i) {
-                o[i][0] *= alpha[0]; o[i][1] *= alpha[0];
-                o[i][2] *= alpha[1]; o[i][3] *= alpha[1];
-            }
-        }
-        // ---- O += P V.  A = P (rows heads, k-slots 2c, 2c+1 <- keys 4c, 4c+1; 2c+8, 2c+9 <- 4c+2, 4c+3)
-        //      B = V (k-slots as above, column n of n-tile 4b + s <- head-dim 32b + 4n + s)
-        if constexpr (Q8) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                float dv[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) dv[r] = cur.vscale(r, b);
-                uint32_t pa[4];
-                pa[0] = pack_half2(p[0][0] * dv[0], p[0][1] * dv[1]);
-                pa[1] = pack_half2(p[1][0] * dv[0], p[1][1] * dv[1]);
-                pa[2] = pack_half2(p[0][2] * dv[2], p[0][3] * dv[3]);
-                pa[3] = pack_half2(p[1][2] * dv[2], p[1][3] * dv[3]);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint32_t sel = (uint32_t)s | ((uint32_t)(4 + s) << 8);
-                    const uint32_t b0 = codes_to_half2(__byte_perm(cur.v8[0][b], cur.v8[1][b], sel));
-                    const uint32_t b1 = codes_to_half2(__byte_perm(cur.v8[2][b], cur.v8[3][b], sel));
-                    mma16816(o[4 * b + s], pa, b0, b1);
-                }
-            }
-        } else {
-            uint32_t pa[4];
-            pa[0] = pack_half2(p[0][0], p[0][1]);
-            pa[1] = pack_half2(p[1][0], p[1][1]);
-            pa[2] = pack_half2(p[0][2], p[0][3]);
-            pa[3] = pack_half2(p[1][2], p[1][3]);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint32_t sel = (s & 1) ? 0x7632u : 0x5410u;
-                    const uint32_t w0 = (s < 2) ? cur.v16[0][b].x : cur.v16[0][b].y;
-                    const uint32_t w1 = (s < 2) ? cur.v16[1][b].x : cur.v16[1][b].y;
-                    const uint32_t w2 = (s < 2) ? cur.v16[2][b].x : cur.v16[2][b].y;
-                    const uint32_t w3 = (s < 2) ? cur.v16[3][b].x : cur.v16[3][b].y;
-                    mma16816(o[4 * b + s], pa, __byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel));
-                }
-            }
-        }
-        cur = nxt;
     }
 
-    // ---- merge the four warps in shared memory (fixed order) and write the CTA's partial
-    __shared__ float s_m[WARPS][16], s_l[WARPS][16];
-    __shared__ float s_o[WARPS][16][D];
+    // ---- merge the consumer warps in shared memory (fixed order) and write the CTA's partial;
+    // the buffers reuse the ring, whose copies have all been consumed
+    __syncthreads();
+    float *s_m = reinterpret_cast<float *>(sm);
+    float *s_l = s_m + CWARPS * 16;
+    float *s_o = s_l + CWARPS * 16;   // [warp][row][D]
+    if (warp > 0) {
+        const int cw = warp - 1, gq = lane >> 2, cq = lane & 3;
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        float l = l_run[hr];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        const int row = gq + 8 * hr;
-        if (cq == 0) {
-            s_m[warp][row] = m_run[hr];
-            s_l[warp][row] = l;
-        }
+        for (int hr = 0; hr < 2; ++hr) {
+            float l = l_run[hr];
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            const int row = gq + 8 * hr;
+            if (cq == 0) {
+                s_m[cw * 16 + row] = m_run[hr];
+                s_l[cw * 16 + row] = l;
+            }
 #pragma unroll
-        for (int i = 0; i < NT; ++i) {
-            const int b = i >> 2, s = i & 3;
-            s_o[warp][row][32 * b + 8 * cq + s] = o[i][2 * hr];
-            s_o[warp][row][32 * b + 8 * cq + 4 + s] = o[i][2 * hr + 1];
+            for (int n = 0; n < NT; ++n) {
+                const int b = n >> 2, s = n & 3;
+                s_o[(cw * 16 + row) * D + 32 * b + 8 * cq + s] = o[n][2 * hr];
+                s_o[(cw * 16 + row) * D + 32 * b + 8 * cq + 4 + s] = o[n][2 * hr + 1];
+            }
         }
     }
     __syncthreads();
@@ -330,14 +467,14 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodeAr
         const int row = e / D, d = e % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) M = fmaxf(M, s_m[w][row]);
+        for (int w = 0; w < CWARPS; ++w) M = fmaxf(M, s_m[w * 16 + row]);
         float acc = 0.f, lsum = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < WARPS; ++w) {
-                const float f = ptx::ex2(s_m[w][row] - M);
-                acc += f * s_o[w][row][d];
-                lsum += f * s_l[w][row];
+            for (int w = 0; w < CWARPS; ++w) {
+                const float f = ex2(s_m[w * 16 + row] - M);
+                acc += f * s_o[(w * 16 + row) * D + d];
+                lsum += f * s_l[w * 16 + row];
             }
         }
         part_o[(pbase + row) * D + d] = acc;
@@ -346,19 +483,24 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(const DecodeAr
             part_ml[(pbase + row) * 2 + 1] = lsum;
         }
     }
+    if (threadIdx.x == 0 && *s_abort) atomicExch(&g_decode_status, 1);
 }
 
-// One CTA per query head, one thread per output value.  The split maxima and
-// weights are computed once per CTA in shared memory; each thread then sums its
-// value over the splits in split order (independent loads, unrolled).
+// One CTA per query head, one thread per output value.  The split maxima,
+// weights and weighted softmax denominators are computed in parallel into shared
+// memory; the denominators are then added in split order by one thread (from
+// shared memory), and each thread sums its value over the splits in split order
+// (independent loads, unrolled), so the result is deterministic.
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ part, int n_split,
                                                            int group, int n_head_kv, float *__restrict__ out) {
-    __shared__ float s_w[MAX_SPLIT];
+    __shared__ float s_w[MAX_SPLIT], s_wl[MAX_SPLIT];
     __shared__ float s_red[D / 32];
     __shared__ float s_M, s_L;
     const int h = blockIdx.x, d = threadIdx.x;
     const int hkv = h / group, row = h % group;
+    // launched as a programmatic dependent of the split pass: wait until its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *part_o = part;
     const float *part_ml = part + (int64_t)n_head_kv * MAX_SPLIT * group * D;
     const int64_t p0 = ((int64_t)hkv * MAX_SPLIT) * group + row;   // partial index of split 0
@@ -375,15 +517,17 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     }
     __syncthreads();
     const float M = s_M;
-    // split weights; the sum of weighted softmax denominators in split order
+    // split weights and weighted denominators
     for (int i = d; i < n_split; i += D) {
-        const float mi = part_ml[(p0 + (int64_t)i * group) * 2];
-        s_w[i] = (mi == -INFINITY) ? 0.f : ptx::ex2(mi - M);
+        const float2 ml = *reinterpret_cast<const float2 *>(part_ml + (p0 + (int64_t)i * group) * 2);
+        const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+        s_w[i] = w;
+        s_wl[i] = w * ml.y;
     }
     __syncthreads();
     if (d == 0) {
         float L = 0.f;
-        for (int i = 0; i < n_split; ++i) L += s_w[i] * part_ml[(p0 + (int64_t)i * group) * 2 + 1];
+        for (int i = 0; i < n_split; ++i) L += s_wl[i];
         s_L = L;
     }
     float acc = 0.f;
@@ -400,26 +544,526 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     out[(int64_t)h * D + d] = acc / s_L;
 }
 
-int sm_count() {
-    static int n = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 148;
-    });
-    return n;
+// ---- tensor-core split pass for head_dim 128 ---------------------------------------------
+// Tiles of 128 keys.  S^T = K Q^T with M = 128 keys, N = 16 (the G query heads of the group,
+// zero-padded), both operands in shared memory; O^T += V^T P^T with M = 128 head-dim rows, N = 16,
+// V as an MN-major operand and P^T written to shared memory by the softmax threads.  Accumulators
+// live in tensor memory (S double-buffered), so the warps hold no MMA state.
+//   warp 0      TMA producer: K and V tiles (f16) or their int8 codes (q8_0)
+//   warp 1      allocates TMEM; one lane issues the MMAs: S(0), S(1), then per tile PV(k), S(k+2)
+//   warps 2-5   softmax: thread = key of the tile (TMEM lane); per-head tile maxima are combined
+//               across the four warps through shared memory; P^T to shared memory; O^T rescaled
+//               (thread = head-dim row) when a running max grows by more than 2^8
+//   warps 6-9   (q8_0) dequantise K and V rows into fp16 d*q, separate K and V rings
+constexpr int TK = 128;                 // keys per tile
+constexpr int NH = 16;                  // MMA N: query heads of a group, padded
+constexpr uint32_t TC_COLS = 64;        // TMEM: S double buffer (2 x 16) and O^T (16)
+constexpr uint32_t COL_O = 32;
+constexpr float TC_RESCALE_LOG2 = 8.0f;
+
+template <bool Q8>
+struct TCfg {
+    static constexpr int D = 128;
+    static constexpr int OPT = TK * D * 2;                 // one fp16 K or V tile: 32 KB
+    static constexpr int RAWT = 2 * TK * D;                // int8 K and V codes of a tile: 32 KB
+    static constexpr int NK = Q8 ? 2 : 3, NV = Q8 ? 2 : 3, NR = Q8 ? 2 : 0;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + NK * OPT;
+    static constexpr int OFF_RAW = OFF_V + NV * OPT;
+    static constexpr int OFF_QT = OFF_RAW + NR * RAWT;      // Q^T operand: 16 rows x 128, 4 KB
+    static constexpr int OFF_PT = OFF_QT + NH * D * 2;      // two P^T operands: 16 rows x 128 keys
+    static constexpr int OFF_RED = OFF_PT + 2 * NH * TK * 2;  // [parity][warp][head] floats
+    static constexpr int OFF_BAR = OFF_RED + 2 * 4 * NH * 4;
+    static constexpr int USED = OFF_BAR + 512;
+    static constexpr int ALLOC = USED + 1024;
+    static_assert(ALLOC <= 232448, "shared memory plan too large");
+    static constexpr int THREADS = Q8 ? 320 : 192;
+};
+
+enum TcBar {
+    T_QREADY, T_SFULL0, T_SFULL1, T_PFULL0, T_PFULL1, T_ODONE0, T_ODONE1, T_XCHG, T_DRAIN,
+    T_KFULL, T_KEMPTY = T_KFULL + 4, T_VFULL = T_KEMPTY + 4, T_VEMPTY = T_VFULL + 4, T_RFULL = T_VEMPTY + 4,
+    T_REMPTY = T_RFULL + 4, T_NBAR = T_REMPTY + 4
+};
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+    uint32_t u[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr));
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
+}
+__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(r[0])), "r"(__float_as_uint(r[1])), "r"(__float_as_uint(r[2])), "r"(__float_as_uint(r[3])),
+        "r"(__float_as_uint(r[4])), "r"(__float_as_uint(r[5])), "r"(__float_as_uint(r[6])), "r"(__float_as_uint(r[7])),
+        "r"(__float_as_uint(r[8])), "r"(__float_as_uint(r[9])), "r"(__float_as_uint(r[10])), "r"(__float_as_uint(r[11])),
+        "r"(__float_as_uint(r[12])), "r"(__float_as_uint(r[13])), "r"(__float_as_uint(r[14])), "r"(__float_as_uint(r[15]))
+        : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    umma_f16_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled block of 128-byte rows
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+// 4 int8 codes times the fp16 scale, as two fp16x2 words (one rounding each): the sign bit flipped
+// makes each code q + 128 as an unsigned byte, which under the high byte 0x64 is the fp16 value
+// 1024 + q + 128 (exact); subtracting 1152 leaves q
+__device__ __forceinline__ void dequant4(uint32_t w, __half2 d2, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    __half2 ra = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&a), bias), d2);
+    __half2 rb = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b), bias), d2);
+    lo = *reinterpret_cast<uint32_t *>(&ra);
+    hi = *reinterpret_cast<uint32_t *>(&rb);
+}
+
+// GM: heads the softmax loops cover (8 when the group has at most 8 query heads, else 16)
+template <bool Q8, int DT, int GM>
+__global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const DecodeArgs a) {
+    using L = TCfg<Q8>;
+    constexpr int D = 128;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + T_NBAR);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    float *s_red = reinterpret_cast<float *>(sm + L::OFF_RED);
+    const int split = blockIdx.x, hkv = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = a.group;
+    const int j_begin = split * a.split_len;
+    const int j_end = min(a.n_keys, j_begin + a.split_len);
+    const int T = (j_end - j_begin + TK - 1) / TK;   // tiles of this split
+
+    if (threadIdx.x == 0) {
+        *s_abort = 0;
+        mbar_init(&bars[T_QREADY], 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[T_SFULL0 + b], 1);
+            mbar_init(&bars[T_PFULL0 + b], 128);
+            mbar_init(&bars[T_ODONE0 + b], 1);
+        }
+        mbar_init(&bars[T_XCHG], 128);
+        mbar_init(&bars[T_DRAIN], 1);
+        for (int s = 0; s < L::NK; ++s) {
+            mbar_init(&bars[T_KFULL + s], Q8 ? 128 : 1);
+            mbar_init(&bars[T_KEMPTY + s], 1);
+        }
+        for (int s = 0; s < L::NV; ++s) {
+            mbar_init(&bars[T_VFULL + s], Q8 ? 128 : 1);
+            mbar_init(&bars[T_VEMPTY + s], 1);
+        }
+        if constexpr (Q8) {
+            for (int s = 0; s < L::NR; ++s) {
+                mbar_init(&bars[T_RFULL + s], 1);
+                mbar_init(&bars[T_REMPTY + s], 128);
+            }
+        }
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, TC_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    // inputs written by the kernels before this one are read only past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            int kn = 0, vn = 0;   // tiles whose K (or raw) and V copies have been issued
+            for (int k = 0; k < T; ++k) {
+                const int j = j_begin + k * TK;
+                if constexpr (Q8) {
+                    const int rs = k % L::NR;
+                    if (k >= L::NR && !mbar_wait(&bars[T_REMPTY + rs], ((k / L::NR) - 1) & 1, s_abort)) break;
+                    uint8_t *dst = sm + L::OFF_RAW + rs * L::RAWT;
+                    mbar_arrive_expect_tx(&bars[T_RFULL + rs], L::RAWT);
+                    tma_load_3d(dst, &tm_k, &bars[T_RFULL + rs], 0, j, hkv);
+                    tma_load_3d(dst + TK * D, &tm_v, &bars[T_RFULL + rs], 0, j, hkv);
+                    ++kn;
+                } else {
+                    const int ks = k % L::NK, vs = k % L::NV;
+                    if (k >= L::NK && !mbar_wait(&bars[T_KEMPTY + ks], ((k / L::NK) - 1) & 1, s_abort)) break;
+                    mbar_arrive_expect_tx(&bars[T_KFULL + ks], L::OPT);
+                    for (int dh = 0; dh < 2; ++dh)
+                        tma_load_3d(sm + L::OFF_K + ks * L::OPT + dh * TK * 128, &tm_k, &bars[T_KFULL + ks], dh * 64, j,
+                                    hkv);
+                    ++kn;
+                    if (k >= L::NV && !mbar_wait(&bars[T_VEMPTY + vs], ((k / L::NV) - 1) & 1, s_abort)) break;
+                    mbar_arrive_expect_tx(&bars[T_VFULL + vs], L::OPT);
+                    for (int dh = 0; dh < 2; ++dh)
+                        tma_load_3d(sm + L::OFF_V + vs * L::OPT + dh * TK * 128, &tm_v, &bars[T_VFULL + vs], dh * 64, j,
+                                    hkv);
+                    ++vn;
+                }
+            }
+            if (*s_abort) {
+                // after a wait gave up: let the copies still in flight land before the CTA exits
+                volatile int never = 0;
+                auto drain = [&](int first_bar, int stages, int n) {
+                    for (int st = 0; st < stages && st < n; ++st) {
+                        const int last = st + ((n - 1 - st) / stages) * stages;
+                        mbar_wait(&bars[first_bar + st], (last / stages) & 1, &never, 200000000ull);
+                    }
+                };
+                if constexpr (Q8) {
+                    drain(T_RFULL, L::NR, kn);
+                } else {
+                    drain(T_KFULL, L::NK, kn);
+                    drain(T_VFULL, L::NV, vn);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_f16(128, NH, 0, 0);   // A = K (K-major), B = Q (K-major)
+            constexpr uint32_t IDESC_O = idesc_f16(128, NH, 1, 0);   // A = V^T (MN-major), B = P^T (K-major)
+            const uint32_t sK = smem_u32(sm + L::OFF_K), sV = smem_u32(sm + L::OFF_V);
+            const uint32_t sQ = smem_u32(sm + L::OFF_QT), sP = smem_u32(sm + L::OFF_PT);
+            bool ok = mbar_wait(&bars[T_QREADY], 0, s_abort);
+            tc_fence_after();
+            auto issue_s = [&](int j) -> bool {
+                const int ks = j % L::NK;
+                if (!mbar_wait(&bars[T_KFULL + ks], (j / L::NK) & 1, s_abort)) return false;
+                tc_fence_after();
+                const uint32_t kb = sK + ks * L::OPT;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint32_t kk = (s & 3) * 32;
+                    umma_ss(tmem + 16 * (j & 1), sdesc_sw128(kb + (s >> 2) * (TK * 128) + kk, 16, 1024),
+                            sdesc_sw128(sQ + (s >> 2) * (NH * 128) + kk, 16, 1024), IDESC_S, s > 0);
+                }
+                umma_commit(&bars[T_SFULL0 + (j & 1)]);
+                umma_commit(&bars[T_KEMPTY + ks]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            if (ok && T > 1) ok = issue_s(1);
+            for (int k = 0; ok && k < T; ++k) {
+                if (!mbar_wait(&bars[T_PFULL0 + (k & 1)], (k >> 1) & 1, s_abort)) { ok = false; break; }
+                const int vs = k % L::NV;
+                if (!mbar_wait(&bars[T_VFULL + vs], (k / L::NV) & 1, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t vb = sV + vs * L::OPT, pb = sP + (k & 1) * (NH * TK * 2);
+#pragma unroll
+                for (int s = 0; s < TK / 16; ++s)
+                    umma_ss(tmem + COL_O, sdesc_sw128(vb + s * 16 * 128, TK * 128, 1024),
+                            sdesc_sw128(pb + (s >> 2) * (NH * 128) + (s & 3) * 32, 16, 1024), IDESC_O,
+                            (k > 0 || s > 0) ? 1u : 0u);
+                umma_commit(&bars[T_ODONE0 + (k & 1)]);
+                umma_commit(&bars[T_VEMPTY + vs]);
+                if (k + 2 < T && !issue_s(k + 2)) { ok = false; break; }
+            }
+            if (*s_abort) {
+                // after a wait gave up: let the MMAs in flight finish before TMEM is freed
+                volatile int never = 0;
+                umma_commit(&bars[T_DRAIN]);
+                mbar_wait(&bars[T_DRAIN], 0, &never, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------ softmax
+        const int quarter = warp & 3;
+        const int L0 = quarter * 32 + lane;      // TMEM lane: key of the tile / head-dim row of O^T
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        // Q^T operand (rows >= G zero) and both P^T operands cleared (their rows >= G stay zero)
+        {
+            uint8_t *qt = sm + L::OFF_QT;
+            const int h = L0 >> 3, c = L0 & 7;
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    x[e] = h < G ? load_q<DT>(a.q, ((int64_t)hkv * G + h) * D + blk * 64 + c * 8 + e) : 0.f;
+                *reinterpret_cast<uint4 *>(qt + blk * (NH * 128) + sw128(h, c)) =
+                    make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
+                               pack_half2(x[6], x[7]));
+            }
+            uint4 *pt = reinterpret_cast<uint4 *>(sm + L::OFF_PT);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pt[L0 + 128 * i] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[T_QREADY]);
+        }
+        float m_run[GM], l_part[GM];
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+            m_run[h] = -INFINITY;
+            l_part[h] = 0.f;
+        }
+        uint32_t x_seq = 0;
+        int pv_seen[2] = {0, 0};
+        bool ok = true;
+        auto wait_pv = [&](int j) -> bool {  // PV(j) and every MMA before it have completed
+            const int b = j & 1, n = j >> 1;
+            if (pv_seen[b] > n) return true;
+            if (!mbar_wait(&bars[T_ODONE0 + b], n & 1, s_abort)) return false;
+            pv_seen[b] = n + 1;
+            tc_fence_after();
+            return true;
+        };
+        const float sl2 = a.scale_log2;
+        for (int k = 0; k < T; ++k) {
+            if (!mbar_wait(&bars[T_SFULL0 + (k & 1)], (k >> 1) & 1, s_abort)) { ok = false; break; }
+            tc_fence_after();
+            float sc[NH];
+            tmem_ld16(tmem + 16 * (k & 1) + lane_base, sc);
+            const bool valid = j_begin + k * TK + L0 < j_end;
+            // branch-free over the 16 padded heads: heads >= G score -inf, offset 0, so p = 0 exactly
+            float x[GM];
+#pragma unroll
+            for (int h = 0; h < GM; ++h) x[h] = (valid && h < G) ? sc[h] * sl2 : -INFINITY;
+            // per-head maximum over the warp (one warp reduction per head), then over the four warps;
+            // the four values of a head are adjacent ([head][warp]) and read as one 16-byte load
+            float *slot = s_red + (x_seq & 1) * 4 * NH;
+            {
+                float v = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < GM; ++h) {
+                    float mx;
+                    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(x[h]));
+                    v = lane == h ? mx : v;
+                }
+                if (lane < GM) slot[lane * 4 + quarter] = v;
+            }
+            mbar_arrive(&bars[T_XCHG]);
+            if (!mbar_wait(&bars[T_XCHG], x_seq & 1, s_abort)) { ok = false; break; }
+            ++x_seq;
+            bool rescale = false;
+            float alpha[GM];
+#pragma unroll
+            for (int h = 0; h < GM; ++h) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(slot + 4 * h);
+                const float M = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w));
+                // the split's first key is visible, so M is finite on the first tile for heads < G
+                const bool grow = k > 0 && M > m_run[h] + TC_RESCALE_LOG2;
+                alpha[h] = grow ? ex2(m_run[h] - M) : 1.f;
+                m_run[h] = (k == 0 || grow) ? M : m_run[h];
+                rescale |= grow;
+            }
+            float p[GM];
+#pragma unroll
+            for (int h = 0; h < GM; ++h) {
+                const float m_sub = m_run[h] == -INFINITY ? 0.f : m_run[h];
+                p[h] = ex2(x[h] - m_sub);
+                l_part[h] = l_part[h] * alpha[h] + p[h];
+            }
+            // P^T buffer k & 1 was last read by PV(k - 2); O^T must hold PV(k - 1) before a rescale
+            if (k >= 2 && !wait_pv(k - 2)) { ok = false; break; }
+            if (rescale && k >= 1) {
+                if (!wait_pv(k - 1)) { ok = false; break; }
+                float o[NH];
+                tmem_ld16(tmem + COL_O + lane_base, o);
+#pragma unroll
+                for (int h = 0; h < GM; ++h) o[h] *= alpha[h];
+                tmem_st16f(tmem + COL_O + lane_base, o);
+                tmem_st_wait();
+            }
+            uint8_t *pt = sm + L::OFF_PT + (k & 1) * (NH * TK * 2) + (L0 >> 6) * (NH * 128);
+            const int kc = (L0 & 63) >> 3, kb = (L0 & 7) * 2;
+#pragma unroll
+            for (int h = 0; h < GM; ++h)
+                if (h < G) *reinterpret_cast<__half *>(pt + sw128(h, kc) + kb) = __float2half_rn(p[h]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars[T_PFULL0 + (k & 1)]);
+        }
+        // ---- epilogue: this split's (m, l, O) per head of the group
+        if (ok && T > 0 && wait_pv(T - 1)) {
+            float o[NH];
+            tmem_ld16(tmem + COL_O + lane_base, o);
+            // row sums: over the warp (fixed tree), then the four warps in order
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int h = 0; h < GM; ++h) l_part[h] += __shfl_xor_sync(0xffffffffu, l_part[h], off);
+            float *slot = s_red + (x_seq & 1) * 4 * NH;
+            if (lane < GM) {
+                float v = l_part[0];
+#pragma unroll
+                for (int h = 1; h < GM; ++h) v = lane == h ? l_part[h] : v;
+                slot[lane * 4 + quarter] = v;
+            }
+            mbar_arrive(&bars[T_XCHG]);
+            if (mbar_wait(&bars[T_XCHG], x_seq & 1, s_abort)) {
+                ++x_seq;
+                const int64_t pbase = ((int64_t)hkv * MAX_SPLIT + split) * G;
+                float *part_o = a.part;
+                float *part_ml = a.part + (int64_t)a.n_head_kv * MAX_SPLIT * G * D;
+#pragma unroll
+                for (int h = 0; h < GM; ++h)
+                    if (h < G) part_o[(pbase + h) * D + L0] = o[h];
+                if (L0 < G) {
+                    float mv = m_run[0];
+#pragma unroll
+                    for (int h = 1; h < GM; ++h) mv = L0 == h ? m_run[h] : mv;
+                    const float4 w4 = *reinterpret_cast<const float4 *>(slot + 4 * L0);
+                    part_ml[(pbase + L0) * 2] = mv;
+                    part_ml[(pbase + L0) * 2 + 1] = ((w4.x + w4.y) + w4.z) + w4.w;
+                }
+            }
+        }
+    } else if constexpr (Q8) {
+        // ------------------------------------------------------------------ dequantise (q8_0)
+        const int r = threadIdx.x - 192;   // key row of the tile
+        constexpr int NB = D / 32;
+        bool ok = true;
+        uint2 sk_n = make_uint2(0u, 0u), sv_n = sk_n;
+        auto scales = [&](int k, uint2 &sk, uint2 &sv) {
+            const int key = min(j_begin + k * TK + r, a.n_keys - 1);  // keys past the end: any finite scale
+            const int64_t srow = a.layer * a.g.s_layer + hkv * a.g.s_head + (int64_t)key * a.g.s_tok;
+            sk = __ldg(reinterpret_cast<const uint2 *>(a.ks + srow));
+            sv = __ldg(reinterpret_cast<const uint2 *>(a.vs + srow));
+        };
+        if (T > 0) scales(0, sk_n, sv_n);
+        for (int k = 0; ok && k < T; ++k) {
+            const uint2 sk = sk_n, sv = sv_n;
+            if (k + 1 < T) scales(k + 1, sk_n, sv_n);
+            const int rs = k % L::NR;
+            if (!mbar_wait(&bars[T_RFULL + rs], (k / L::NR) & 1, s_abort)) { ok = false; break; }
+            const uint8_t *raw = sm + L::OFF_RAW + rs * L::RAWT;
+#pragma unroll 1
+            for (int kv = 0; kv < 2; ++kv) {
+                const int s = k % (kv ? L::NV : L::NK);
+                const int n = kv ? L::NV : L::NK;
+                if (k >= n && !mbar_wait(&bars[(kv ? T_VEMPTY : T_KEMPTY) + s], ((k / n) - 1) & 1, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *src = raw + kv * (TK * D);
+                uint8_t *dst = sm + (kv ? L::OFF_V : L::OFF_K) + s * L::OPT;
+                const uint2 sw = kv ? sv : sk;
+                uint4 q[D / 16];
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) q[c] = *reinterpret_cast<const uint4 *>(src + sw128(r, c));
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    const int b = c >> 1;
+                    const unsigned short sb = (unsigned short)((b < 2 ? sw.x : sw.y) >> (16 * (b & 1)));
+                    const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
+                    uint32_t o[8];
+                    dequant4(q[c].x, d2, o[0], o[1]);
+                    dequant4(q[c].y, d2, o[2], o[3]);
+                    dequant4(q[c].z, d2, o[4], o[5]);
+                    dequant4(q[c].w, d2, o[6], o[7]);
+                    // fp16 chunk 2c and 2c + 1 of the row: column block (2c) / 8, chunk (2c) % 8 inside it
+                    *reinterpret_cast<uint4 *>(dst + (c >> 2) * (TK * 128) + sw128(r, (2 * c) & 7)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(dst + (c >> 2) * (TK * 128) + sw128(r, (2 * c + 1) & 7)) =
+                        make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                // order the operand writes before the MMA (async proxy) reads them
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[(kv ? T_VFULL : T_KFULL) + s]);
+            }
+            if (!ok) break;
+            // the raw stage's generic reads are ordered by the fence above before its TMA refill
+            mbar_arrive(&bars[T_REMPTY + rs]);
+        }
+        (void)NB;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *s_abort) atomicExch(&g_decode_status, 1);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TC_COLS);
+    }
+}
+
+template <bool Q8, int DT>
+int launch_tc(const kvc_cache &c, const DecodeArgs &a0, int n_head_q, float *out, float *scratch, cudaStream_t s) {
+    using L = TCfg<Q8>;
+    constexpr int D = 128;
+    DecodeArgs a = a0;
+    // one wave, one CTA per SM over (split, kv head), whole tiles per split
+    const int target = sm_count() / a.n_head_kv;
+    int n_split = (a.n_keys + TK - 1) / TK;
+    if (n_split > target) n_split = target;
+    if (n_split > MAX_SPLIT) n_split = MAX_SPLIT;
+    if (n_split < 1) n_split = 1;
+    int len = (a.n_keys + n_split - 1) / n_split;
+    len = (len + TK - 1) / TK * TK;
+    n_split = (a.n_keys + len - 1) / len;
+    a.split_len = len;
+    a.n_split = n_split;
+    CUtensorMap tk, tv;
+    const Geom &g = a.g;
+    const int eb = Q8 ? 1 : 2;
+    const uint8_t *kb = static_cast<const uint8_t *>(c.k_q), *vb = static_cast<const uint8_t *>(c.v_q);
+    const CUtensorMapDataType dt = Q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t box0 = 128 / eb;   // 128-byte rows: all 128 codes (q8_0) or 64 halves (f16)
+    if (!make_map_3d(&tk, dt, kb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv, eb * g.c_tok,
+                     eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_3d(&tv, dt, vb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv, eb * g.c_tok,
+                     eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+        return KVC_ECUDA;
+    auto kern = a.group <= 8 ? decode_tc_kernel<Q8, DT, 8> : decode_tc_kernel<Q8, DT, 16>;
+    static bool attr_set[2] = {false, false};  // per instantiation
+    if (!attr_set[a.group <= 8]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+            return KVC_ECUDA;
+        attr_set[a.group <= 8] = true;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_split, a.n_head_kv);
+    cfg.blockDim = dim3(L::THREADS);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess) return KVC_ECUDA;
+    cudaLaunchConfig_t cfg2 = {};
+    cfg2.gridDim = dim3(n_head_q);
+    cfg2.blockDim = dim3(D);
+    cfg2.dynamicSmemBytes = 0;
+    cfg2.stream = s;
+    cfg2.attrs = attr;
+    cfg2.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg2, decode_combine_kernel<D>, (const float *)scratch, n_split, a.group, a.n_head_kv,
+                           out) != cudaSuccess)
+        return KVC_ECUDA;
+    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 
 template <int D, bool Q8, int DT>
 int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q, float *out,
              float *scratch, cudaStream_t s) {
+    using L = DCfg<D, Q8>;
     DecodeArgs a;
     a.q = q;
-    a.kq = c.k_q;
     a.ks = static_cast<const uint16_t *>(c.k_s);
-    a.vq = c.v_q;
     a.vs = static_cast<const uint16_t *>(c.v_s);
     a.part = scratch;
     a.g = geom_of(c.d);
@@ -428,20 +1072,65 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
     a.n_head_kv = c.d.n_head_kv;
     a.group = n_head_q / c.d.n_head_kv;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
-    // about three CTAs per SM in total, whole 64-key rounds per split
-    const int target = (3 * sm_count() + a.n_head_kv - 1) / a.n_head_kv;
-    int n_split = (a.n_keys + 63) / 64;
+    if constexpr (D == 128) {
+        return launch_tc<Q8, DT>(c, a, n_head_q, out, scratch, s);
+    } else {
+    // one wave: CTAS_PER_SM CTAs per SM over (split, kv head), whole stages per split
+    const int target = (CTAS_PER_SM * sm_count()) / a.n_head_kv;
+    int n_split = (a.n_keys + STAGE_KEYS - 1) / STAGE_KEYS;
     if (n_split > target) n_split = target;
     if (n_split > MAX_SPLIT) n_split = MAX_SPLIT;
     if (n_split < 1) n_split = 1;
     int len = (a.n_keys + n_split - 1) / n_split;
-    len = (len + 63) / 64 * 64;
+    len = (len + STAGE_KEYS - 1) / STAGE_KEYS * STAGE_KEYS;
     n_split = (a.n_keys + len - 1) / len;
     a.split_len = len;
     a.n_split = n_split;
-    decode_split_kernel<D, Q8, DT><<<dim3(n_split, a.n_head_kv), WARPS * 32, 0, s>>>(a);
-    decode_combine_kernel<D><<<n_head_q, D, 0, s>>>(scratch, n_split, a.group, a.n_head_kv, out);
+    // K and V of this layer as (element in row, key, kv head); keys past pos read as zeros
+    CUtensorMap tk, tv;
+    const Geom &g = a.g;
+    const uint8_t *kb = static_cast<const uint8_t *>(c.k_q), *vb = static_cast<const uint8_t *>(c.v_q);
+    const int eb = Q8 ? 1 : 2;
+    const CUtensorMapDataType dt = Q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle sw = L::BLK_ROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const uint32_t box0 = L::BLK_ROW / eb;
+    if (!make_map_3d(&tk, dt, kb + (int64_t)eb * layer * g.c_layer, D, a.n_keys, a.n_head_kv, eb * g.c_tok,
+                     eb * g.c_head, box0, STAGE_KEYS, 1, sw) ||
+        !make_map_3d(&tv, dt, vb + (int64_t)eb * layer * g.c_layer, D, a.n_keys, a.n_head_kv, eb * g.c_tok,
+                     eb * g.c_head, box0, STAGE_KEYS, 1, sw))
+        return KVC_ECUDA;
+    auto split_kern = decode_split_kernel<D, Q8, DT>;
+    static bool attr_set = false;  // per instantiation
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(split_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+            return KVC_ECUDA;
+        attr_set = true;
+    }
+    // both passes may start while the previous kernel of the stream finishes; each waits for it on
+    // the device before reading what it wrote
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_split, a.n_head_kv);
+    cfg.blockDim = dim3((CWARPS + 1) * 32);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, split_kern, tk, tv, a) != cudaSuccess) return KVC_ECUDA;
+    cudaLaunchConfig_t cfg2 = {};
+    cfg2.gridDim = dim3(n_head_q);
+    cfg2.blockDim = dim3(D);
+    cfg2.dynamicSmemBytes = 0;
+    cfg2.stream = s;
+    cfg2.attrs = attr;
+    cfg2.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg2, decode_combine_kernel<D>, (const float *)scratch, n_split, a.group,
+                           a.n_head_kv, out) != cudaSuccess)
+        return KVC_ECUDA;
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
+    }
 }
 
 template <int D, bool Q8>
@@ -483,6 +1172,15 @@ int noalloc_scratch_address(float **out) {
 }
 
 }  // namespace
+
+int read_and_clear_decode_status(int32_t *status) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(int)) != cudaSuccess) return KVC_ECUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(int)) != cudaSuccess) return KVC_ECUDA;
+    *status = v;
+    return KVC_OK;
+}
 
 size_t decode_noalloc_capacity() { return NOALLOC_SCRATCH_BYTES; }
 

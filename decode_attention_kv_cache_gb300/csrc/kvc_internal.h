@@ -1,6 +1,7 @@
 // Internal declarations shared by the C-ABI layer and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,6 +32,14 @@ inline Geom geom_of(const kvc_desc &d) {
 
 inline int dtype_bytes(int dtype) { return dtype == KVC_IN_F32 ? 4 : 2; }
 
+// A 3-D tiled TMA tensor map (dims innermost first, strides of dims 1 and 2 in bytes); false when
+// the driver entry point is missing or the encoding is rejected.
+bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
+                 uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+                 uint32_t b2, CUtensorMapSwizzle sw);
+// Streaming multiprocessors of the current device (cached after the first call).
+int sm_count();
+
 // Launchers: arguments are already validated; return KVC_OK or KVC_ECUDA.
 int launch_append(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *k,
                   const void *v, int dtype, cudaStream_t s);
@@ -46,7 +55,8 @@ int launch_decode_noalloc(const kvc_cache &c, int layer, int pos, const void *q,
 int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream_t s);
 int launch_state_unpack(const kvc_cache &c, int n_tokens, const uint8_t *src, cudaStream_t s);
 
-// Device status word set by kernels that give up a bounded wait.
+// Device status word set by kernels that give up a bounded wait (all kernels' words, read and cleared).
 int read_and_clear_device_status(int32_t *status);
+int read_and_clear_decode_status(int32_t *status);
 
 }  // namespace kvc

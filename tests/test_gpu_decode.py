@@ -26,6 +26,7 @@ CASES = [
     (8, 8, 128, "q8_0", "bf16", 150),   # G = 1
     (16, 1, 64, "q8_0", "bf16", 200),   # G = 16
     (24, 2, 128, "f16", "bf16", 90),    # G = 12: heads in both row halves of the MMA
+    (32, 2, 128, "q8_0", "f32", 333),   # G = 16 at head_dim 128: every padded head column in use
 ]
 
 
