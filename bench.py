@@ -59,6 +59,29 @@ def prefill_flops(w, chunks=None):
     return out
 
 
+# DRAM traffic of one prefill-attention launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only for the kernel source it was taken on (first 16 hex digits of
+# the SHA-256 of csrc/prefill.cu); any change to the kernel makes the bench report null instead.
+PREFILL_TRAFFIC = {
+    "source_sha256": "c4b3ebf4093242ba",
+    "f16_17k": (76.849152e6 + 38.323712e6, "chunk at position 15360 (512 rows), ncu --set full"),
+    "q8_0_58k": (207.285248e6 + 336.550656e6, "chunk at position 51200 (2048 rows), ncu --set full"),
+}
+
+
+def prefill_traffic(workload):
+    import hashlib
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "decode_attention_kv_cache_gb300", "csrc",
+                       "prefill.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None, None
+    if digest != PREFILL_TRAFFIC["source_sha256"] or workload not in PREFILL_TRAFFIC:
+        return None, None
+    return PREFILL_TRAFFIC[workload]
+
+
 def prefill_split_keys(n_ctx):
     """Keys per prefill split as the library chooses them: about a tenth of the cache in steps of
     1024 keys, at least 2048, and at most 64 splits (in 256-key tiles)."""
@@ -364,12 +387,14 @@ def run_gpu(args, rank, world, local):
     assert kvc.kvc_device_status() == 0
 
     peaks, peak_src = load_peaks()
+    traffic, traffic_launch = prefill_traffic(w.name)
     achieved = attn_flops / (attn_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roof = {"kernel": "prefill_chunk_attn (tcgen05 f16 x f16 -> f32)", "bound": "tensor",
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "peak_source": "%s dense bf16 burst (f16 runs at the bf16 rate)" % peak_src,
-            "traffic": None, "launches": n_attn // K, "avg_launch_ms": attn_ms / n_attn,
+            "traffic": traffic, "traffic_launch": traffic_launch, "launches": n_attn // K,
+            "avg_launch_ms": attn_ms / n_attn,
             "algorithmic_flops_per_step": attn_flops / K}
     bt = cache_bytes_per_token(w)
     dec_bytes = sum(w.n_layer * ((w.n_prompt + i + 1) * bt + w.n_head_q * w.head_dim * (2 + 4)
