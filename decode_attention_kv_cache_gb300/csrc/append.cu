@@ -10,11 +10,13 @@
 // amax exact, d = amax/127 and x/d by IEEE division, ties away from zero,
 // fp16 by round to nearest even.
 //
-// Work split: one thread per 8 consecutive values (one 16-byte load of bf16
-// or f16 input, two of f32), four neighbouring lanes per 32-value block; the
-// block's amax is a 4-lane xor-shuffle reduction.  Stores are 8-byte code
-// stores (16 threads cover a 128-value head row) plus one 2-byte scale per
-// block, so every warp writes whole 128-byte segments.  HBM-bound.
+// Work split.  q8_0: one thread per 32-value block (two or four 16-byte input
+// loads in flight per thread, 32 code bytes and one 2-byte scale stored).  The
+// quotient x/d is taken as x times the IEEE reciprocal of d and rounded with a
+// 1.5*2^23 shift; that product is within 5e-5 of the IEEE quotient, so the
+// rounded code can differ from round(x/d) only when the product lies within
+// that distance of a .5 boundary, and exactly those values are recomputed with
+// the IEEE division.  f16: one thread per 8 values.  HBM-bound.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,89 +49,98 @@ __device__ __forceinline__ void load8(const void *base, int64_t idx, float (&x)[
     }
 }
 
-// grid.x covers units of 8 values of one tensor; grid.y selects K (0) or V (1).
-template <int DT, bool Q8>
-__global__ void __launch_bounds__(256) append_kernel(
+// f16 cache: grid.x covers units of 8 values of one tensor; grid.y selects K (0) or V (1).
+template <int DT>
+__global__ void __launch_bounds__(256) append_f16_kernel(
     const void *__restrict__ k, const void *__restrict__ v, int64_t n_units, int units_per_tok,
-    int units_per_head, void *kq, uint16_t *ks, void *vq, uint16_t *vs, Geom g, int layer, int pos0) {
+    int units_per_head, void *kq, void *vq, Geom g, int layer, int pos0) {
     // a kernel launched after this one as a programmatic dependent (the decode split pass) may be
     // scheduled now; it waits for this grid's completion before it reads the cache
     asm volatile("griddepcontrol.launch_dependents;");
     const bool is_v = blockIdx.y != 0;
-    const void *src = is_v ? v : k;
     const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool live = u < n_units;
-    const int64_t uu = live ? u : 0;
-    const int tok = (int)(uu / units_per_tok);
-    const int rem = (int)(uu % units_per_tok);
+    if (u >= n_units) return;
+    const int tok = (int)(u / units_per_tok);
+    const int rem = (int)(u % units_per_tok);
     const int head = rem / units_per_head;
     const int c = rem % units_per_head;  // which 8-value group along head_dim
     float x[8];
-    if (live) load8<DT>(src, uu * 8, x);
-    else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = 0.f;
-    }
+    load8<DT>(is_v ? v : k, u * 8, x);
     const int64_t pos = (int64_t)pos0 + tok;
     const int64_t code_off = layer * g.c_layer + pos * g.c_tok + head * g.c_head + (int64_t)c * 8;
-    if constexpr (Q8) {
-        float amax = 0.f;
+    uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        // the four lanes of one 32-value block are neighbours (units of a head row are consecutive)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const float d = __fdiv_rn(amax, 127.0f);
-        uint32_t packed[2] = {0u, 0u};
-        if (d > 0.f) {  // codes are zero when amax/127 is zero (x/d undefined)
+    for (int i = 0; i < 4; ++i)
+        w[i] = (uint32_t)__half_as_ushort(__float2half_rn(x[2 * i])) |
+               ((uint32_t)__half_as_ushort(__float2half_rn(x[2 * i + 1])) << 16);
+    uint16_t *dst = static_cast<uint16_t *>(is_v ? vq : kq) + code_off;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// q8_0 cache: one thread per 32-value block; grid.y selects K (0) or V (1).
+template <int DT>
+__global__ void __launch_bounds__(256) append_q8_kernel(
+    const void *__restrict__ k, const void *__restrict__ v, int64_t n_blocks, int nb, int H, void *kq,
+    uint16_t *ks, void *vq, uint16_t *vs, Geom g, int layer, int pos0) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    const bool is_v = blockIdx.y != 0;
+    const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (blk >= n_blocks) return;
+    const int64_t row = blk / nb;                    // (token, head) in input order
+    const int b = (int)(blk - row * nb);
+    const int tok = (int)(row / H), head = (int)(row - (int64_t)tok * H);
+    float x[32];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float r = roundf(__fdiv_rn(x[i], d));  // round half away from zero
-                r = fminf(fmaxf(r, -127.f), 127.f);
-                const uint32_t b = (uint32_t)(uint8_t)(int8_t)(int)r;
-                packed[i >> 2] |= b << (8 * (i & 3));
-            }
-        }
-        if (live) {
-            int8_t *dst = static_cast<int8_t *>(is_v ? vq : kq) + code_off;
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-            if ((c & 3) == 0) {
-                uint16_t *sd = is_v ? vs : ks;
-                sd[layer * g.s_layer + pos * g.s_tok + head * g.s_head + (c >> 2)] =
-                    __half_as_ushort(__float2half_rn(d));
-            }
-        }
-    } else {
-        if (live) {
-            uint32_t w[4];
+    for (int j = 0; j < 4; ++j) {
+        float t8[8];
+        load8<DT>(is_v ? v : k, blk * 32 + 8 * j, t8);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                w[i] = (uint32_t)__half_as_ushort(__float2half_rn(x[2 * i])) |
-                       ((uint32_t)__half_as_ushort(__float2half_rn(x[2 * i + 1])) << 16);
-            }
-            uint16_t *dst = static_cast<uint16_t *>(is_v ? vq : kq) + code_off;
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 8; ++i) x[8 * j + i] = t8[i];
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    const float d = __fdiv_rn(amax, 127.0f);
+    uint32_t packed[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (d > 0.f) {  // codes are zero when amax/127 is zero (x/d undefined)
+        const float r = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float y = x[i] * r;
+            const float t = y + 12582912.0f;                 // y rounded to an integer (to even)
+            const float f = y - (t - 12582912.0f);            // y minus that integer, in [-1/2, 1/2]
+            int q = __float_as_int(t) - 0x4B400000;
+            if (fabsf(f) > 0.4999f) q = (int)roundf(__fdiv_rn(x[i], d));  // near a tie: exact quotient
+            q = min(max(q, -127), 127);
+            packed[i >> 2] |= (uint32_t)(q & 0xFF) << (8 * (i & 3));
         }
     }
+    const int64_t pos = (int64_t)pos0 + tok;
+    int8_t *dst = static_cast<int8_t *>(is_v ? vq : kq) + layer * g.c_layer + pos * g.c_tok + head * g.c_head + b * 32;
+    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    (is_v ? vs : ks)[layer * g.s_layer + pos * g.s_tok + head * g.s_head + b] = __half_as_ushort(__float2half_rn(d));
 }
 
 template <int DT>
 void launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *k, const void *v,
               cudaStream_t s) {
     const Geom g = geom_of(c.d);
-    const int units_per_head = c.d.head_dim / 8;
-    const int units_per_tok = units_per_head * c.d.n_head_kv;
-    const int64_t n_units = (int64_t)n * units_per_tok;
     const int threads = 256;
-    dim3 grid((unsigned)((n_units + threads - 1) / threads), 2);
-    if (c.d.type == KVC_Q8_0)
-        append_kernel<DT, true><<<grid, threads, 0, s>>>(
-            k, v, n_units, units_per_tok, units_per_head, c.k_q, (uint16_t *)c.k_s, c.v_q,
-            (uint16_t *)c.v_s, g, layer, pos0);
-    else
-        append_kernel<DT, false><<<grid, threads, 0, s>>>(
-            k, v, n_units, units_per_tok, units_per_head, c.k_q, nullptr, c.v_q, nullptr, g, layer,
-            pos0);
+    if (c.d.type == KVC_Q8_0) {
+        const int nb = c.d.head_dim / 32;
+        const int64_t n_blocks = (int64_t)n * c.d.n_head_kv * nb;
+        dim3 grid((unsigned)((n_blocks + threads - 1) / threads), 2);
+        append_q8_kernel<DT><<<grid, threads, 0, s>>>(k, v, n_blocks, nb, c.d.n_head_kv, c.k_q, (uint16_t *)c.k_s,
+                                                      c.v_q, (uint16_t *)c.v_s, g, layer, pos0);
+    } else {
+        const int units_per_head = c.d.head_dim / 8;
+        const int units_per_tok = units_per_head * c.d.n_head_kv;
+        const int64_t n_units = (int64_t)n * units_per_tok;
+        dim3 grid((unsigned)((n_units + threads - 1) / threads), 2);
+        append_f16_kernel<DT><<<grid, threads, 0, s>>>(k, v, n_units, units_per_tok, units_per_head, c.k_q, c.v_q, g,
+                                                       layer, pos0);
+    }
 }
 
 }  // namespace

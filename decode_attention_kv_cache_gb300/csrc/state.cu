@@ -11,12 +11,15 @@
 // record; a record lists the kv heads in order, each as head_dim/32 blocks of
 // [fp16 scale][32 int8 codes] (q8_0) or head_dim fp16 values (f16).
 //
-// Every unit of the stream is a 2-byte halfword (a 34-byte q8_0 block is 17
-// halfwords: the scale, then 16 code pairs).  A CTA takes RPC consecutive
-// records (RPC a multiple of 8, so its share of the stream starts on a 16-byte
-// boundary): pack loads the records' codes and scales with 16-byte loads into
-// shared memory, then assembles 16-byte output chunks from halfwords; unpack
-// does the reverse.  Both are HBM-bound copies with a permutation.
+// q8_0: the body is a sequence of 34-byte blocks.  Eight consecutive blocks
+// are a 272-byte unit that starts on a 16-byte boundary (32 + 272u), so one
+// thread moves one unit: pack loads the eight blocks' 32-byte code runs and
+// 2-byte scales and assembles the 17 16-byte output chunks with byte permutes
+// (a block pair is 17 words: scale + codes shifted by two bytes, then the
+// second scale, then the second block's codes word-aligned); unpack is the
+// mirror image.  A last unit with fewer than eight blocks moves halfword by
+// halfword.  f16: records are runs of 16-byte chunks; one thread moves four.
+// Both are HBM-bound copies with a permutation.
 #include <cuda_runtime.h>
 
 #include "kvc_internal.h"
@@ -25,173 +28,219 @@ namespace kvc {
 namespace {
 
 constexpr int THREADS = 256;
+constexpr int F16_CHUNKS = 4;   // 16-byte chunks per thread (f16)
 
 struct StateArgs {
-    const uint8_t *kq, *vq;        // codes (q8_0) or values (f16)
-    const uint16_t *ks, *vs;       // scales (q8_0)
-    uint8_t *kq_w, *vq_w;          // same, writable (unpack)
-    uint16_t *ks_w, *vs_w;
+    uint8_t *kq, *vq;              // codes (q8_0) or values (f16)
+    uint16_t *ks, *vs;             // scales (q8_0)
     Geom g;
-    int n_tokens, H, D, nb, n_records, rpc;
-    int rec_hw;                    // halfwords per record
-    uint8_t *out;                  // stream body (pack)
-    const uint8_t *in;             // stream body (unpack)
+    int n_tokens, H, D, nb;
+    int64_t n_blocks;              // q8_0: 34-byte blocks in the body
+    int64_t n_chunks;              // f16: 16-byte chunks in the body
+    uint8_t *body;                 // stream body (after the header)
 };
 
-// Record rho = (layer * n_tokens + t) * 2 + kv.
-__device__ __forceinline__ void record_coords(int rho, int n_tokens, int &layer, int &t, int &kv) {
-    kv = rho & 1;
-    const int lt = rho >> 1;
-    layer = lt / n_tokens;
-    t = lt - layer * n_tokens;
+// Coordinates of block `beta` of the body: record (layer, t, kv), head h, block b within the head.
+struct BlockPos {
+    int layer, t, kv, h, b;
+};
+
+__device__ __forceinline__ BlockPos block_pos(const StateArgs &a, int64_t beta) {
+    const int bpr = a.H * a.nb;                 // blocks per record
+    const int64_t rec = beta / bpr;
+    const int within = (int)(beta - rec * bpr);
+    BlockPos p;
+    p.kv = (int)(rec & 1);
+    const int64_t lt = rec >> 1;
+    p.layer = (int)(lt / a.n_tokens);
+    p.t = (int)(lt - (int64_t)p.layer * a.n_tokens);
+    p.h = within / a.nb;
+    p.b = within - p.h * a.nb;
+    return p;
 }
 
-template <bool Q8>
-__global__ void __launch_bounds__(THREADS) pack_kernel(const StateArgs a) {
-    extern __shared__ uint4 smem4[];
-    uint8_t *s_codes = reinterpret_cast<uint8_t *>(smem4);
-    const int esz = Q8 ? 1 : 2;
-    const int row_bytes = a.D * esz;                // one head's codes of one record
-    const int rec_code_bytes = a.H * row_bytes;
-    uint16_t *s_scales = reinterpret_cast<uint16_t *>(s_codes + a.rpc * rec_code_bytes);
-    const int rec0 = blockIdx.x * a.rpc;
-    const int nrec = min(a.rpc, a.n_records - rec0);
-
-    // 1. gather codes (16-byte chunks) and scales into shared memory, record by record
-    const int chunks_per_row = row_bytes / 16;
-    const int chunks_per_rec = a.H * chunks_per_row;
-    for (int i = threadIdx.x; i < nrec * chunks_per_rec; i += THREADS) {
-        const int r = i / chunks_per_rec, rem = i - r * chunks_per_rec;
-        const int h = rem / chunks_per_row, c = rem - h * chunks_per_row;
-        int layer, t, kv;
-        record_coords(rec0 + r, a.n_tokens, layer, t, kv);
-        const uint8_t *src = (kv ? a.vq : a.kq) +
-                             (layer * a.g.c_layer + (int64_t)t * a.g.c_tok + h * a.g.c_head) * esz + c * 16;
-        *reinterpret_cast<uint4 *>(s_codes + r * rec_code_bytes + h * row_bytes + c * 16) =
-            __ldg(reinterpret_cast<const uint4 *>(src));
+__device__ __forceinline__ void next_block(const StateArgs &a, BlockPos &p) {
+    if (++p.b < a.nb) return;
+    p.b = 0;
+    if (++p.h < a.H) return;
+    p.h = 0;
+    if (p.kv == 0) {
+        p.kv = 1;
+        return;
     }
-    if (Q8) {
-        const int per_rec = a.H * a.nb;
-        for (int i = threadIdx.x; i < nrec * per_rec; i += THREADS) {
-            const int r = i / per_rec, rem = i - r * per_rec;
-            const int h = rem / a.nb, b = rem - h * a.nb;
-            int layer, t, kv;
-            record_coords(rec0 + r, a.n_tokens, layer, t, kv);
-            s_scales[i] = __ldg((kv ? a.vs : a.ks) + layer * a.g.s_layer + (int64_t)t * a.g.s_tok +
-                                h * a.g.s_head + b);
-        }
-    }
-    __syncthreads();
+    p.kv = 0;
+    if (++p.t < a.n_tokens) return;
+    p.t = 0;
+    ++p.layer;
+}
 
-    // 2. assemble the stream: halfword x of record r is
-    //    q8_0: block k = x / 17, m = x % 17 -> m == 0 ? scale k : code pair (m - 1) of block k
-    //    f16:  value x of the record (heads in order)
-    const uint16_t *s_hw = reinterpret_cast<const uint16_t *>(s_codes);
-    const int total_hw = nrec * a.rec_hw;
-    uint8_t *dst = a.out + (int64_t)rec0 * a.rec_hw * 2;
-    auto hw_at = [&](int u) -> uint32_t {
-        const int r = u / a.rec_hw, x = u - r * a.rec_hw;
-        if (Q8) {
-            const int k = x / 17, m = x - k * 17;
-            return m == 0 ? s_scales[r * a.H * a.nb + k]
-                          : s_hw[(r * rec_code_bytes + k * 32) / 2 + (m - 1)];
-        }
-        return s_hw[r * (rec_code_bytes / 2) + x];
-    };
-    const int n_vec = total_hw / 8;
-    for (int i = threadIdx.x; i < n_vec; i += THREADS) {
-        uint32_t w[4];
+__device__ __forceinline__ int64_t code_off(const StateArgs &a, const BlockPos &p) {
+    return p.layer * a.g.c_layer + (int64_t)p.t * a.g.c_tok + p.h * a.g.c_head + p.b * 32;
+}
+__device__ __forceinline__ int64_t scale_off(const StateArgs &a, const BlockPos &p) {
+    return p.layer * a.g.s_layer + (int64_t)p.t * a.g.s_tok + p.h * a.g.s_head + p.b;
+}
+
+// the 68 words of a unit from its eight blocks' scales and code words (block pairs, see the file comment)
+__device__ __forceinline__ void assemble(const uint32_t (&sc)[8], const uint4 (&c)[16], uint32_t (&w)[68]) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = hw_at(8 * i + 2 * j) | (hw_at(8 * i + 2 * j + 1) << 16);
-        *reinterpret_cast<uint4 *>(dst + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t a[8] = {c[4 * pr].x, c[4 * pr].y, c[4 * pr].z, c[4 * pr].w,
+                               c[4 * pr + 1].x, c[4 * pr + 1].y, c[4 * pr + 1].z, c[4 * pr + 1].w};
+        const uint32_t b[8] = {c[4 * pr + 2].x, c[4 * pr + 2].y, c[4 * pr + 2].z, c[4 * pr + 2].w,
+                               c[4 * pr + 3].x, c[4 * pr + 3].y, c[4 * pr + 3].z, c[4 * pr + 3].w};
+        uint32_t *o = w + 17 * pr;
+        o[0] = __byte_perm(sc[2 * pr], a[0], 0x5410);          // scale, codes 0-1
+#pragma unroll
+        for (int k = 1; k < 8; ++k) o[k] = __byte_perm(a[k - 1], a[k], 0x5432);   // codes 4k-2 .. 4k+1
+        o[8] = __byte_perm(a[7], sc[2 * pr + 1], 0x5432);      // codes 30-31, second scale
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[9 + k] = b[k];
     }
-    for (int u = n_vec * 8 + threadIdx.x; u < total_hw; u += THREADS)
-        reinterpret_cast<uint16_t *>(dst)[u] = (uint16_t)hw_at(u);
 }
 
-template <bool Q8>
-__global__ void __launch_bounds__(THREADS) unpack_kernel(const StateArgs a) {
-    extern __shared__ uint4 smem4[];
-    uint16_t *s_hw = reinterpret_cast<uint16_t *>(smem4);
-    const int rec0 = blockIdx.x * a.rpc;
-    const int nrec = min(a.rpc, a.n_records - rec0);
-    const int total_hw = nrec * a.rec_hw;
-    const uint8_t *src = a.in + (int64_t)rec0 * a.rec_hw * 2;
+// the inverse: eight scales and code words from the 68 words of a unit
+__device__ __forceinline__ void disassemble(const uint32_t (&w)[68], uint32_t (&sc)[8], uint4 (&c)[16]) {
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t *o = w + 17 * pr;
+        uint32_t a[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a[k] = __byte_perm(o[k], o[k + 1], 0x5432);
+        sc[2 * pr] = o[0] & 0xFFFFu;
+        sc[2 * pr + 1] = o[8] >> 16;
+        c[4 * pr] = make_uint4(a[0], a[1], a[2], a[3]);
+        c[4 * pr + 1] = make_uint4(a[4], a[5], a[6], a[7]);
+        c[4 * pr + 2] = make_uint4(o[9], o[10], o[11], o[12]);
+        c[4 * pr + 3] = make_uint4(o[13], o[14], o[15], o[16]);
+    }
+}
 
-    // 1. stage the records' stream bytes
-    const int n_vec = total_hw / 8;
-    for (int i = threadIdx.x; i < n_vec; i += THREADS)
-        smem4[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
-    for (int u = n_vec * 8 + threadIdx.x; u < total_hw; u += THREADS)
-        s_hw[u] = __ldg(reinterpret_cast<const uint16_t *>(src) + u);
-    __syncthreads();
-
-    // 2. scatter: 16 bytes of one head's codes (or values) per thread
-    const int esz = Q8 ? 1 : 2;
-    const int row_bytes = a.D * esz;
-    const int chunks_per_row = row_bytes / 16;
-    const int chunks_per_rec = a.H * chunks_per_row;
-    for (int i = threadIdx.x; i < nrec * chunks_per_rec; i += THREADS) {
-        const int r = i / chunks_per_rec, rem = i - r * chunks_per_rec;
-        const int h = rem / chunks_per_row, c = rem - h * chunks_per_row;
-        int layer, t, kv;
-        record_coords(rec0 + r, a.n_tokens, layer, t, kv);
-        int x0;  // first stream halfword of these 16 bytes within the record
-        if (Q8) {
-            const int k = h * a.nb + (c * 16) / 32;          // block
-            x0 = k * 17 + 1 + ((c * 16) % 32) / 2;
+__global__ void __launch_bounds__(THREADS) pack_q8_kernel(const StateArgs a) {
+    const int64_t u = (int64_t)blockIdx.x * THREADS + threadIdx.x;
+    const int64_t beta0 = u * 8;
+    if (beta0 >= a.n_blocks) return;
+    const int nblk = (int)min((int64_t)8, a.n_blocks - beta0);
+    uint32_t sc[8];
+    uint4 c[16];
+    BlockPos p = block_pos(a, beta0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < nblk) {
+            const uint8_t *src = (p.kv ? a.vq : a.kq) + code_off(a, p);
+            c[2 * i] = __ldg(reinterpret_cast<const uint4 *>(src));
+            c[2 * i + 1] = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+            sc[i] = __ldg((p.kv ? a.vs : a.ks) + scale_off(a, p));
+            next_block(a, p);
         } else {
-            x0 = h * a.D + c * 8;
+            c[2 * i] = c[2 * i + 1] = make_uint4(0u, 0u, 0u, 0u);
+            sc[i] = 0u;
         }
-        const uint16_t *p = s_hw + r * a.rec_hw + x0;
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = (uint32_t)p[2 * j] | ((uint32_t)p[2 * j + 1] << 16);
-        uint8_t *dst = (kv ? a.vq_w : a.kq_w) +
-                       (layer * a.g.c_layer + (int64_t)t * a.g.c_tok + h * a.g.c_head) * esz + c * 16;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    if (Q8) {
-        const int per_rec = a.H * a.nb;
-        for (int i = threadIdx.x; i < nrec * per_rec; i += THREADS) {
-            const int r = i / per_rec, k = i - r * per_rec;
-            const int h = k / a.nb, b = k - h * a.nb;
-            int layer, t, kv;
-            record_coords(rec0 + r, a.n_tokens, layer, t, kv);
-            (kv ? a.vs_w : a.ks_w)[layer * a.g.s_layer + (int64_t)t * a.g.s_tok + h * a.g.s_head + b] =
-                s_hw[r * a.rec_hw + k * 17];
+    uint32_t w[68];
+    assemble(sc, c, w);
+    uint8_t *dst = a.body + u * 272;
+    if (nblk == 8) {
+#pragma unroll
+        for (int k = 0; k < 17; ++k)
+            *reinterpret_cast<uint4 *>(dst + 16 * k) = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    } else {
+        // the body ends inside this unit: 17 halfwords per block
+        uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
+#pragma unroll
+        for (int x = 0; x < 136; ++x)
+            if (x < 17 * nblk) d16[x] = (uint16_t)(w[x >> 1] >> (16 * (x & 1)));
+    }
+}
+
+__global__ void __launch_bounds__(THREADS) unpack_q8_kernel(const StateArgs a) {
+    const int64_t u = (int64_t)blockIdx.x * THREADS + threadIdx.x;
+    const int64_t beta0 = u * 8;
+    if (beta0 >= a.n_blocks) return;
+    const int nblk = (int)min((int64_t)8, a.n_blocks - beta0);
+    const uint8_t *src = a.body + u * 272;
+    uint32_t w[68];
+    if (nblk == 8) {
+#pragma unroll
+        for (int k = 0; k < 17; ++k) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + k);
+            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 68; ++k) w[k] = 0u;
+        const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
+#pragma unroll
+        for (int x = 0; x < 136; ++x)
+            if (x < 17 * nblk) w[x >> 1] |= (uint32_t)__ldg(s16 + x) << (16 * (x & 1));
+    }
+    uint32_t sc[8];
+    uint4 c[16];
+    disassemble(w, sc, c);
+    BlockPos p = block_pos(a, beta0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < nblk) {
+            uint8_t *dst = (p.kv ? a.vq : a.kq) + code_off(a, p);
+            reinterpret_cast<uint4 *>(dst)[0] = c[2 * i];
+            reinterpret_cast<uint4 *>(dst)[1] = c[2 * i + 1];
+            (p.kv ? a.vs : a.ks)[scale_off(a, p)] = (uint16_t)sc[i];
+            next_block(a, p);
         }
     }
 }
 
-StateArgs make_args(const kvc_cache &c, int n_tokens) {
+// f16: chunk gamma of the body -> (record, head, chunk within the head row)
+__device__ __forceinline__ uint8_t *f16_cache_ptr(const StateArgs &a, int64_t gamma) {
+    const int cpr = a.D / 8;                    // 16-byte chunks per head row
+    const int64_t row = gamma / cpr;            // (record, head) in stream order
+    const int ch = (int)(gamma - row * cpr);
+    const int64_t rec = row / a.H;
+    const int h = (int)(row - rec * a.H);
+    const int kv = (int)(rec & 1);
+    const int64_t lt = rec >> 1;
+    const int layer = (int)(lt / a.n_tokens);
+    const int t = (int)(lt - (int64_t)layer * a.n_tokens);
+    return (kv ? a.vq : a.kq) + 2 * (layer * a.g.c_layer + (int64_t)t * a.g.c_tok + h * a.g.c_head) + 16 * ch;
+}
+
+template <bool PACK>
+__global__ void __launch_bounds__(THREADS) copy_f16_kernel(const StateArgs a) {
+    const int64_t first = ((int64_t)blockIdx.x * THREADS + threadIdx.x) * F16_CHUNKS;
+    uint4 v[F16_CHUNKS];
+#pragma unroll
+    for (int i = 0; i < F16_CHUNKS; ++i) {
+        const int64_t gamma = first + i;
+        if (gamma < a.n_chunks)
+            v[i] = PACK ? __ldg(reinterpret_cast<const uint4 *>(f16_cache_ptr(a, gamma)))
+                        : __ldg(reinterpret_cast<const uint4 *>(a.body) + gamma);
+    }
+#pragma unroll
+    for (int i = 0; i < F16_CHUNKS; ++i) {
+        const int64_t gamma = first + i;
+        if (gamma < a.n_chunks) {
+            if (PACK) reinterpret_cast<uint4 *>(a.body)[gamma] = v[i];
+            else *reinterpret_cast<uint4 *>(f16_cache_ptr(a, gamma)) = v[i];
+        }
+    }
+}
+
+StateArgs make_args(const kvc_cache &c, int n_tokens, uint8_t *body) {
     StateArgs a = {};
-    a.kq = static_cast<const uint8_t *>(c.k_q);
-    a.vq = static_cast<const uint8_t *>(c.v_q);
-    a.ks = static_cast<const uint16_t *>(c.k_s);
-    a.vs = static_cast<const uint16_t *>(c.v_s);
-    a.kq_w = static_cast<uint8_t *>(c.k_q);
-    a.vq_w = static_cast<uint8_t *>(c.v_q);
-    a.ks_w = static_cast<uint16_t *>(c.k_s);
-    a.vs_w = static_cast<uint16_t *>(c.v_s);
+    a.kq = static_cast<uint8_t *>(c.k_q);
+    a.vq = static_cast<uint8_t *>(c.v_q);
+    a.ks = static_cast<uint16_t *>(c.k_s);
+    a.vs = static_cast<uint16_t *>(c.v_s);
     a.g = geom_of(c.d);
     a.n_tokens = n_tokens;
     a.H = c.d.n_head_kv;
     a.D = c.d.head_dim;
     a.nb = c.d.head_dim / 32;
-    a.n_records = c.d.n_layer * n_tokens * 2;
-    const bool q8 = c.d.type == KVC_Q8_0;
-    const int rec_bytes = q8 ? a.H * a.nb * 34 : a.H * a.D * 2;
-    a.rec_hw = rec_bytes / 2;
-    // records per CTA: a multiple of 8 (16-byte aligned CTA boundaries), about 16 KB of stream
-    int rpc = (16384 / rec_bytes) / 8 * 8;
-    a.rpc = rpc < 8 ? 8 : rpc;
+    const int64_t n_records = (int64_t)c.d.n_layer * n_tokens * 2;
+    a.n_blocks = n_records * a.H * a.nb;
+    a.n_chunks = n_records * a.H * (a.D / 8);
+    a.body = body;
     return a;
-}
-
-size_t pack_smem(const StateArgs &a, bool q8) {
-    const size_t codes = (size_t)a.rpc * a.H * a.D * (q8 ? 1 : 2);
-    return codes + (q8 ? (size_t)a.rpc * a.H * a.nb * 2 : 0);
 }
 
 __global__ void write_header(uint8_t *dst, uint32_t n_layer, uint32_t H, uint32_t D, uint32_t type,
@@ -207,49 +256,29 @@ __global__ void write_header(uint8_t *dst, uint32_t n_layer, uint32_t H, uint32_
     w[7] = 0u;
 }
 
+int grid_for(int64_t work, int per_thread) {
+    return (int)((work + (int64_t)THREADS * per_thread - 1) / ((int64_t)THREADS * per_thread));
+}
+
 }  // namespace
 
 int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream_t s) {
     const bool q8 = c.d.type == KVC_Q8_0;
     write_header<<<1, 1, 0, s>>>(dst, c.d.n_layer, c.d.n_head_kv, c.d.head_dim, q8 ? 1u : 0u, n_tokens);
-    StateArgs a = make_args(c, n_tokens);
-    a.out = dst + 32;
-    if (a.n_records > 0) {
-        const size_t smem = pack_smem(a, q8);
-        const int grid = (a.n_records + a.rpc - 1) / a.rpc;
-        if (q8) {
-            if (smem > 48 * 1024 && cudaFuncSetAttribute(pack_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         (int)smem) != cudaSuccess)
-                return KVC_ECUDA;
-            pack_kernel<true><<<grid, THREADS, smem, s>>>(a);
-        } else {
-            if (smem > 48 * 1024 && cudaFuncSetAttribute(pack_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         (int)smem) != cudaSuccess)
-                return KVC_ECUDA;
-            pack_kernel<false><<<grid, THREADS, smem, s>>>(a);
-        }
+    const StateArgs a = make_args(c, n_tokens, dst + 32);
+    if (n_tokens > 0) {
+        if (q8) pack_q8_kernel<<<grid_for(a.n_blocks, 8), THREADS, 0, s>>>(a);
+        else copy_f16_kernel<true><<<grid_for(a.n_chunks, F16_CHUNKS), THREADS, 0, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 
 int launch_state_unpack(const kvc_cache &c, int n_tokens, const uint8_t *src, cudaStream_t s) {
     const bool q8 = c.d.type == KVC_Q8_0;
-    StateArgs a = make_args(c, n_tokens);
-    a.in = src + 32;
-    if (a.n_records > 0) {
-        const size_t smem = ((size_t)a.rpc * a.rec_hw * 2 + 15) / 16 * 16;
-        const int grid = (a.n_records + a.rpc - 1) / a.rpc;
-        if (q8) {
-            if (smem > 48 * 1024 && cudaFuncSetAttribute(unpack_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         (int)smem) != cudaSuccess)
-                return KVC_ECUDA;
-            unpack_kernel<true><<<grid, THREADS, smem, s>>>(a);
-        } else {
-            if (smem > 48 * 1024 && cudaFuncSetAttribute(unpack_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         (int)smem) != cudaSuccess)
-                return KVC_ECUDA;
-            unpack_kernel<false><<<grid, THREADS, smem, s>>>(a);
-        }
+    const StateArgs a = make_args(c, n_tokens, const_cast<uint8_t *>(src) + 32);
+    if (n_tokens > 0) {
+        if (q8) unpack_q8_kernel<<<grid_for(a.n_blocks, 8), THREADS, 0, s>>>(a);
+        else copy_f16_kernel<false><<<grid_for(a.n_chunks, F16_CHUNKS), THREADS, 0, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
