@@ -21,6 +21,7 @@
 #include <cuda_fp16.h>
 
 #include "kvc_internal.h"
+#include "ptx.cuh"
 
 namespace kvc {
 namespace {
@@ -70,9 +71,7 @@ __global__ void __launch_bounds__(256) append_f16_kernel(
     const int64_t code_off = layer * g.c_layer + pos * g.c_tok + head * g.c_head + (int64_t)c * 8;
     uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        w[i] = (uint32_t)__half_as_ushort(__float2half_rn(x[2 * i])) |
-               ((uint32_t)__half_as_ushort(__float2half_rn(x[2 * i + 1])) << 16);
+    for (int i = 0; i < 4; ++i) w[i] = ptx::pack_half2(x[2 * i], x[2 * i + 1]);
     uint16_t *dst = static_cast<uint16_t *>(is_v ? vq : kq) + code_off;
     *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }

@@ -95,10 +95,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
-           ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
-}
 
 // Two int8 codes placed in bytes 0 and 2 of `t` (bytes 1 and 3 ignored) -> fp16x2 of the exact codes.
 __device__ __forceinline__ uint32_t codes_to_half2(uint32_t t) {

@@ -162,10 +162,6 @@ __device__ __forceinline__ uint32_t op_off(int rows, int row, int cc) {
     return (uint32_t)((cc >> 3) * rows * 128) + sw128(row, cc & 7);
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
-           ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
-}
 
 // 4 int8 codes times the fp16 scale, as two fp16x2 words (one rounding each).  Flipping the sign
 // bit makes each code q + 128 as an unsigned byte; under the high byte 0x64 that is the fp16 value

@@ -209,6 +209,14 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two floats to one fp16x2 word (lo in the low half), both rounded to nearest even, by one packed
+// conversion instruction (two scalar conversions plus a merge cost several times more).
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // ---- packed and three-input fp32 arithmetic (IEEE round-to-nearest per lane) ----
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
     uint64_t r;
