@@ -86,7 +86,7 @@ struct Cfg {
     static constexpr int OFF_RING = OFF_Q + QT_BYTES;
     static constexpr int OFF_RAW = OFF_RING + NS * ST_BYTES;
     static constexpr int OFF_BAR = OFF_RAW + (Q8 ? NR * RAW_BYTES : 0);
-    static constexpr int OFF_RED = OFF_BAR + 512;             // [parity][group][row] floats
+    static constexpr int OFF_RED = OFF_BAR + 384;             // mailbox words [slot][group][row]
     static constexpr int USED = OFF_RED + 2 * 2 * BM * 4;
     static constexpr int ALLOC = (USED + 1024 <= MAX_DYN_SMEM) ? USED + 1024 : MAX_DYN_SMEM;
     static_assert(USED <= MAX_DYN_SMEM, "shared memory plan too large");
@@ -102,7 +102,7 @@ struct Cfg {
 };
 
 enum Bar {
-    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_OFREE, B_XCHG, B_DRAIN,
+    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_OFREE, B_DRAIN,
     B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
     B_RAW_EMPTY = B_RAW_FULL + 8, NBAR = B_RAW_EMPTY + 8
 };
@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
-    float *s_red = reinterpret_cast<float *>(sm + L::OFF_RED);
+    volatile uint32_t *s_mb = reinterpret_cast<volatile uint32_t *>(sm + L::OFF_RED);
+    static_assert(NBAR * 8 + 8 <= 384, "barrier area too small");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -226,7 +227,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         mbar_init(&bars[B_PFULL], 256);
         mbar_init(&bars[B_ODONE], 1);
         mbar_init(&bars[B_OFREE], 256);
-        mbar_init(&bars[B_XCHG], 256);
+        // mailbox words start with flag bit 1: the first value written to each slot carries flag 0
+        for (int i = 0; i < 2 * 2 * BM; ++i) reinterpret_cast<uint32_t *>(sm + L::OFF_RED)[i] = 1u;
         mbar_init(&bars[B_DRAIN], 1);
         for (int s = 0; s < L::NS; ++s) {
             mbar_init(&bars[B_RING_FULL + s], Q8 ? 128 : 1);
@@ -434,17 +436,34 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         const uint32_t tS = tmem + COL_S + 128 * grp + lane_base;
         const uint32_t tP = tmem + COL_P + 64 * grp + lane_base;
         const uint32_t tO = tmem + COL_O + (D / 2) * grp + lane_base;
-        uint32_t s_seq = 0, o_seq = 0, x_seq = 0;
+        uint32_t s_seq = 0, o_seq = 0, mb_n = 0;
         bool ok = true;
         const float sl2 = a.scale_log2;
-        // the other group's value for my row, through shared memory (bounded rendezvous of both groups)
-        auto exchange = [&](float mine, float &theirs) -> bool {
-            float *slot = s_red + (x_seq & 1) * 2 * BM;
-            slot[grp * BM + r] = mine;
-            mbar_arrive(&bars[B_XCHG]);
-            if (!mbar_wait(&bars[B_XCHG], x_seq & 1, s_abort)) return false;
-            ++x_seq;
-            theirs = slot[(grp ^ 1) * BM + r];
+        // The two threads that own a row exchange one float through a mailbox word per (slot, group,
+        // row) in shared memory: the value with its lowest mantissa bit replaced by a flag, written and
+        // read as one 32-bit word (so no fence is needed).  Exchange n uses slot n & 1 with flag
+        // (n >> 1) & 1; a slot is written again only after the partner's next value has been read, which
+        // the partner wrote after reading this one, so no value is overwritten unread.  Both threads use
+        // the two encoded values (within one ulp of the true ones), so they agree exactly; -inf travels
+        // as -FLT_MAX, which every use treats alike.  The wait is bounded.
+        auto exchange = [&](float &mine, float &theirs) -> bool {
+            const int slot = mb_n & 1;
+            const uint32_t flag = (mb_n >> 1) & 1u;
+            const int me = (slot * 2 + grp) * BM + r, other = (slot * 2 + (grp ^ 1)) * BM + r;
+            mine = fmaxf(mine, -3.402823466e38f);
+            const uint32_t enc = (__float_as_uint(mine) & ~1u) | flag;
+            mine = __uint_as_float(enc & ~1u);
+            s_mb[me] = enc;
+            uint32_t w = s_mb[other];
+            for (uint32_t n = 0; (w & 1u) != flag; ++n) {
+                if ((n & 1023u) == 1023u && (*s_abort || n > (1u << 26))) {
+                    *s_abort = 1;
+                    return false;
+                }
+                w = s_mb[other];
+            }
+            theirs = __uint_as_float(w & ~1u);
+            ++mb_n;
             return true;
         };
         for (int i = first_item; ok && i < a.n_items; i += stride) {
@@ -457,35 +476,37 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 if (!mbar_wait(&bars[B_SFULL], s_seq & 1, s_abort)) { ok = false; break; }
                 ++s_seq;
                 tc_fence_after();
-                // the row max over the whole tile: the other group's half first (read only for the max),
-                // then my half, kept in registers; both groups reach the same max (max is exact in any
-                // order).  Then S may be overwritten.
+                // my half of the S row in registers (one TMEM round trip), then S may be overwritten
                 uint32_t s[128];
-                float mx8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-#pragma unroll 1
-                for (int half = 1; half >= 0; --half) {
-                    const int hg = grp ^ half;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld32p(tmem + COL_S + 128 * hg + lane_base + c * 32, s + c * 32);
-                    tmem_ld_wait();
-                    const int key0 = k * BN + 128 * hg;
-                    if (key0 + 127 > it.tf) {
-#pragma unroll
-                        for (int e = 0; e < 128; ++e)
-                            if (key0 + e > t) s[e] = 0xFF800000u;  // -inf: a key after the query
-                    }
-#pragma unroll
-                    for (int e = 0; e < 128; e += 16) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            mx8[u] = fmax3(mx8[u], __uint_as_float(s[e + u]), __uint_as_float(s[e + 8 + u]));
-                    }
-                }
+                for (int c = 0; c < 4; ++c) tmem_ld32p(tS + c * 32, s + c * 32);
+                tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&bars[B_SFREE]);
-                const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                const int key0 = k * BN + 128 * grp;
+                if (key0 + 127 > it.tf) {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        if (key0 + e > t) s[e] = 0xFF800000u;  // -inf: a key after the query
+                }
+                // row max: my half in 8 chains of three-input maxima, then the other group's half-row max
+                // from the mailbox; both groups take fmaxf(own, other) of the same two values
+                float mx8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+#pragma unroll
+                for (int e = 8; e < 120; e += 16) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        mx8[u] = fmax3(mx8[u], __uint_as_float(s[e + u]), __uint_as_float(s[e + 8 + u]));
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], __uint_as_float(s[120 + u]));
+                float mx_own =
+                    fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                float mx_other;
+                if (!exchange(mx_own, mx_other)) { ok = false; break; }
+                const float mx = grp == 0 ? fmaxf(mx_own, mx_other) : fmaxf(mx_other, mx_own);
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 float m_use = m_ref, alpha = 1.f;
                 if (k == it.k0) {
