@@ -37,11 +37,13 @@
 //               global memory); Q is released after the item's last S MMA, so
 //               the next item's Q loads during this one's tail.
 //   warps 4-11  softmax: two warpgroups, each owns 128 of the tile's 256 key
-//               columns for all 128 rows (thread = TMEM lane = row).  Row maxima
-//               are exchanged through shared memory, so both groups use the
-//               same running max; each group writes its half of P and
+//               columns for all 128 rows (thread = TMEM lane = row).  The two
+//               threads of a row exchange their half-row maxima (and at the
+//               end the sums) through flagged shared-memory words, so both use
+//               the same running max; each group writes its half of P and
 //               rescales its half of O (only when the running max grows by
-//               more than 2^8).
+//               more than 2^8).  After an item's last tile they read O out of
+//               TMEM and write O / l, or the partial, 32 bytes per store.
 //   warps 12-15 (q8_0) dequantise int8 rows into fp16 d*q in the 128-byte
 //               swizzled operand layout.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
@@ -72,8 +74,8 @@ constexpr uint32_t COL_S = 0, COL_P = 256, COL_O = 384;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr int MAX_SPLITS = 64;
 constexpr int MAX_DYN_SMEM = 232448;   // 227 KB per CTA
-// a partial row: D values, the running max, the sum, two pad floats (keeps rows 16-byte aligned)
-#define PART_ROW(D) ((D) + 4)
+// a partial row: D values, the running max, the sum, six pad floats (keeps rows 32-byte aligned)
+#define PART_ROW(D) ((D) + 8)
 
 template <int D, bool Q8>
 struct Cfg {
@@ -102,7 +104,7 @@ struct Cfg {
 };
 
 enum Bar {
-    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_OFREE, B_DRAIN,
+    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN,
     B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
     B_RAW_EMPTY = B_RAW_FULL + 8, NBAR = B_RAW_EMPTY + 8
 };
@@ -115,6 +117,7 @@ struct Args {
     float *part;      // partials [q-tile][head][split][row][PART_ROW]
     Geom g;
     int layer, pos0, C, kv_len, H_q, G, H_kv, n_qt, ST, smax, n_items;
+    int v8;                    // out and part are 32-byte aligned: rows are stored 32 bytes at a time
     float scale_log2;
     int cum[MAX_SPLITS + 1];   // items before split index s
     int qtmin[MAX_SPLITS];     // first q-tile whose keys reach split s
@@ -226,7 +229,6 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         mbar_init(&bars[B_SFREE], 256);
         mbar_init(&bars[B_PFULL], 256);
         mbar_init(&bars[B_ODONE], 1);
-        mbar_init(&bars[B_OFREE], 256);
         // mailbox words start with flag bit 1: the first value written to each slot carries flag 0
         for (int i = 0; i < 2 * 2 * BM; ++i) reinterpret_cast<uint32_t *>(sm + L::OFF_RED)[i] = 1u;
         mbar_init(&bars[B_DRAIN], 1);
@@ -316,8 +318,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             constexpr uint32_t IDESC_S = idesc_f16(BM, BN, 0, 0);
             constexpr uint32_t IDESC_O = idesc_f16(BM, D, 0, 1);
             const uint32_t sQ = smem_u32(sm + L::OFF_Q), sRing = smem_u32(sm + L::OFF_RING);
-            uint32_t ring_seq = 0, q_seq = 0, s_issued = 0, p_seq = 0, ofree_seq = 0;
-            bool o_used = false, ok = true;
+            uint32_t ring_seq = 0, q_seq = 0, s_issued = 0, p_seq = 0;
+            bool ok = true;
             auto ring_wait = [&](uint32_t seq) -> bool {
                 if (!mbar_wait(&bars[B_RING_FULL + seq % L::NS], (seq / L::NS) & 1, s_abort)) return false;
                 tc_fence_after();
@@ -368,15 +370,12 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                         if (!issue_s()) { ok = false; break; }
                         if (k + 2 == it.k1) umma_commit(&bars[B_QEMPTY]);
                     }
-                    if (k == it.k0 && o_used) {  // the previous item's epilogue has read O
-                        if (!mbar_wait(&bars[B_OFREE], ofree_seq & 1, s_abort)) { ok = false; break; }
-                        ++ofree_seq;
-                    }
+                    // an item's first PV starts a new O: the softmax has read the previous one out of TMEM
+                    // before it signals that P is ready
                     if (!mbar_wait(&bars[B_PFULL], p_seq & 1, s_abort)) { ok = false; break; }
                     ++p_seq;
                     tc_fence_after();
                     if (!issue_pv(k > it.k0)) { ok = false; break; }
-                    o_used = true;
                 }
             }
             if (*s_abort) {
@@ -469,7 +468,6 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         for (int i = first_item; ok && i < a.n_items; i += stride) {
             const Item it = decode_item(a, i);
             const int row = it.qt * BM + r;       // row within the chunk
-            const bool valid = row < a.C;
             const int t = it.tf + r;              // absolute position
             float m_ref = -INFINITY, l = 0.f;
             for (int k = it.k0; k < it.k1; ++k) {
@@ -568,45 +566,45 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 m_ref = m_use;
             }
             if (!ok) break;
-            // ---- epilogue: the row sum over both halves, then O / l or the partial (O, m, l)
+            // ---- epilogue: the row sum over both halves, then O / l or the partial (O, m, l).  The
+            // next item's first PV overwrites O only after this thread's next P is published, which
+            // comes after these TMEM reads.  A warp stores 32 rows per instruction, so each thread
+            // writes 32 bytes at a time (whole sectors) where the buffers are 32-byte aligned.
             if (!mbar_wait(&bars[B_ODONE], o_seq & 1, s_abort)) { ok = false; break; }
             ++o_seq;
             tc_fence_after();
             float l_other;
             if (!exchange(l, l_other)) { ok = false; break; }
             const float l_row = grp == 0 ? l + l_other : l_other + l;
-            const int unit = it.qt * a.H_q + it.h;
-            float *part_row = a.part + (((int64_t)unit * a.smax + it.s) * BM + r) * PART_ROW(D);
-            float *out_row = a.out + ((int64_t)row * a.H_q + it.h) * D;
-            const float inv = 1.f / l_row;
-#pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
-                tmem_ld_wait();
-                const int col = (D / 2) * grp + c * 32;
-                if (it.ns == 1) {
-                    if (valid) {
+            uint32_t o[D / 2];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4 *>(out_row + col + e) =
-                                make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                                            __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                    }
-                } else if (valid) {
+            for (int c = 0; c < D / 64; ++c) tmem_ld32p(tO + c * 32, o + c * 32);
+            tmem_ld_wait();
+            if (row < a.C) {
+                const int unit = it.qt * a.H_q + it.h;
+                float *dst = it.ns == 1 ? a.out + ((int64_t)row * a.H_q + it.h) * D
+                                        : a.part + (((int64_t)unit * a.smax + it.s) * BM + r) * PART_ROW(D);
+                const float sc = it.ns == 1 ? 1.f / l_row : 1.f;
+                float *half = dst + (D / 2) * grp;
+                if (a.v8) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(part_row + col + e) =
-                            make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
-                                        __uint_as_float(o[e + 3]));
+                    for (int e = 0; e < D / 2; e += 8)
+                        st_global_v8(half + e, __uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
+                                     __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc,
+                                     __uint_as_float(o[e + 4]) * sc, __uint_as_float(o[e + 5]) * sc,
+                                     __uint_as_float(o[e + 6]) * sc, __uint_as_float(o[e + 7]) * sc);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < D / 2; e += 4)
+                        *reinterpret_cast<float4 *>(half + e) =
+                            make_float4(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
+                                        __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc);
+                }
+                if (it.ns > 1 && grp == 0) {
+                    dst[D] = m_ref;
+                    dst[D + 1] = l_row;
                 }
             }
-            if (it.ns > 1 && valid && grp == 0) {
-                part_row[D] = m_ref;
-                part_row[D + 1] = l_row;
-            }
-            tc_fence_before();
-            mbar_arrive(&bars[B_OFREE]);
         }
     } else if (Q8) {
         // ------------------------------------------------------------------ dequantise
@@ -811,6 +809,7 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     a.vs = static_cast<const uint16_t *>(c.v_s);
     a.out = out;
     a.part = static_cast<float *>(scratch);
+    a.v8 = ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(scratch)) & 31) == 0;
     a.g = g;
     a.layer = layer;
     a.pos0 = pos0;

@@ -211,6 +211,14 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Two floats to one fp16x2 word (lo in the low half), both rounded to nearest even, by one packed
 // conversion instruction (two scalar conversions plus a merge cost several times more).
+// 32 bytes to global memory in one access (the address must be 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(float *p, float a0, float a1, float a2, float a3, float a4, float a5,
+                                             float a6, float a7) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a0), "f"(a1), "f"(a2),
+                 "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
