@@ -544,17 +544,23 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
 // Tiles of 128 keys.  S^T = K Q^T with M = 128 keys, N = 16 (the G query heads of the group,
 // zero-padded), both operands in shared memory; O^T += V^T P^T with M = 128 head-dim rows, N = 16,
 // V as an MN-major operand and P^T written to shared memory by the softmax threads.  Accumulators
-// live in tensor memory (S double-buffered), so the warps hold no MMA state.
+// live in tensor memory (S double-buffered), so the warps hold no MMA state.  A chain of dependent
+// N = 16 MMAs advances about one step per 220 cycles, while independent chains issued interleaved
+// overlap (MMAs of one kind: interleaving S and PV steps costs more than it saves); so S is
+// accumulated as two partial sums (head-dim halves) and O^T as two (key halves of each tile), and the
+// MMA issuer interleaves the two chains of each.
 //   warp 0      TMA producer: K and V tiles (f16) or their int8 codes (q8_0)
 //   warp 1      allocates TMEM; one lane issues the MMAs: S(0), S(1), then per tile PV(k), S(k+2)
 //   warps 2-5   softmax: thread = key of the tile (TMEM lane); per-head tile maxima are combined
 //               across the four warps through shared memory; P^T to shared memory; O^T rescaled
 //               (thread = head-dim row) when a running max grows by more than 2^8
-//   warps 6-9   (q8_0) dequantise K and V rows into fp16 d*q, separate K and V rings
+//   warps 6-9   (q8_0) dequantise K and V rows into fp16 d*q, separate K and V rings (one thread
+//               per key row; NDQ = 256 gives two per row, one per head-dim half)
 constexpr int TK = 128;                 // keys per tile
 constexpr int NH = 16;                  // MMA N: query heads of a group, padded
-constexpr uint32_t TC_COLS = 64;        // TMEM: S double buffer (2 x 16) and O^T (16)
-constexpr uint32_t COL_O = 32;
+// TMEM: S buffer b, half hh at column 32 b + 16 hh; O^T part hh at COL_O + 16 hh
+constexpr uint32_t TC_COLS = 128;
+constexpr uint32_t COL_O = 64;
 constexpr float TC_RESCALE_LOG2 = 8.0f;
 
 template <bool Q8>
@@ -573,7 +579,9 @@ struct TCfg {
     static constexpr int USED = OFF_BAR + 512;
     static constexpr int ALLOC = USED + 1024;
     static_assert(ALLOC <= 232448, "shared memory plan too large");
-    static constexpr int THREADS = Q8 ? 320 : 192;
+    static constexpr int NDQ = 128;                         // dequantising threads (q8_0): 1 or 2 per key
+    static constexpr int THREADS = Q8 ? 192 + NDQ : 192;
+    static constexpr int CTAS = 1;                          // CTAs per SM
 };
 
 enum TcBar {
@@ -628,7 +636,7 @@ __device__ __forceinline__ void dequant4(uint32_t w, __half2 d2, uint32_t &lo, u
 
 // GM: heads the softmax loops cover (8 when the group has at most 8 query heads, else 16)
 template <bool Q8, int DT, int GM>
-__global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
+__global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeArgs a) {
     using L = TCfg<Q8>;
@@ -658,17 +666,17 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
         mbar_init(&bars[T_XCHG], 128);
         mbar_init(&bars[T_DRAIN], 1);
         for (int s = 0; s < L::NK; ++s) {
-            mbar_init(&bars[T_KFULL + s], Q8 ? 128 : 1);
+            mbar_init(&bars[T_KFULL + s], Q8 ? L::NDQ : 1);
             mbar_init(&bars[T_KEMPTY + s], 1);
         }
         for (int s = 0; s < L::NV; ++s) {
-            mbar_init(&bars[T_VFULL + s], Q8 ? 128 : 1);
+            mbar_init(&bars[T_VFULL + s], Q8 ? L::NDQ : 1);
             mbar_init(&bars[T_VEMPTY + s], 1);
         }
         if constexpr (Q8) {
             for (int s = 0; s < L::NR; ++s) {
                 mbar_init(&bars[T_RFULL + s], 1);
-                mbar_init(&bars[T_REMPTY + s], 128);
+                mbar_init(&bars[T_REMPTY + s], L::NDQ);
             }
         }
         fence_mbar_init();
@@ -743,37 +751,60 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
             const uint32_t sQ = smem_u32(sm + L::OFF_QT), sP = smem_u32(sm + L::OFF_PT);
             bool ok = mbar_wait(&bars[T_QREADY], 0, s_abort);
             tc_fence_after();
-            auto issue_s = [&](int j) -> bool {
-                const int ks = j % L::NK;
-                if (!mbar_wait(&bars[T_KFULL + ks], (j / L::NK) & 1, s_abort)) return false;
+            auto wait_k = [&](int j) -> bool {
+                if (!mbar_wait(&bars[T_KFULL + j % L::NK], (j / L::NK) & 1, s_abort)) return false;
                 tc_fence_after();
-                const uint32_t kb = sK + ks * L::OPT;
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t kk = (s & 3) * 32;
-                    umma_ss(tmem + 16 * (j & 1), sdesc_sw128(kb + (s >> 2) * (TK * 128) + kk, 16, 1024),
-                            sdesc_sw128(sQ + (s >> 2) * (NH * 128) + kk, 16, 1024), IDESC_S, s > 0);
-                }
-                umma_commit(&bars[T_SFULL0 + (j & 1)]);
-                umma_commit(&bars[T_KEMPTY + ks]);
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            if (ok && T > 1) ok = issue_s(1);
+            // step s (0..3) of both halves of S(j): head-dim k-steps s and 4 + s
+            auto s_mma = [&](int j, int s) {
+                const uint32_t kb = sK + (j % L::NK) * L::OPT;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int ks = 4 * hh + s;
+                    const uint32_t kk = (ks & 3) * 32;
+                    umma_ss(tmem + 32 * (j & 1) + 16 * hh, sdesc_sw128(kb + (ks >> 2) * (TK * 128) + kk, 16, 1024),
+                            sdesc_sw128(sQ + (ks >> 2) * (NH * 128) + kk, 16, 1024), IDESC_S, s > 0);
+                }
+            };
+            // step s of both key halves of PV(k): key k-steps s and 4 + s
+            auto pv_mma = [&](int k, int s) {
+                const uint32_t vb = sV + (k % L::NV) * L::OPT, pb = sP + (k & 1) * (NH * TK * 2);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int ks = 4 * hh + s;
+                    umma_ss(tmem + COL_O + 16 * hh, sdesc_sw128(vb + ks * 16 * 128, TK * 128, 1024),
+                            sdesc_sw128(pb + (ks >> 2) * (NH * 128) + (ks & 3) * 32, 16, 1024), IDESC_O,
+                            (k > 0 || s > 0) ? 1u : 0u);
+                }
+            };
+            auto commit_s = [&](int j) {
+                umma_commit(&bars[T_SFULL0 + (j & 1)]);
+                umma_commit(&bars[T_KEMPTY + j % L::NK]);
+            };
+            // S(0) and S(1) (S(1) into the other buffer), then per tile PV(k) with S(k + 2)
+            for (int j = 0; ok && j < 2 && j < T; ++j) {
+                if (!wait_k(j)) { ok = false; break; }
+#pragma unroll
+                for (int s = 0; s < 4; ++s) s_mma(j, s);
+                commit_s(j);
+            }
             for (int k = 0; ok && k < T; ++k) {
                 if (!mbar_wait(&bars[T_PFULL0 + (k & 1)], (k >> 1) & 1, s_abort)) { ok = false; break; }
                 const int vs = k % L::NV;
                 if (!mbar_wait(&bars[T_VFULL + vs], (k / L::NV) & 1, s_abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t vb = sV + vs * L::OPT, pb = sP + (k & 1) * (NH * TK * 2);
 #pragma unroll
-                for (int s = 0; s < TK / 16; ++s)
-                    umma_ss(tmem + COL_O, sdesc_sw128(vb + s * 16 * 128, TK * 128, 1024),
-                            sdesc_sw128(pb + (s >> 2) * (NH * 128) + (s & 3) * 32, 16, 1024), IDESC_O,
-                            (k > 0 || s > 0) ? 1u : 0u);
+                for (int s = 0; s < 4; ++s) pv_mma(k, s);
                 umma_commit(&bars[T_ODONE0 + (k & 1)]);
                 umma_commit(&bars[T_VEMPTY + vs]);
-                if (k + 2 < T && !issue_s(k + 2)) { ok = false; break; }
+                // S(k + 2) reuses S(k)'s buffer, which the softmax read before publishing P(k)
+                if (k + 2 < T) {
+                    if (!wait_k(k + 2)) { ok = false; break; }
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) s_mma(k + 2, s);
+                    commit_s(k + 2);
+                }
             }
             if (*s_abort) {
                 // after a wait gave up: let the MMAs in flight finish before TMEM is freed
@@ -829,8 +860,11 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
         for (int k = 0; k < T; ++k) {
             if (!mbar_wait(&bars[T_SFULL0 + (k & 1)], (k >> 1) & 1, s_abort)) { ok = false; break; }
             tc_fence_after();
-            float sc[NH];
-            tmem_ld16(tmem + 16 * (k & 1) + lane_base, sc);
+            float sc[NH], sc_hi[NH];
+            tmem_ld16(tmem + 32 * (k & 1) + lane_base, sc);
+            tmem_ld16(tmem + 32 * (k & 1) + 16 + lane_base, sc_hi);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) sc[h] += sc_hi[h];
             const bool valid = j_begin + k * TK + L0 < j_end;
             // branch-free over the 16 padded heads: heads >= G score -inf, offset 0, so p = 0 exactly
             float x[GM];
@@ -875,11 +909,14 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
             if (k >= 2 && !wait_pv(k - 2)) { ok = false; break; }
             if (rescale && k >= 1) {
                 if (!wait_pv(k - 1)) { ok = false; break; }
-                float o[NH];
-                tmem_ld16(tmem + COL_O + lane_base, o);
 #pragma unroll
-                for (int h = 0; h < GM; ++h) o[h] *= alpha[h];
-                tmem_st16f(tmem + COL_O + lane_base, o);
+                for (int hh = 0; hh < 2; ++hh) {
+                    float o[NH];
+                    tmem_ld16(tmem + COL_O + 16 * hh + lane_base, o);
+#pragma unroll
+                    for (int h = 0; h < GM; ++h) o[h] *= alpha[h];
+                    tmem_st16f(tmem + COL_O + 16 * hh + lane_base, o);
+                }
                 tmem_st_wait();
             }
             uint8_t *pt = sm + L::OFF_PT + (k & 1) * (NH * TK * 2) + (L0 >> 6) * (NH * 128);
@@ -893,8 +930,11 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
         }
         // ---- epilogue: this split's (m, l, O) per head of the group
         if (ok && T > 0 && wait_pv(T - 1)) {
-            float o[NH];
+            float o[NH], o_hi[NH];
             tmem_ld16(tmem + COL_O + lane_base, o);
+            tmem_ld16(tmem + COL_O + 16 + lane_base, o_hi);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) o[h] += o_hi[h];
             // row sums: over the warp (fixed tree), then the four warps in order
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
@@ -928,19 +968,30 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
         }
     } else if constexpr (Q8) {
         // ------------------------------------------------------------------ dequantise (q8_0)
-        const int r = threadIdx.x - 192;   // key row of the tile
+        constexpr int HPT = 256 / L::NDQ;               // head-dim halves per thread
+        const int dt = threadIdx.x - 192;
+        const int r = dt & (TK - 1), hd0 = dt / TK;   // key row of the tile, first head-dim half
         constexpr int NB = D / 32;
         bool ok = true;
-        uint2 sk_n = make_uint2(0u, 0u), sv_n = sk_n;
-        auto scales = [&](int k, uint2 &sk, uint2 &sv) {
+        uint32_t sk_n[HPT], sv_n[HPT];
+        // the fp16 scales of blocks 2 hd and 2 hd + 1 of my key's K and V rows, for my halves hd
+        auto scales = [&](int k, uint32_t (&sk)[HPT], uint32_t (&sv)[HPT]) {
             const int key = min(j_begin + k * TK + r, a.n_keys - 1);  // keys past the end: any finite scale
             const int64_t srow = a.layer * a.g.s_layer + hkv * a.g.s_head + (int64_t)key * a.g.s_tok;
-            sk = __ldg(reinterpret_cast<const uint2 *>(a.ks + srow));
-            sv = __ldg(reinterpret_cast<const uint2 *>(a.vs + srow));
+#pragma unroll
+            for (int hh = 0; hh < HPT; ++hh) {
+                sk[hh] = __ldg(reinterpret_cast<const uint32_t *>(a.ks + srow) + hd0 + hh);
+                sv[hh] = __ldg(reinterpret_cast<const uint32_t *>(a.vs + srow) + hd0 + hh);
+            }
         };
         if (T > 0) scales(0, sk_n, sv_n);
         for (int k = 0; ok && k < T; ++k) {
-            const uint2 sk = sk_n, sv = sv_n;
+            uint32_t sk[HPT], sv[HPT];
+#pragma unroll
+            for (int hh = 0; hh < HPT; ++hh) {
+                sk[hh] = sk_n[hh];
+                sv[hh] = sv_n[hh];
+            }
             if (k + 1 < T) scales(k + 1, sk_n, sv_n);
             const int rs = k % L::NR;
             if (!mbar_wait(&bars[T_RFULL + rs], (k / L::NR) & 1, s_abort)) { ok = false; break; }
@@ -955,25 +1006,30 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, 1)
                 }
                 const uint8_t *src = raw + kv * (TK * D);
                 uint8_t *dst = sm + (kv ? L::OFF_V : L::OFF_K) + s * L::OPT;
-                const uint2 sw = kv ? sv : sk;
-                uint4 q[D / 16];
 #pragma unroll
-                for (int c = 0; c < D / 16; ++c) q[c] = *reinterpret_cast<const uint4 *>(src + sw128(r, c));
+                for (int hh = 0; hh < HPT; ++hh) {
+                const int hd = hd0 + hh;
+                const uint32_t sw = kv ? sv[hh] : sk[hh];
+                // my half row: 16-byte code chunks 4 hd .. 4 hd + 3 (two 32-value blocks)
+                uint4 q[D / 32];
 #pragma unroll
-                for (int c = 0; c < D / 16; ++c) {
-                    const int b = c >> 1;
-                    const unsigned short sb = (unsigned short)((b < 2 ? sw.x : sw.y) >> (16 * (b & 1)));
+                for (int i = 0; i < D / 32; ++i) q[i] = *reinterpret_cast<const uint4 *>(src + sw128(r, 4 * hd + i));
+#pragma unroll
+                for (int i = 0; i < D / 32; ++i) {
+                    const int c = 4 * hd + i;
+                    const unsigned short sb = (unsigned short)(sw >> (16 * (i >> 1)));
                     const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
                     uint32_t o[8];
-                    dequant4(q[c].x, d2, o[0], o[1]);
-                    dequant4(q[c].y, d2, o[2], o[3]);
-                    dequant4(q[c].z, d2, o[4], o[5]);
-                    dequant4(q[c].w, d2, o[6], o[7]);
+                    dequant4(q[i].x, d2, o[0], o[1]);
+                    dequant4(q[i].y, d2, o[2], o[3]);
+                    dequant4(q[i].z, d2, o[4], o[5]);
+                    dequant4(q[i].w, d2, o[6], o[7]);
                     // fp16 chunk 2c and 2c + 1 of the row: column block (2c) / 8, chunk (2c) % 8 inside it
                     *reinterpret_cast<uint4 *>(dst + (c >> 2) * (TK * 128) + sw128(r, (2 * c) & 7)) =
                         make_uint4(o[0], o[1], o[2], o[3]);
                     *reinterpret_cast<uint4 *>(dst + (c >> 2) * (TK * 128) + sw128(r, (2 * c + 1) & 7)) =
                         make_uint4(o[4], o[5], o[6], o[7]);
+                }
                 }
                 // order the operand writes before the MMA (async proxy) reads them
                 fence_proxy_async_smem();
@@ -1001,7 +1057,7 @@ int launch_tc(const kvc_cache &c, const DecodeArgs &a0, int n_head_q, float *out
     constexpr int D = 128;
     DecodeArgs a = a0;
     // one wave, one CTA per SM over (split, kv head), whole tiles per split
-    const int target = sm_count() / a.n_head_kv;
+    const int target = (L::CTAS * sm_count()) / a.n_head_kv;
     int n_split = (a.n_keys + TK - 1) / TK;
     if (n_split > target) n_split = target;
     if (n_split > MAX_SPLIT) n_split = MAX_SPLIT;
