@@ -10,13 +10,18 @@
 // amax exact, d = amax/127 and x/d by IEEE division, ties away from zero,
 // fp16 by round to nearest even.
 //
-// Work split.  q8_0: one thread per 32-value block (two or four 16-byte input
-// loads in flight per thread, 32 code bytes and one 2-byte scale stored).  The
+// Work split.  q8_0: one thread per 32-value block.  A warp's 32 blocks are
+// one contiguous run of input, loaded 16 bytes per lane (consecutive lanes on
+// consecutive chunks) into shared memory, from which each lane takes its own
+// block; 32 code bytes and one 2-byte scale are stored per block.  The
 // quotient x/d is taken as x times the IEEE reciprocal of d and rounded with a
 // 1.5*2^23 shift; that product is within 5e-5 of the IEEE quotient, so the
 // rounded code can differ from round(x/d) only when the product lies within
 // that distance of a .5 boundary, and exactly those values are recomputed with
-// the IEEE division.  f16: one thread per 8 values.  HBM-bound.
+// the IEEE division (both values of a pair, the one away from the boundary
+// giving the same code either way).  The arithmetic runs on fp32 pairs.  A
+// non-finite block (outside the method's domain) stores zero codes.  f16: one
+// thread per 8 values.  HBM-bound.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -76,43 +81,98 @@ __global__ void __launch_bounds__(256) append_f16_kernel(
     *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// the values of one 16-byte input chunk (8 bf16 / f16 or 4 f32) as floats
+template <int DT>
+__device__ __forceinline__ void chunk_values(const uint4 &u, float *x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (DT == KVC_IN_F32) {
+            x[i] = __uint_as_float(w[i]);
+        } else if constexpr (DT == KVC_IN_BF16) {
+            // bf16 -> f32 is exact: the bf16 bits are the top half of the f32
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        } else {
+            x[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFF)));
+            x[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+        }
+    }
+}
+
+// Staging slot of 16-byte chunk c of a warp's input: XOR-swizzled so that lanes storing consecutive
+// chunks and lanes reading their own block's chunks are both free of bank conflicts.
+__device__ __forceinline__ int stage_slot(int c) { return c ^ ((c >> 3) & 7); }
+
 // q8_0 cache: one thread per 32-value block; grid.y selects K (0) or V (1).
 template <int DT>
 __global__ void __launch_bounds__(256) append_q8_kernel(
     const void *__restrict__ k, const void *__restrict__ v, int64_t n_blocks, int nb, int H, void *kq,
     uint16_t *ks, void *vq, uint16_t *vs, Geom g, int layer, int pos0) {
     asm volatile("griddepcontrol.launch_dependents;");
+    constexpr int ESZ = DT == KVC_IN_F32 ? 4 : 2;
+    constexpr int CPB = 2 * ESZ;                   // 16-byte input chunks per block
+    __shared__ uint4 stage[8][32 * CPB];
     const bool is_v = blockIdx.y != 0;
-    const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    uint4 *S = stage[threadIdx.x >> 5];
+    const int64_t blk0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;   // the warp's first block
+    if (blk0 >= n_blocks) return;   // the whole warp
+    const int nwc = (int)min((int64_t)32, n_blocks - blk0) * CPB;                 // the warp's input chunks
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(is_v ? v : k) + blk0 * 32 * ESZ);
+    {
+        uint4 t[CPB];
+#pragma unroll
+        for (int m = 0; m < CPB; ++m) {
+            const int c = 32 * m + lane;
+            t[m] = c < nwc ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int m = 0; m < CPB; ++m) S[stage_slot(32 * m + lane)] = t[m];
+    }
+    __syncwarp();
+    const int64_t blk = blk0 + lane;
     if (blk >= n_blocks) return;
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < CPB; ++j) chunk_values<DT>(S[stage_slot(CPB * lane + j)], x + j * (16 / ESZ));
     const int64_t row = blk / nb;                    // (token, head) in input order
     const int b = (int)(blk - row * nb);
     const int tok = (int)(row / H), head = (int)(row - (int64_t)tok * H);
-    float x[32];
+    float m2[2] = {0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float t8[8];
-        load8<DT>(is_v ? v : k, blk * 32 + 8 * j, t8);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[8 * j + i] = t8[i];
+    for (int i = 0; i < 32; i += 4) {
+        m2[0] = ptx::fmax3(m2[0], fabsf(x[i]), fabsf(x[i + 1]));
+        m2[1] = ptx::fmax3(m2[1], fabsf(x[i + 2]), fabsf(x[i + 3]));
     }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    const float amax = fmaxf(m2[0], m2[1]);
     const float d = __fdiv_rn(amax, 127.0f);
     uint32_t packed[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (d > 0.f) {  // codes are zero when amax/127 is zero (x/d undefined)
+    // codes are zero when amax/127 is zero (x/d undefined); |x * r| <= 127 (to an ulp) otherwise
+    if (d > 0.f && amax <= 3.402823466e38f) {
         const float r = __frcp_rn(d);
+        const uint64_t r2 = ptx::f2_pack(r, r), mz = ptx::f2_pack(-0.f, -0.f), M2 = ptx::f2_pack(12582912.f, 12582912.f),
+                       nM2 = ptx::f2_pack(-12582912.f, -12582912.f), n1 = ptx::f2_pack(-1.f, -1.f);
+        int q[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float y = x[i] * r;
-            const float t = y + 12582912.0f;                 // y rounded to an integer (to even)
-            const float f = y - (t - 12582912.0f);            // y minus that integer, in [-1/2, 1/2]
-            int q = __float_as_int(t) - 0x4B400000;
-            if (fabsf(f) > 0.4999f) q = (int)roundf(__fdiv_rn(x[i], d));  // near a tie: exact quotient
-            q = min(max(q, -127), 127);
-            packed[i >> 2] |= (uint32_t)(q & 0xFF) << (8 * (i & 3));
+        for (int i = 0; i < 32; i += 2) {
+            const uint64_t y = ptx::f2_fma(ptx::f2_pack(x[i], x[i + 1]), r2, mz);   // x * r, one rounding
+            const uint64_t t = ptx::f2_add(y, M2);                                // y rounded to an integer (to even)
+            const uint64_t f = ptx::f2_fma(ptx::f2_add(t, nM2), n1, y);              // y minus that integer
+            float t0, t1, f0, f1;
+            ptx::f2_unpack(t, t0, t1);
+            ptx::f2_unpack(f, f0, f1);
+            q[i] = __float_as_int(t0) - 0x4B400000;
+            q[i + 1] = __float_as_int(t1) - 0x4B400000;
+            if (fmaxf(fabsf(f0), fabsf(f1)) > 0.4999f) {  // near a tie: exact quotients
+                q[i] = (int)roundf(__fdiv_rn(x[i], d));
+                q[i + 1] = (int)roundf(__fdiv_rn(x[i + 1], d));
+            }
         }
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            packed[w] = __byte_perm(__byte_perm(q[4 * w], q[4 * w + 1], 0x0040),
+                                    __byte_perm(q[4 * w + 2], q[4 * w + 3], 0x0040), 0x5410);
     }
     const int64_t pos = (int64_t)pos0 + tok;
     int8_t *dst = static_cast<int8_t *>(is_v ? vq : kq) + layer * g.c_layer + pos * g.c_tok + head * g.c_head + b * 32;

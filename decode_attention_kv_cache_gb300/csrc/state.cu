@@ -12,13 +12,18 @@
 // [fp16 scale][32 int8 codes] (q8_0) or head_dim fp16 values (f16).
 //
 // q8_0: the body is a sequence of 34-byte blocks.  Eight consecutive blocks
-// are a 272-byte unit that starts on a 16-byte boundary (32 + 272u), so one
-// thread moves one unit: pack loads the eight blocks' 32-byte code runs and
-// 2-byte scales and assembles the 17 16-byte output chunks with byte permutes
-// (a block pair is 17 words: scale + codes shifted by two bytes, then the
-// second scale, then the second block's codes word-aligned); unpack is the
-// mirror image.  A last unit with fewer than eight blocks moves halfword by
-// halfword.  f16: records are runs of 16-byte chunks; one thread moves four.
+// are a 272-byte unit that starts on a 16-byte boundary (32 + 272u); a lane
+// assembles one unit from its eight blocks' 32-byte code runs and 2-byte
+// scales with byte permutes (a block pair is 17 words: scale + codes shifted
+// by two bytes, then the second scale, then the second block's codes
+// word-aligned), and unpack splits it the same way back.  A warp takes 32
+// consecutive units through shared memory, so that both sides move in long
+// runs: the cache side as 16-byte code chunks with consecutive lanes on
+// consecutive chunks (8 lanes per 128-byte row of a head) and 2-byte scales,
+// the stream side as the warp's 8704 contiguous bytes, 16 per lane.  The
+// stream's last bytes (a body that ends inside a 16-byte chunk) move halfword
+// by halfword.  f16: records are runs of 16-byte chunks; a warp moves 128 consecutive chunks, lane by
+// lane.
 // Both are HBM-bound copies with a permutation.
 #include <cuda_runtime.h>
 
@@ -116,77 +121,166 @@ __device__ __forceinline__ void disassemble(const uint32_t (&w)[68], uint32_t (&
     }
 }
 
-__global__ void __launch_bounds__(THREADS) pack_q8_kernel(const StateArgs a) {
-    const int64_t u = (int64_t)blockIdx.x * THREADS + threadIdx.x;
-    const int64_t beta0 = u * 8;
-    if (beta0 >= a.n_blocks) return;
-    const int nblk = (int)min((int64_t)8, a.n_blocks - beta0);
-    uint32_t sc[8];
-    uint4 c[16];
-    BlockPos p = block_pos(a, beta0);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i < nblk) {
-            const uint8_t *src = (p.kv ? a.vq : a.kq) + code_off(a, p);
-            c[2 * i] = __ldg(reinterpret_cast<const uint4 *>(src));
-            c[2 * i + 1] = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
-            sc[i] = __ldg((p.kv ? a.vs : a.ks) + scale_off(a, p));
-            next_block(a, p);
+// p moved on by n blocks in stream order (n >= 0)
+__device__ __forceinline__ void advance(const StateArgs &a, BlockPos &p, int n) {
+    const int bpr = a.H * a.nb;
+    int within = p.h * a.nb + p.b + n;
+    while (within >= bpr) {
+        within -= bpr;
+        if (p.kv == 0) {
+            p.kv = 1;
         } else {
-            c[2 * i] = c[2 * i + 1] = make_uint4(0u, 0u, 0u, 0u);
-            sc[i] = 0u;
+            p.kv = 0;
+            if (++p.t == a.n_tokens) {
+                p.t = 0;
+                ++p.layer;
+            }
         }
     }
+    p.h = within / a.nb;
+    p.b = within - p.h * a.nb;
+}
+
+constexpr int QW = 4;                    // warps per CTA (q8_0 pack and unpack)
+constexpr int WARP_UNITS = 32;
+constexpr int WARP_BLOCKS = 8 * WARP_UNITS;
+constexpr int WARP_BYTES = 272 * WARP_UNITS;
+
+struct __align__(16) WarpStage {
+    uint8_t buf[WARP_BYTES];             // the warp's block codes (swizzled chunks), then its 32 units
+    uint16_t sc[WARP_BLOCKS];            // the warp's block scales
+};
+
+// Position of 16-byte code chunk c (block c / 2, half c % 2) in the staging: XOR-swizzled so that a
+// lane reading its unit's 16 consecutive chunks and lanes writing consecutive chunks are both free
+// of bank conflicts.
+__device__ __forceinline__ int phys_chunk(int c) { return c ^ ((c >> 4) & 7); }
+
+__global__ void __launch_bounds__(QW * 32) pack_q8_kernel(const StateArgs a) {
+    __shared__ WarpStage stage[QW];
+    const int lane = threadIdx.x & 31;
+    WarpStage &S = stage[threadIdx.x >> 5];
+    const int64_t wg = (int64_t)blockIdx.x * QW + (threadIdx.x >> 5);
+    const int64_t beta0 = wg * WARP_BLOCKS;
+    if (beta0 >= a.n_blocks) return;   // the whole warp
+    {
+        // code chunk 32 m + lane of the warp: block beta0 + 16 m + lane / 2, half lane % 2
+        uint4 v[16];
+        BlockPos p = block_pos(a, beta0 + (lane >> 1));
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            v[m] = make_uint4(0u, 0u, 0u, 0u);
+            if (beta0 + 16 * m + (lane >> 1) < a.n_blocks)
+                v[m] = __ldg(reinterpret_cast<const uint4 *>((p.kv ? a.vq : a.kq) + code_off(a, p)) + (lane & 1));
+            if (m < 15) advance(a, p, 16);
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) *reinterpret_cast<uint4 *>(S.buf + 16 * phys_chunk(32 * m + lane)) = v[m];
+        // scale of block beta0 + 32 m + lane
+        uint16_t s8[8];
+        BlockPos q = block_pos(a, beta0 + lane);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            s8[m] = 0;
+            if (beta0 + 32 * m + lane < a.n_blocks) s8[m] = __ldg((q.kv ? a.vs : a.ks) + scale_off(a, q));
+            if (m < 7) advance(a, q, 32);
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) S.sc[32 * m + lane] = s8[m];
+    }
+    __syncwarp();
+    // my unit: blocks 8 lane .. 8 lane + 7, i.e. chunks 16 lane .. 16 lane + 15
+    uint4 c[16];
+    uint32_t sc[8];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) c[k] = *reinterpret_cast<const uint4 *>(S.buf + 16 * phys_chunk(16 * lane + k));
+    {
+        const uint4 s4 = *reinterpret_cast<const uint4 *>(S.sc + 8 * lane);
+        const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc[i] = (sw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    }
+    __syncwarp();
     uint32_t w[68];
     assemble(sc, c, w);
-    uint8_t *dst = a.body + u * 272;
-    if (nblk == 8) {
 #pragma unroll
-        for (int k = 0; k < 17; ++k)
-            *reinterpret_cast<uint4 *>(dst + 16 * k) = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-    } else {
-        // the body ends inside this unit: 17 halfwords per block
-        uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
+    for (int k = 0; k < 17; ++k)
+        *reinterpret_cast<uint4 *>(S.buf + 272 * lane + 16 * k) = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    __syncwarp();
+    // the warp's stream bytes (the body may end inside them)
+    const int64_t off0 = wg * WARP_BYTES;
+    const int nbytes = (int)min((int64_t)WARP_BYTES, a.n_blocks * 34 - off0);
 #pragma unroll
-        for (int x = 0; x < 136; ++x)
-            if (x < 17 * nblk) d16[x] = (uint16_t)(w[x >> 1] >> (16 * (x & 1)));
+    for (int m = 0; m < 17; ++m) {
+        const int o = 16 * (32 * m + lane);
+        if (o + 16 <= nbytes) {
+            *reinterpret_cast<uint4 *>(a.body + off0 + o) = *reinterpret_cast<const uint4 *>(S.buf + o);
+        } else if (o < nbytes) {
+            for (int x = o; x < nbytes; x += 2)
+                *reinterpret_cast<uint16_t *>(a.body + off0 + x) = *reinterpret_cast<const uint16_t *>(S.buf + x);
+        }
     }
 }
 
-__global__ void __launch_bounds__(THREADS) unpack_q8_kernel(const StateArgs a) {
-    const int64_t u = (int64_t)blockIdx.x * THREADS + threadIdx.x;
-    const int64_t beta0 = u * 8;
-    if (beta0 >= a.n_blocks) return;
-    const int nblk = (int)min((int64_t)8, a.n_blocks - beta0);
-    const uint8_t *src = a.body + u * 272;
-    uint32_t w[68];
-    if (nblk == 8) {
+__global__ void __launch_bounds__(QW * 32) unpack_q8_kernel(const StateArgs a) {
+    __shared__ WarpStage stage[QW];
+    const int lane = threadIdx.x & 31;
+    WarpStage &S = stage[threadIdx.x >> 5];
+    const int64_t wg = (int64_t)blockIdx.x * QW + (threadIdx.x >> 5);
+    const int64_t beta0 = wg * WARP_BLOCKS;
+    if (beta0 >= a.n_blocks) return;   // the whole warp
+    // the warp's stream bytes into the staging (zero past the body's end)
+    const int64_t off0 = wg * WARP_BYTES;
+    const int nbytes = (int)min((int64_t)WARP_BYTES, a.n_blocks * 34 - off0);
+    {
+        uint4 v[17];
 #pragma unroll
-        for (int k = 0; k < 17; ++k) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + k);
-            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+        for (int m = 0; m < 17; ++m) {
+            const int o = 16 * (32 * m + lane);
+            v[m] = make_uint4(0u, 0u, 0u, 0u);
+            if (o + 16 <= nbytes) {
+                v[m] = __ldg(reinterpret_cast<const uint4 *>(a.body + off0 + o));
+            } else if (o < nbytes) {
+                uint32_t t[4] = {0u, 0u, 0u, 0u};
+                for (int x = o; x < nbytes; x += 2)
+                    t[(x - o) >> 2] |= (uint32_t)__ldg(reinterpret_cast<const uint16_t *>(a.body + off0 + x))
+                                       << (8 * ((x - o) & 3));
+                v[m] = make_uint4(t[0], t[1], t[2], t[3]);
+            }
         }
-    } else {
 #pragma unroll
-        for (int k = 0; k < 68; ++k) w[k] = 0u;
-        const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
+        for (int m = 0; m < 17; ++m) *reinterpret_cast<uint4 *>(S.buf + 16 * (32 * m + lane)) = v[m];
+    }
+    __syncwarp();
+    uint32_t w[68];
 #pragma unroll
-        for (int x = 0; x < 136; ++x)
-            if (x < 17 * nblk) w[x >> 1] |= (uint32_t)__ldg(s16 + x) << (16 * (x & 1));
+    for (int k = 0; k < 17; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(S.buf + 272 * lane + 16 * k);
+        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
     }
     uint32_t sc[8];
     uint4 c[16];
     disassemble(w, sc, c);
-    BlockPos p = block_pos(a, beta0);
+    __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i < nblk) {
-            uint8_t *dst = (p.kv ? a.vq : a.kq) + code_off(a, p);
-            reinterpret_cast<uint4 *>(dst)[0] = c[2 * i];
-            reinterpret_cast<uint4 *>(dst)[1] = c[2 * i + 1];
-            (p.kv ? a.vs : a.ks)[scale_off(a, p)] = (uint16_t)sc[i];
-            next_block(a, p);
-        }
+    for (int k = 0; k < 16; ++k) *reinterpret_cast<uint4 *>(S.buf + 16 * phys_chunk(16 * lane + k)) = c[k];
+    *reinterpret_cast<uint4 *>(S.sc + 8 * lane) = make_uint4(sc[0] | (sc[1] << 16), sc[2] | (sc[3] << 16),
+                                                           sc[4] | (sc[5] << 16), sc[6] | (sc[7] << 16));
+    __syncwarp();
+    // code chunk 32 m + lane and scale 32 m + lane of the warp to the cache
+    BlockPos p = block_pos(a, beta0 + (lane >> 1));
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        if (beta0 + 16 * m + (lane >> 1) < a.n_blocks)
+            reinterpret_cast<uint4 *>((p.kv ? a.vq : a.kq) + code_off(a, p))[lane & 1] =
+                *reinterpret_cast<const uint4 *>(S.buf + 16 * phys_chunk(32 * m + lane));
+        if (m < 15) advance(a, p, 16);
+    }
+    BlockPos q = block_pos(a, beta0 + lane);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        if (beta0 + 32 * m + lane < a.n_blocks) (q.kv ? a.vs : a.ks)[scale_off(a, q)] = S.sc[32 * m + lane];
+        if (m < 7) advance(a, q, 32);
     }
 }
 
@@ -204,20 +298,22 @@ __device__ __forceinline__ uint8_t *f16_cache_ptr(const StateArgs &a, int64_t ga
     return (kv ? a.vq : a.kq) + 2 * (layer * a.g.c_layer + (int64_t)t * a.g.c_tok + h * a.g.c_head) + 16 * ch;
 }
 
+// a warp moves 32 * F16_CHUNKS consecutive chunks, lane-interleaved: each access is 512 contiguous bytes
 template <bool PACK>
 __global__ void __launch_bounds__(THREADS) copy_f16_kernel(const StateArgs a) {
-    const int64_t first = ((int64_t)blockIdx.x * THREADS + threadIdx.x) * F16_CHUNKS;
+    const int lane = threadIdx.x & 31;
+    const int64_t first = ((int64_t)blockIdx.x * THREADS + (threadIdx.x - lane)) * F16_CHUNKS + lane;
     uint4 v[F16_CHUNKS];
 #pragma unroll
     for (int i = 0; i < F16_CHUNKS; ++i) {
-        const int64_t gamma = first + i;
+        const int64_t gamma = first + 32 * i;
         if (gamma < a.n_chunks)
             v[i] = PACK ? __ldg(reinterpret_cast<const uint4 *>(f16_cache_ptr(a, gamma)))
                         : __ldg(reinterpret_cast<const uint4 *>(a.body) + gamma);
     }
 #pragma unroll
     for (int i = 0; i < F16_CHUNKS; ++i) {
-        const int64_t gamma = first + i;
+        const int64_t gamma = first + 32 * i;
         if (gamma < a.n_chunks) {
             if (PACK) reinterpret_cast<uint4 *>(a.body)[gamma] = v[i];
             else *reinterpret_cast<uint4 *>(f16_cache_ptr(a, gamma)) = v[i];
@@ -256,6 +352,11 @@ __global__ void write_header(uint8_t *dst, uint32_t n_layer, uint32_t H, uint32_
     w[7] = 0u;
 }
 
+int grid_q8(int64_t n_blocks) {
+    const int64_t per_cta = (int64_t)QW * WARP_BLOCKS;
+    return (int)((n_blocks + per_cta - 1) / per_cta);
+}
+
 int grid_for(int64_t work, int per_thread) {
     return (int)((work + (int64_t)THREADS * per_thread - 1) / ((int64_t)THREADS * per_thread));
 }
@@ -267,7 +368,7 @@ int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream
     write_header<<<1, 1, 0, s>>>(dst, c.d.n_layer, c.d.n_head_kv, c.d.head_dim, q8 ? 1u : 0u, n_tokens);
     const StateArgs a = make_args(c, n_tokens, dst + 32);
     if (n_tokens > 0) {
-        if (q8) pack_q8_kernel<<<grid_for(a.n_blocks, 8), THREADS, 0, s>>>(a);
+        if (q8) pack_q8_kernel<<<grid_q8(a.n_blocks), QW * 32, 0, s>>>(a);
         else copy_f16_kernel<true><<<grid_for(a.n_chunks, F16_CHUNKS), THREADS, 0, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
@@ -277,7 +378,7 @@ int launch_state_unpack(const kvc_cache &c, int n_tokens, const uint8_t *src, cu
     const bool q8 = c.d.type == KVC_Q8_0;
     const StateArgs a = make_args(c, n_tokens, const_cast<uint8_t *>(src) + 32);
     if (n_tokens > 0) {
-        if (q8) unpack_q8_kernel<<<grid_for(a.n_blocks, 8), THREADS, 0, s>>>(a);
+        if (q8) unpack_q8_kernel<<<grid_q8(a.n_blocks), QW * 32, 0, s>>>(a);
         else copy_f16_kernel<false><<<grid_for(a.n_chunks, F16_CHUNKS), THREADS, 0, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
