@@ -99,7 +99,7 @@ def test_prefill_other_layer_and_repeatability(kvc):
 
 
 def test_prefill_key_splits_merge_and_stay_chunk_invariant(kvc):
-    # 9,000 keys: the splits (2,048 keys at this context size) are merged in split order; rows of one
+    # 9,000 keys: the splits (4,096 keys at this context size) are merged in split order; rows of one
     # chunking and another must agree bit for bit, and sampled rows must match the oracle
     w = si.small_workload("split", 10, 2, 128, "q8_0", "bf16", n_prompt=9000, chunk=1024, n_decode=0, seed=31,
                           k_outlier_frac=0.01)
