@@ -83,9 +83,9 @@ def prefill_traffic(workload):
 
 
 def prefill_split_keys(n_ctx):
-    """Keys per prefill split as the library chooses them: about a tenth of the cache in steps of
-    1024 keys, at least 2048, and at most 64 splits (in 256-key tiles)."""
-    keys = max((n_ctx // 10 + 512) // 1024 * 1024, 2048)
+    """Keys per prefill split as the library chooses them: about a fifth of the cache in steps of
+    2048 keys, at least 4096, and at most 64 splits (in 256-key tiles)."""
+    keys = max((n_ctx // 10 + 512) // 1024 * 2048, 4096)
     return max(keys, -(-n_ctx // (64 * 256)) * 256)
 
 

@@ -59,6 +59,7 @@ def _load():
         "kv_state_set": (ctypes.c_int, [P(kvc_cache), VP, SZ, P(I32), VP]),
         "kvc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvc_device_status": (ctypes.c_int, [P(I32)]),
+        "kvc_pipeline_chunk": (ctypes.c_int, [I32, I32, I32, ctypes.c_double, P(I32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -171,6 +172,14 @@ class KVCache:
 
     def state_size(self, n_tokens):
         return _lib().kv_state_size(ctypes.byref(self.desc), n_tokens)
+
+
+def pipeline_chunk(n_tokens, cap, stages, b_over_a=1024.0):
+    """Prompt chunk size for prefill over `stages` layer-split pipeline stages (host only)."""
+    c = ctypes.c_int32(0)
+    _check(_lib().kvc_pipeline_chunk(int(n_tokens), int(cap), int(stages), ctypes.c_double(b_over_a),
+                                     ctypes.byref(c)), "kvc_pipeline_chunk")
+    return c.value
 
 
 def kv_cache_append(cache, layer, pos0, k, v, stream=None):

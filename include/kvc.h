@@ -116,6 +116,18 @@ size_t kv_state_size(const kvc_desc *desc, int32_t n_tokens);
  * (shape, non-null, 16-byte alignment).  Writes *out only on success. */
 int kvc_cache_init(kvc_cache *out, const kvc_desc *desc, void *k_q, void *k_s, void *v_q, void *v_s);
 
+/* The prompt chunk size for prefill when the layers are split over `stages`
+ * pipeline stages (strata PR #1441 "Prompt chunks sized for a layer split's
+ * pipeline", sections "Summary" and "What changed"): C = sqrt(n_tokens *
+ * b_over_a / (stages - 1)), where b_over_a is a layer's fixed cost per chunk
+ * over its cost per token (the page uses 1024), rounded up to the 256-token grid,
+ * kept within [512, cap] and evened out over the ceil(n_tokens / C) chunks it
+ * needs (ceil(n_tokens / chunks), rounded up to the grid, within [512, cap]).  A
+ * prompt that fits in one chunk is read whole; one stage gives min(n_tokens,
+ * cap).  Host only.  Writes *chunk on success; KVC_EINVAL for n_tokens, cap or
+ * stages <= 0, a b_over_a that is not finite and positive, or a null chunk. */
+int kvc_pipeline_chunk(int32_t n_tokens, int32_t cap, int32_t stages, double b_over_a, int32_t *chunk);
+
 /* ---- hot path ---------------------------------------------------------------- */
 
 /* Append (quantise and store) the K/V rows of n_tokens tokens at cache

@@ -143,3 +143,28 @@ def test_prefill_scratch_query(kvc):
 def test_strerror(kvc):
     for code in (0, -1, -2, -3, -4, -5, -6, 12):
         assert len(kvc.lib.kvc_strerror(code)) > 0
+
+
+@pytest.mark.parametrize("n,chunk", [(2013, 1024), (3865, 1024), (10041, 2048), (28998, 3328)])
+def test_pipeline_chunk_gives_the_printed_chunks(kvc, n, chunk):
+    # strata #1441, "Prompt chunks sized for a layer split's pipeline": four stages, b/a = 1024
+    assert kvc.pipeline_chunk(n, cap=8192, stages=4) == chunk
+
+
+def test_pipeline_chunk_equals_the_oracle_rule(kvc):
+    from oracle.chunking import pipeline_chunk
+    for n in list(range(1, 3000, 37)) + list(range(3000, 200000, 1999)):
+        for cap in (256, 512, 2048, 4096, 65536):
+            for stages in (1, 2, 3, 4, 8):
+                for ba in (64.0, 1024.0, 3000.5):
+                    assert kvc.pipeline_chunk(n, cap, stages, ba) == pipeline_chunk(n, cap, stages, ba), \
+                        (n, cap, stages, ba)
+
+
+def test_pipeline_chunk_rejects_bad_arguments(kvc):
+    for args in ((0, 8192, 4), (100, 0, 4), (100, 8192, 0), (-5, 8192, 4)):
+        with pytest.raises(kvc.KvcError):
+            kvc.pipeline_chunk(*args)
+    for ba in (0.0, -1.0, float("nan"), float("inf")):
+        with pytest.raises(kvc.KvcError):
+            kvc.pipeline_chunk(1000, 8192, 4, ba)
