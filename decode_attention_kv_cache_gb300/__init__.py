@@ -60,6 +60,7 @@ def _load():
         "kvc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvc_device_status": (ctypes.c_int, [P(I32)]),
         "kvc_pipeline_chunk": (ctypes.c_int, [I32, I32, I32, ctypes.c_double, P(I32)]),
+        "kv_cache_truncate": (ctypes.c_int, [P(kvc_cache), I32, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -243,6 +244,12 @@ def kv_state_set(cache, src, stream=None):
                           _stream(stream, cache.device))
     _check(st, "kv_state_set")
     return n.value
+
+
+def kv_cache_truncate(cache, n_tokens, stream=None):
+    """Rewind `cache` to its first n_tokens positions (later positions cleared to zero bytes)."""
+    _check(_lib().kv_cache_truncate(ctypes.byref(cache.c), int(n_tokens), _stream(stream, cache.device)),
+           "kv_cache_truncate")
 
 
 def kvc_device_status():

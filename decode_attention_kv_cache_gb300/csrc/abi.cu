@@ -181,6 +181,30 @@ int kv_state_set(kvc_cache *cache, const void *src, size_t src_bytes, int32_t *n
     return rc;
 }
 
+int kv_cache_truncate(const kvc_cache *cache, int32_t n_tokens, kvc_stream_t stream) {
+    if (!cache_ok(cache)) return KVC_EINVAL;
+    const kvc_desc &d = cache->d;
+    if (n_tokens < 0 || n_tokens > d.n_ctx) return KVC_ERANGE;
+    if (n_tokens == d.n_ctx) return KVC_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t T = d.n_ctx, n = n_tokens, H = d.n_head_kv, L = d.n_layer;
+    // one strided fill per buffer: rows of positions [0, n_ctx), their tail [n_tokens, n_ctx) cleared
+    auto clear = [&](void *buf, size_t row_bytes) -> bool {  // row_bytes: one position of one row
+        const bool hm = d.layout == KVC_HEAD_MAJOR;
+        const size_t per_pos = hm ? row_bytes : row_bytes * H;   // bytes of one position in a row
+        const size_t rows = hm ? H * L : L;
+        return cudaMemset2DAsync(static_cast<uint8_t *>(buf) + n * per_pos, T * per_pos, 0, (T - n) * per_pos, rows,
+                                 s) == cudaSuccess;
+    };
+    const size_t code_bytes = (size_t)d.head_dim * (d.type == KVC_Q8_0 ? 1 : 2);
+    if (!clear(cache->k_q, code_bytes) || !clear(cache->v_q, code_bytes)) return KVC_ECUDA;
+    if (d.type == KVC_Q8_0) {
+        const size_t scale_bytes = (size_t)(d.head_dim / 32) * 2;
+        if (!clear(cache->k_s, scale_bytes) || !clear(cache->v_s, scale_bytes)) return KVC_ECUDA;
+    }
+    return KVC_OK;
+}
+
 const char *kvc_strerror(int status) {
     switch (status) {
         case KVC_OK: return "ok";

@@ -215,6 +215,20 @@ int kv_state_get(const kvc_cache *cache, int32_t n_tokens, void *dst, size_t dst
 int kv_state_set(kvc_cache *cache, const void *src, size_t src_bytes, int32_t *n_tokens_out,
                  kvc_stream_t stream);
 
+/* Rewind the cache to its first n_tokens positions: positions [n_tokens, n_ctx)
+ * of every layer, codes and scales, are cleared to zero bytes, as in a zeroed
+ * cache; earlier positions are untouched.  This is the undo of appends past
+ * n_tokens that a sequence needs when it drops speculative decode appends or
+ * trims excess state (mlxcel issue #2170 "refactor: one prefill planner and one
+ * pad-trim hook for CLI and server", sections "Current Behavior", the hook that
+ * unwinds decode appends exactly, and "Proposed Solution", item 2, one trim hook
+ * with an excess count).  Appends and attention address positions, so a cache
+ * rewound to n and appended again computes exactly what a cache that never held
+ * the dropped tokens computes.  Asynchronous on `stream` (strided memsets).
+ * Errors: KVC_EINVAL (invalid cache), KVC_ERANGE (n_tokens < 0 or > n_ctx),
+ * KVC_ECUDA. */
+int kv_cache_truncate(const kvc_cache *cache, int32_t n_tokens, kvc_stream_t stream);
+
 /* ---- diagnostics ------------------------------------------------------------- */
 
 /* A short static description of a status code. */

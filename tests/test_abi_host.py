@@ -117,6 +117,10 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     assert kvc.lib.kv_state_get(ctypes.byref(c), 65, k, 1 << 20, S) == kvc.KVC_ERANGE
     assert kvc.lib.kv_state_get(ctypes.byref(c), 10, k, 100, S) == kvc.KVC_ENOSPC
     assert kvc.lib.kv_state_set(ctypes.byref(c), k, 16, ctypes.byref(ctypes.c_int32()), S) == kvc.KVC_EFORMAT
+    assert kvc.lib.kv_cache_truncate(ctypes.byref(c), 65, S) == kvc.KVC_ERANGE
+    assert kvc.lib.kv_cache_truncate(ctypes.byref(c), -1, S) == kvc.KVC_ERANGE
+    assert kvc.lib.kv_cache_truncate(ctypes.byref(c), 64, S) == kvc.KVC_OK      # nothing past n_ctx: no-op
+    assert kvc.lib.kv_cache_truncate(None, 0, S) == kvc.KVC_EINVAL
     # unsupported head_dim for attention (append and state accept any multiple of 32)
     c96 = kvc.kvc_cache()
     d96 = kvc.make_desc(1, 64, 2, 96, "f16")
