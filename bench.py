@@ -422,7 +422,40 @@ def run_gpu(args, rank, world, local):
         "phases": phases, "roofline": roof, "e2e": e2e, "gpu_launches": req.launches_per_step() * K,
         "clocks": clk,
     }
+    if w.chunk_sweep:
+        line["chunk_sweep"] = chunk_sweep(kvc, torch, w, req, device, flush, max(3, K))
     return line
+
+
+def chunk_sweep(kvc, torch, w, req, device, flush, reps):
+    """Prefill time (appends + attention, L2 flushed before each) of the same prompt under each
+    chunking, and the fit T = b * chunks + a * tokens: b is this layer's fixed cost per chunk and a
+    its cost per token, the two numbers the pipeline chunk rule takes as b/a."""
+    import numpy as np
+    ms = {}
+    for chunk in w.chunk_sweep:
+        ww = si.Workload(**{**w.__dict__, "chunk": chunk, "n_decode": 0})
+        r = GpuRequest(kvc, ww, device, inputs=req.dev_in)
+        r.step()
+        ts = []
+        for _ in range(reps):
+            l2_flush(torch, flush)
+            ev = {"prefill": [], "attn": [], "decode": [], "state": []}
+            r.step(ev)
+            torch.cuda.synchronize()
+            ts.append(sum(x[0].elapsed_time(x[1]) for x in ev["prefill"]))
+        ms[len(r.chunks)] = (chunk or w.n_prompt, min(ts))
+        del r
+    k = np.array(sorted(ms), dtype=np.float64)
+    t = np.array([ms[int(x)][1] for x in k])
+    b, c = np.polyfit(k, t, 1)
+    a = c / w.n_prompt
+    out = {"prefill_ms": {str(ms[int(x)][0]): ms[int(x)][1] for x in k},
+           "fit": {"b_us_per_chunk": b * 1e3, "a_us_per_token": a * 1e3,
+                   "b_over_a_tokens": (b / a) if a > 0 else None}}
+    if a > 0 and b > 0:
+        out["pipeline_chunk"] = {str(s): kvc.pipeline_chunk(w.n_prompt, 8192, s, b / a) for s in (2, 4, 8)}
+    return out
 
 
 # --------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
