@@ -61,6 +61,7 @@ def _load():
         "kvc_device_status": (ctypes.c_int, [P(I32)]),
         "kvc_pipeline_chunk": (ctypes.c_int, [I32, I32, I32, ctypes.c_double, P(I32)]),
         "kv_cache_truncate": (ctypes.c_int, [P(kvc_cache), I32, VP]),
+        "decode_attn_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, I32, I32, VP, VP, SZ, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -221,6 +222,29 @@ def decode_attn(cache, layer, pos, q, out=None, scratch=None, stream=None):
     st = _lib().decode_attn(ctypes.byref(cache.c), layer, pos, _ptr(q), DTYPES[q.dtype], n_head_q, _ptr(out),
                          _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream, q.device))
     _check(st, "decode_attn")
+    return out
+
+
+def decode_attn_batch(caches, layer, pos, q, out=None, scratch=None, stream=None):
+    """Decode one token for each of len(caches) sequences in one call: q [n_seq][n_head_q][head_dim]
+    (CUDA), pos a list of positions; returns out [n_seq][n_head_q][head_dim] float32."""
+    n = len(caches)
+    if n != len(pos) or q.dim() != 3 or q.shape[0] != n:
+        raise ValueError("one position and one query row block per sequence")
+    _need(q, "q")
+    c0 = caches[0]
+    n_head_q = q.shape[1]
+    if out is None:
+        out = torch.empty(n, n_head_q, c0.head_dim, dtype=torch.float32, device=c0.device)
+    _need(out, "out", torch.float32)
+    if scratch is None:
+        scratch = torch.empty(n * c0.scratch_bytes(n_head_q), dtype=torch.uint8, device=c0.device)
+    _need(scratch, "scratch")
+    arr = (kvc_cache * n)(*[c.c for c in caches])
+    ps = (ctypes.c_int32 * n)(*[int(p) for p in pos])
+    st = _lib().decode_attn_batch(arr, n, layer, ps, _ptr(q), DTYPES[q.dtype], n_head_q, _ptr(out), _ptr(scratch),
+                               scratch.numel() * scratch.element_size(), _stream(stream, c0.device))
+    _check(st, "decode_attn_batch")
     return out
 
 

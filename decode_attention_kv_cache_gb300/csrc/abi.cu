@@ -153,6 +153,30 @@ int decode_attn_noalloc(const kvc_cache *cache, int32_t layer, int32_t pos, cons
     return launch_decode_noalloc(*cache, layer, pos, q, dtype, n_head_q, out, (cudaStream_t)stream);
 }
 
+int decode_attn_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *q,
+                      int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
+                      kvc_stream_t stream) {
+    if (!caches || !pos || n_seq < 1 || n_seq > decode_max_batch() || !dtype_ok(dtype)) return KVC_EINVAL;
+    const kvc_desc &d = caches[0].d;
+    for (int i = 0; i < n_seq; ++i) {
+        const kvc_desc &e = caches[i].d;
+        if (!cache_ok(&caches[i]) || e.n_layer != d.n_layer || e.n_ctx != d.n_ctx || e.n_head_kv != d.n_head_kv ||
+            e.head_dim != d.head_dim || e.type != d.type)
+            return KVC_EINVAL;
+    }
+    if (d.head_dim != 64 && d.head_dim != 128) return KVC_EINVAL;
+    if (n_head_q <= 0 || n_head_q % d.n_head_kv || n_head_q / d.n_head_kv > 16) return KVC_EINVAL;
+    if (layer < 0 || layer >= d.n_layer) return KVC_ERANGE;
+    for (int i = 0; i < n_seq; ++i)
+        if (pos[i] < 0 || pos[i] >= d.n_ctx) return KVC_ERANGE;
+    if (!q || !out || !scratch || !aligned16(q) || !aligned16(out) || !aligned16(scratch)) return KVC_EINVAL;
+    size_t need = 0;
+    kvc_scratch_bytes(&d, n_head_q, &need);
+    if (scratch_bytes / (size_t)n_seq < need) return KVC_ENOSPC;
+    return launch_decode_batch(caches, n_seq, layer, pos, q, dtype, n_head_q, out, static_cast<float *>(scratch),
+                               need, (cudaStream_t)stream);
+}
+
 int kv_state_get(const kvc_cache *cache, int32_t n_tokens, void *dst, size_t dst_bytes, kvc_stream_t stream) {
     if (!cache_ok(cache) || !dst || !aligned16(dst) || n_tokens < 0) return KVC_EINVAL;
     if (n_tokens > cache->d.n_ctx) return KVC_ERANGE;

@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "kvc_internal.h"
@@ -122,6 +123,22 @@ struct DecodeArgs {
     Geom g;
     int layer, n_keys, group, split_len, n_split, n_head_kv;
     float scale_log2;
+};
+
+// Several sequences decoded by one launch: each has its own cache (and so its own tensor maps),
+// position, query, scratch and output.  Grid z (or y for the combine pass) is the sequence.
+constexpr int MAX_BATCH = 8;
+template <int NS>
+struct TcBatch {
+    CUtensorMap tk[NS];
+    CUtensorMap tv[NS];
+    DecodeArgs a[NS];
+};
+template <int NS>
+struct CombineBatch {
+    const float *part[NS];
+    float *out[NS];
+    int n_split[NS];
 };
 
 // One consumer warp's fragments of a 16-key group.
@@ -487,9 +504,12 @@ __global__ void __maxnreg__(200)
 // memory; the denominators are then added in split order by one thread (from
 // shared memory), and each thread sums its value over the splits in split order
 // (independent loads, unrolled), so the result is deterministic.
-template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ part, int n_split,
-                                                           int group, int n_head_kv, float *__restrict__ out) {
+template <int D, int NS>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS> cb, int group, int n_head_kv) {
+    const int seq = NS == 1 ? 0 : (int)blockIdx.y;
+    const float *__restrict__ part = cb.part[seq];
+    float *__restrict__ out = cb.out[seq];
+    const int n_split = cb.n_split[seq];
     __shared__ float s_w[MAX_SPLIT], s_wl[MAX_SPLIT];
     __shared__ float s_red[D / 32];
     __shared__ float s_M, s_L;
@@ -635,12 +655,16 @@ __device__ __forceinline__ void dequant4(uint32_t w, __half2 d2, uint32_t &lo, u
 }
 
 // GM: heads the softmax loops cover (8 when the group has at most 8 query heads, else 16)
-template <bool Q8, int DT, int GM>
+// NS: sequences of a batch the parameters hold (1, or MAX_BATCH for a batched call; grid z = sequence)
+template <bool Q8, int DT, int GM, int NS>
 __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ TcBatch<NS> b) {
     using L = TCfg<Q8>;
     constexpr int D = 128;
+    const int seq = NS == 1 ? 0 : (int)blockIdx.z;
+    const DecodeArgs &a = b.a[seq];
+    const CUtensorMap *tm_k = &b.tk[seq], *tm_v = &b.tv[seq];
+    if ((int)blockIdx.x >= a.n_split) return;   // a batch's shorter sequences use fewer splits
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -680,8 +704,8 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
             }
         }
         fence_mbar_init();
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(tm_k);
+        tma_prefetch_desc(tm_v);
     }
     if (warp == 1) {
         tmem_alloc(s_tmem, TC_COLS);
@@ -706,21 +730,21 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
                     if (k >= L::NR && !mbar_wait(&bars[T_REMPTY + rs], ((k / L::NR) - 1) & 1, s_abort)) break;
                     uint8_t *dst = sm + L::OFF_RAW + rs * L::RAWT;
                     mbar_arrive_expect_tx(&bars[T_RFULL + rs], L::RAWT);
-                    tma_load_3d(dst, &tm_k, &bars[T_RFULL + rs], 0, j, hkv);
-                    tma_load_3d(dst + TK * D, &tm_v, &bars[T_RFULL + rs], 0, j, hkv);
+                    tma_load_3d(dst, tm_k, &bars[T_RFULL + rs], 0, j, hkv);
+                    tma_load_3d(dst + TK * D, tm_v, &bars[T_RFULL + rs], 0, j, hkv);
                     ++kn;
                 } else {
                     const int ks = k % L::NK, vs = k % L::NV;
                     if (k >= L::NK && !mbar_wait(&bars[T_KEMPTY + ks], ((k / L::NK) - 1) & 1, s_abort)) break;
                     mbar_arrive_expect_tx(&bars[T_KFULL + ks], L::OPT);
                     for (int dh = 0; dh < 2; ++dh)
-                        tma_load_3d(sm + L::OFF_K + ks * L::OPT + dh * TK * 128, &tm_k, &bars[T_KFULL + ks], dh * 64, j,
+                        tma_load_3d(sm + L::OFF_K + ks * L::OPT + dh * TK * 128, tm_k, &bars[T_KFULL + ks], dh * 64, j,
                                     hkv);
                     ++kn;
                     if (k >= L::NV && !mbar_wait(&bars[T_VEMPTY + vs], ((k / L::NV) - 1) & 1, s_abort)) break;
                     mbar_arrive_expect_tx(&bars[T_VFULL + vs], L::OPT);
                     for (int dh = 0; dh < 2; ++dh)
-                        tma_load_3d(sm + L::OFF_V + vs * L::OPT + dh * TK * 128, &tm_v, &bars[T_VFULL + vs], dh * 64, j,
+                        tma_load_3d(sm + L::OFF_V + vs * L::OPT + dh * TK * 128, tm_v, &bars[T_VFULL + vs], dh * 64, j,
                                     hkv);
                     ++vn;
                 }
@@ -1051,60 +1075,79 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
     }
 }
 
-template <bool Q8, int DT>
-int launch_tc(const kvc_cache &c, const DecodeArgs &a0, int n_head_q, float *out, float *scratch, cudaStream_t s) {
+// The tensor-core split pass and the combine, one launch each, over n_seq sequences (NS = 1, or
+// MAX_BATCH for a batched call).  Sequence i: cache caches[i], arguments a0[i] (its q and its scratch
+// as part), output outs[i].  The sequences share the SMs evenly: one wave over (split, kv head,
+// sequence), whole tiles per split.
+template <bool Q8, int DT, int NS>
+int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_head_q, float *const *outs,
+              cudaStream_t s) {
     using L = TCfg<Q8>;
     constexpr int D = 128;
-    DecodeArgs a = a0;
-    // one wave, one CTA per SM over (split, kv head), whole tiles per split
-    const int target = (L::CTAS * sm_count()) / a.n_head_kv;
-    int n_split = (a.n_keys + TK - 1) / TK;
-    if (n_split > target) n_split = target;
-    if (n_split > MAX_SPLIT) n_split = MAX_SPLIT;
-    if (n_split < 1) n_split = 1;
-    int len = (a.n_keys + n_split - 1) / n_split;
-    len = (len + TK - 1) / TK * TK;
-    n_split = (a.n_keys + len - 1) / len;
-    a.split_len = len;
-    a.n_split = n_split;
-    CUtensorMap tk, tv;
-    const Geom &g = a.g;
-    const int eb = Q8 ? 1 : 2;
-    const uint8_t *kb = static_cast<const uint8_t *>(c.k_q), *vb = static_cast<const uint8_t *>(c.v_q);
-    const CUtensorMapDataType dt = Q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const uint32_t box0 = 128 / eb;   // 128-byte rows: all 128 codes (q8_0) or 64 halves (f16)
-    if (!make_map_3d(&tk, dt, kb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv, eb * g.c_tok,
-                     eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_3d(&tv, dt, vb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv, eb * g.c_tok,
-                     eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B))
-        return KVC_ECUDA;
-    auto kern = a.group <= 8 ? decode_tc_kernel<Q8, DT, 8> : decode_tc_kernel<Q8, DT, 16>;
+    TcBatch<NS> b;
+    CombineBatch<NS> cb;
+    memset(&b, 0, sizeof(b));
+    memset(&cb, 0, sizeof(cb));
+    int target = (L::CTAS * sm_count()) / (a0[0].n_head_kv * n_seq);
+    if (target < 1) target = 1;
+    int max_split = 1;
+    for (int i = 0; i < n_seq; ++i) {
+        DecodeArgs a = a0[i];
+        int n_split = (a.n_keys + TK - 1) / TK;
+        if (n_split > target) n_split = target;
+        if (n_split > MAX_SPLIT) n_split = MAX_SPLIT;
+        if (n_split < 1) n_split = 1;
+        int len = (a.n_keys + n_split - 1) / n_split;
+        len = (len + TK - 1) / TK * TK;
+        n_split = (a.n_keys + len - 1) / len;
+        a.split_len = len;
+        a.n_split = n_split;
+        const kvc_cache &c = caches[i];
+        const Geom &g = a.g;
+        const int eb = Q8 ? 1 : 2;
+        const uint8_t *kb = static_cast<const uint8_t *>(c.k_q), *vb = static_cast<const uint8_t *>(c.v_q);
+        const CUtensorMapDataType dt = Q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const uint32_t box0 = 128 / eb;   // 128-byte rows: all 128 codes (q8_0) or 64 halves (f16)
+        if (!make_map_3d(&b.tk[i], dt, kb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv,
+                         eb * g.c_tok, eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map_3d(&b.tv[i], dt, vb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv,
+                         eb * g.c_tok, eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+            return KVC_ECUDA;
+        b.a[i] = a;
+        cb.part[i] = a.part;
+        cb.out[i] = outs[i];
+        cb.n_split[i] = n_split;
+        if (n_split > max_split) max_split = n_split;
+    }
+    const int group = a0[0].group, n_head_kv = a0[0].n_head_kv;
+    auto kern = group <= 8 ? decode_tc_kernel<Q8, DT, 8, NS> : decode_tc_kernel<Q8, DT, 16, NS>;
     static bool attr_set[2] = {false, false};  // per instantiation
-    if (!attr_set[a.group <= 8]) {
+    if (!attr_set[group <= 8]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
             return KVC_ECUDA;
-        attr_set[a.group <= 8] = true;
+        attr_set[group <= 8] = true;
     }
+    // both passes may start while the previous kernel of the stream finishes; each waits for it on
+    // the device before reading what it wrote
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_split, a.n_head_kv);
+    cfg.gridDim = dim3(max_split, n_head_kv, n_seq);
     cfg.blockDim = dim3(L::THREADS);
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess) return KVC_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, b) != cudaSuccess) return KVC_ECUDA;
     cudaLaunchConfig_t cfg2 = {};
-    cfg2.gridDim = dim3(n_head_q);
+    cfg2.gridDim = dim3(n_head_q, n_seq);
     cfg2.blockDim = dim3(D);
     cfg2.dynamicSmemBytes = 0;
     cfg2.stream = s;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg2, decode_combine_kernel<D>, (const float *)scratch, n_split, a.group, a.n_head_kv,
-                           out) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg2, decode_combine_kernel<D, NS>, cb, group, n_head_kv) != cudaSuccess)
         return KVC_ECUDA;
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
@@ -1125,7 +1168,7 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
     a.group = n_head_q / c.d.n_head_kv;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
     if constexpr (D == 128) {
-        return launch_tc<Q8, DT>(c, a, n_head_q, out, scratch, s);
+        return launch_tc<Q8, DT, 1>(&c, &a, 1, n_head_q, &out, s);
     } else {
     // one wave: CTAS_PER_SM CTAs per SM over (split, kv head), whole stages per split
     const int target = (CTAS_PER_SM * sm_count()) / a.n_head_kv;
@@ -1178,8 +1221,11 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
     cfg2.stream = s;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg2, decode_combine_kernel<D>, (const float *)scratch, n_split, a.group,
-                           a.n_head_kv, out) != cudaSuccess)
+    CombineBatch<1> cb;
+    cb.part[0] = scratch;
+    cb.out[0] = out;
+    cb.n_split[0] = n_split;
+    if (cudaLaunchKernelEx(&cfg2, decode_combine_kernel<D, 1>, cb, a.group, a.n_head_kv) != cudaSuccess)
         return KVC_ECUDA;
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
     }
@@ -1246,6 +1292,65 @@ int launch_decode_noalloc(const kvc_cache &c, int layer, int pos, const void *q,
 }
 
 int decode_max_split() { return MAX_SPLIT; }
+
+int decode_max_batch() { return MAX_BATCH; }
+
+namespace {
+
+template <bool Q8, int DT>
+int launch_batch_t(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, int n_head_q,
+                   float *out, float *scratch, size_t seq_scratch_floats, cudaStream_t s) {
+    constexpr int D = 128;
+    DecodeArgs a[MAX_BATCH];
+    float *outs[MAX_BATCH];
+    const size_t q_bytes = (size_t)n_head_q * D * dtype_bytes(DT);
+    for (int i = 0; i < n_seq; ++i) {
+        const kvc_cache &c = caches[i];
+        a[i].q = static_cast<const uint8_t *>(q) + i * q_bytes;
+        a[i].ks = static_cast<const uint16_t *>(c.k_s);
+        a[i].vs = static_cast<const uint16_t *>(c.v_s);
+        a[i].part = scratch + i * seq_scratch_floats;
+        a[i].g = geom_of(c.d);
+        a[i].layer = layer;
+        a[i].n_keys = pos[i] + 1;
+        a[i].n_head_kv = c.d.n_head_kv;
+        a[i].group = n_head_q / c.d.n_head_kv;
+        a[i].split_len = a[i].n_split = 0;
+        a[i].scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
+        outs[i] = out + (size_t)i * n_head_q * D;
+    }
+    return launch_tc<Q8, DT, MAX_BATCH>(caches, a, n_seq, n_head_q, outs, s);
+}
+
+}  // namespace
+
+int launch_decode_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, int dtype,
+                        int n_head_q, float *out, float *scratch, size_t seq_scratch_bytes, cudaStream_t s) {
+    const kvc_desc &d = caches[0].d;
+    const size_t seq_floats = seq_scratch_bytes / sizeof(float);
+    if (n_seq == 1 || d.head_dim != 128) {
+        // one sequence, or head_dim 64 (its split pass takes one cache per launch): a launch pair per sequence
+        const size_t q_bytes = (size_t)n_head_q * d.head_dim * dtype_bytes(dtype);
+        for (int i = 0; i < n_seq; ++i) {
+            const int rc = launch_decode(caches[i], layer, pos[i], static_cast<const uint8_t *>(q) + i * q_bytes, dtype,
+                                         n_head_q, out + (size_t)i * n_head_q * d.head_dim, scratch + i * seq_floats, s);
+            if (rc != KVC_OK) return rc;
+        }
+        return KVC_OK;
+    }
+    const bool q8 = d.type == KVC_Q8_0;
+    switch (dtype) {
+        case KVC_IN_F32:
+            return q8 ? launch_batch_t<true, KVC_IN_F32>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s)
+                      : launch_batch_t<false, KVC_IN_F32>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s);
+        case KVC_IN_BF16:
+            return q8 ? launch_batch_t<true, KVC_IN_BF16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s)
+                      : launch_batch_t<false, KVC_IN_BF16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s);
+        default:
+            return q8 ? launch_batch_t<true, KVC_IN_F16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s)
+                      : launch_batch_t<false, KVC_IN_F16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s);
+    }
+}
 
 int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                   float *out, float *scratch, cudaStream_t s) {

@@ -49,6 +49,9 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
 int decode_max_split();
 int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                   float *out, float *scratch, cudaStream_t s);
+int decode_max_batch();
+int launch_decode_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, int dtype,
+                        int n_head_q, float *out, float *scratch, size_t seq_scratch_bytes, cudaStream_t s);
 size_t decode_noalloc_capacity();
 int launch_decode_noalloc(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                           float *out, cudaStream_t s);

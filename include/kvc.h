@@ -177,6 +177,31 @@ int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *
                 int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
                 kvc_stream_t stream);
 
+/* Decode attention for n_seq sequences in one call (1 <= n_seq <= 8): sequence i
+ * attends with its query at position pos[i] over positions [0, pos[i]] of its
+ * own cache caches[i], exactly as decode_attn would.  This is decoding several
+ * sequences together, one token each per step, as llama-batched-bench's npl
+ * parallel sequences do (llama.cpp PR #58 "completion : allow the prompt to be
+ * processed under its own split mode", section "Why -np 1", the npl
+ * table; llama.cpp PR #59 "llama : switch the split mode of a live context",
+ * section "Several sequences at once").  caches: host array of n_seq caches
+ * whose descriptors agree in n_layer, n_ctx, n_head_kv, head_dim and type (the
+ * layouts may differ).  pos: host array of n_seq positions.  q: device,
+ * [n_seq][n_head_q][head_dim] in `dtype`; out: device, [n_seq][n_head_q]
+ * [head_dim] float32.  scratch: device, at least n_seq * kvc_scratch_bytes(desc,
+ * n_head_q) bytes, sequence i using the i-th slice.  With head_dim 128 the split
+ * pass of all sequences is one launch over (split, kv head, sequence), the SMs
+ * shared evenly among the sequences, followed by one combine launch; with
+ * head_dim 64 (or n_seq == 1) each sequence is its own launch pair.  A batched
+ * call may choose other split boundaries than decode_attn for the same
+ * sequence, so results agree within rounding, not bit for bit.  Errors as
+ * decode_attn; KVC_EINVAL also for n_seq outside [1, 8] or caches that disagree,
+ * KVC_ERANGE for any pos[i] out of range, KVC_ENOSPC for a scratch below n_seq
+ * slices. */
+int decode_attn_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *q,
+                      int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
+                      kvc_stream_t stream);
+
 /* decode_attn without a scratch argument, for callers that cannot allocate
  * device memory themselves (code hosted by an engine that owns every device
  * allocation, or a path where cudaMalloc's implicit synchronisation is not

@@ -121,6 +121,25 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     assert kvc.lib.kv_cache_truncate(ctypes.byref(c), -1, S) == kvc.KVC_ERANGE
     assert kvc.lib.kv_cache_truncate(ctypes.byref(c), 64, S) == kvc.KVC_OK      # nothing past n_ctx: no-op
     assert kvc.lib.kv_cache_truncate(None, 0, S) == kvc.KVC_EINVAL
+    # batched decode: the checks of decode_attn per sequence, plus the batch's own
+    big = 1 << 30
+    d128 = kvc.make_desc(2, 64, 2, 128, "q8_0")
+    cb = kvc.kvc_cache()
+    p4 = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(4)]
+    assert kvc.lib.kvc_cache_init(ctypes.byref(cb), ctypes.byref(d128), *p4) == kvc.KVC_OK
+    nine = (kvc.kvc_cache * 9)(*([cb] * 9))
+    p9 = (ctypes.c_int32 * 9)(*([5] * 9))
+    assert kvc.lib.decode_attn_batch(nine, 9, 0, p9, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL     # n_seq > 8
+    assert kvc.lib.decode_attn_batch(nine, 0, 0, p9, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL     # n_seq < 1
+    bad = (ctypes.c_int32 * 2)(5, 64)
+    assert kvc.lib.decode_attn_batch(nine, 2, 0, bad, k, 1, 4, k, k, big, S) == kvc.KVC_ERANGE    # pos[1] = n_ctx
+    assert kvc.lib.decode_attn_batch(nine, 2, 2, p9, k, 1, 4, k, k, big, S) == kvc.KVC_ERANGE     # layer
+    assert kvc.lib.decode_attn_batch(nine, 2, 0, p9, k, 1, 3, k, k, big, S) == kvc.KVC_EINVAL     # n_head_q
+    one = ctypes.c_size_t()
+    assert kvc.lib.kvc_scratch_bytes(ctypes.byref(d128), 4, ctypes.byref(one)) == kvc.KVC_OK
+    assert kvc.lib.decode_attn_batch(nine, 3, 0, p9, k, 1, 4, k, k, 3 * one.value - 16, S) == kvc.KVC_ENOSPC
+    mixed = (kvc.kvc_cache * 2)(cb, c)                                                            # head_dim 128 and 64
+    assert kvc.lib.decode_attn_batch(mixed, 2, 0, p9, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL
     # unsupported head_dim for attention (append and state accept any multiple of 32)
     c96 = kvc.kvc_cache()
     d96 = kvc.make_desc(1, 64, 2, 96, "f16")
