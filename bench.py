@@ -368,22 +368,7 @@ def run_gpu(args, rank, world, local):
     # ---- end to end: host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        for _ in range(2):
-            req.h2d(); req.step(); req.d2h()
-        torch.cuda.synchronize()
-        dist_barrier(world)
-        e_ms = []
-        for _ in range(K):
-            l2_flush(torch, flush)
-            a = torch.cuda.Event(enable_timing=True); a.record()
-            req.h2d(); req.step(); req.d2h()
-            b = torch.cuda.Event(enable_timing=True); b.record()
-            b.synchronize()
-            e_ms.append(a.elapsed_time(b))
-        e_total = dist_max(sum(e_ms), world)
-        h2d, d2h = req.io_bytes()
-        e2e = {"value": tokens * world * K / (e_total / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_total / K}
+        e2e = end_to_end(kvc, torch, w, req, device, rank, world, K, flush)
     assert kvc.kvc_device_status() == 0
 
     peaks, peak_src = load_peaks()
@@ -424,7 +409,132 @@ def run_gpu(args, rank, world, local):
     }
     if w.chunk_sweep:
         line["chunk_sweep"] = chunk_sweep(kvc, torch, w, req, device, flush, max(3, K))
+    if args.npl:
+        line["batched_decode"] = batched_decode(kvc, torch, w, device, [int(x) for x in args.npl.split(",")])
     return line
+
+
+def batched_decode(kvc, torch, w, device, npls, n_past=2048, n_gen=128):
+    """Generation with npl sequences decoded together (decode_attn_batch), the setup of a batched
+    bench: each sequence holds an n_past-token prompt of this workload's shape in its own cache, then
+    n_gen steps each append one token per sequence (kv_cache_append_batch) and decode all sequences in
+    one call (decode_attn_batch), in a CUDA graph.
+    Reports generated tokens/s over all sequences and the algorithmic cache bytes read per second."""
+    res = {}
+    bt = cache_bytes_per_token(w)
+    n_tok = n_past + n_gen
+    seqs = []
+    for i in range(max(npls)):
+        ws = si.Workload(**{**w.__dict__, "name": "npl%d" % i, "n_layer": 1, "n_prompt": n_past, "n_decode": n_gen,
+                            "n_ctx": n_tok, "seed": w.seed + 100 + i})
+        q, k, v = si.layer_qkv_device(ws, 0, device, n_rows=n_tok)
+        g = kvc.KVCache(1, n_tok, w.n_head_kv, w.head_dim, w.cache, "head_major", device)
+        kvc.kv_cache_append(g, 0, 0, k[:n_past], v[:n_past])
+        seqs.append((g, q, k, v))
+    for npl in npls:
+        caches = [s[0] for s in seqs[:npl]]
+        qs = torch.stack([s[1][n_past:n_tok] for s in seqs[:npl]], dim=1)   # [step][seq][H_q][D]
+        out = torch.empty(n_gen, npl, w.n_head_q, w.head_dim, device=device)
+        scratch = torch.empty(npl * caches[0].scratch_bytes(w.n_head_q), dtype=torch.uint8, device=device)
+
+        ks = torch.stack([s[2][n_past:n_tok] for s in seqs[:npl]], dim=1)   # [step][seq][H_kv][D]
+        vs = torch.stack([s[3][n_past:n_tok] for s in seqs[:npl]], dim=1)
+
+        def gen():
+            for t in range(n_gen):
+                pos = [n_past + t] * npl
+                kvc.kv_cache_append_batch(caches, 0, pos, ks[t], vs[t])
+                kvc.decode_attn_batch(caches, 0, pos, qs[t], out=out[t], scratch=scratch)
+        s = torch.cuda.Stream(device)
+        with torch.cuda.stream(s):
+            gen()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                gen()
+        graph.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+        a.record(); graph.replay(); b.record(); b.synchronize()
+        ms = a.elapsed_time(b)
+        cache_bytes = npl * sum((n_past + t + 1) * bt for t in range(n_gen))
+        res[str(npl)] = {"tg_tok_s": npl * n_gen / (ms / 1e3), "us_per_step": ms * 1e3 / n_gen,
+                         "algorithmic_GB_s": cache_bytes / (ms / 1e3) / 1e9}
+        del graph
+    res["setup"] = "npl sequences, %d-token prompts, %d generated tokens each, kv_cache_append_batch + " \
+                   "decode_attn_batch per step in a CUDA graph" % (n_past, n_gen)
+    return res
+
+
+def end_to_end(kvc, torch, w, req, device, rank, world, K, flush):
+    """The same request through the public API with host buffers: every step copies its inputs in from
+    pinned host memory and its outputs (prefill and decode attention, the state) back out, inside the
+    timed region.  For a one-layer request two requests alternate, so that step i's input copy and
+    step i-1's output copy run on their own streams while the other request computes (as a serving
+    loop overlaps transfers with compute); the inputs copied in each step are larger than L2.  A
+    layer stack (tens of GB of inputs) runs its steps one after another, L2 flushed before each."""
+    h2d, d2h = req.io_bytes()
+    tokens = (w.n_prompt + w.n_decode) * w.n_layer
+    if w.n_layer > 1:
+        for _ in range(2):
+            req.h2d(); req.step(); req.d2h()
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        e_ms = []
+        for _ in range(K):
+            l2_flush(torch, flush)
+            a = torch.cuda.Event(enable_timing=True); a.record()
+            req.h2d(); req.step(); req.d2h()
+            b = torch.cuda.Event(enable_timing=True); b.record()
+            b.synchronize()
+            e_ms.append(a.elapsed_time(b))
+        e_total = dist_max(sum(e_ms), world)
+        return {"value": tokens * world * K / (e_total / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e_total / K, "overlap": "none (steps in series)"}
+    reqs = [req, GpuRequest(kvc, w, device, seed_offset=rank)]
+    if w.n_decode:
+        reqs[1].capture()
+    main = torch.cuda.current_stream(device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    E = torch.cuda.Event
+
+    def run(n):
+        done, out_done = [], []
+        start = E(enable_timing=True)
+        start.record(main)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(n):
+            r = reqs[i % 2]
+            if i >= 2:
+                s_in.wait_event(done[i - 2])          # request r's previous step no longer reads its inputs
+            with torch.cuda.stream(s_in):
+                r.h2d()
+            inp = E(); inp.record(s_in)
+            main.wait_event(inp)
+            if i >= 2:
+                main.wait_event(out_done[i - 2])      # request r's previous outputs are on the host
+            r.step()
+            d = E(); d.record(main); done.append(d)
+            s_out.wait_event(d)
+            with torch.cuda.stream(s_out):
+                r.d2h()
+            o = E(); o.record(s_out); out_done.append(o)
+        main.wait_event(out_done[-1])
+        main.wait_event(done[-1])
+        stop = E(enable_timing=True)
+        stop.record(main)
+        stop.synchronize()
+        return start.elapsed_time(stop)
+
+    run(2)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    e_total = dist_max(run(K), world)
+    return {"value": tokens * world * K / (e_total / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e_total / K,
+            "overlap": "two requests alternate: copies in and out on their own streams beside compute",
+            "l2": "each step copies in %d bytes of inputs (> L2)" % h2d}
 
 
 def chunk_sweep(kvc, torch, w, req, device, flush, reps):
@@ -579,6 +689,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--npl", default="", help="also time batched decode for these sequence counts, e.g. 1,2,4,8")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
 

@@ -62,6 +62,7 @@ def _load():
         "kvc_pipeline_chunk": (ctypes.c_int, [I32, I32, I32, ctypes.c_double, P(I32)]),
         "kv_cache_truncate": (ctypes.c_int, [P(kvc_cache), I32, VP]),
         "decode_attn_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, I32, I32, VP, VP, SZ, VP]),
+        "kv_cache_append_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, VP, I32, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -223,6 +224,19 @@ def decode_attn(cache, layer, pos, q, out=None, scratch=None, stream=None):
                          _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream, q.device))
     _check(st, "decode_attn")
     return out
+
+
+def kv_cache_append_batch(caches, layer, pos, k, v, stream=None):
+    """Append one token per sequence: row i of k and v ([n_seq][H_kv][D], CUDA) to caches[i] at pos[i]."""
+    n = len(caches)
+    if n != len(pos) or k.shape[0] != n or v.shape != k.shape or k.dtype != v.dtype:
+        raise ValueError("one position and one K/V row block per sequence")
+    _need(k, "k"); _need(v, "v")
+    arr = (kvc_cache * n)(*[c.c for c in caches])
+    ps = (ctypes.c_int32 * n)(*[int(p) for p in pos])
+    st = _lib().kv_cache_append_batch(arr, n, layer, ps, _ptr(k), _ptr(v), DTYPES[k.dtype],
+                                   _stream(stream, caches[0].device))
+    _check(st, "kv_cache_append_batch")
 
 
 def decode_attn_batch(caches, layer, pos, q, out=None, scratch=None, stream=None):

@@ -101,6 +101,21 @@ int kv_cache_append(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t
     return launch_append(*cache, layer, pos0, n_tokens, k, v, dtype, (cudaStream_t)stream);
 }
 
+int kv_cache_append_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *k,
+                          const void *v, int32_t dtype, kvc_stream_t stream) {
+    if (!caches || !pos || n_seq < 1 || n_seq > append_max_batch() || !dtype_ok(dtype)) return KVC_EINVAL;
+    const kvc_desc &d = caches[0].d;
+    for (int i = 0; i < n_seq; ++i) {
+        const kvc_desc &e = caches[i].d;
+        if (!cache_ok(&caches[i]) || e.n_head_kv != d.n_head_kv || e.head_dim != d.head_dim || e.type != d.type)
+            return KVC_EINVAL;
+    }
+    for (int i = 0; i < n_seq; ++i)
+        if (layer < 0 || layer >= caches[i].d.n_layer || pos[i] < 0 || pos[i] >= caches[i].d.n_ctx) return KVC_ERANGE;
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return KVC_EINVAL;
+    return launch_append_batch(caches, n_seq, layer, pos, k, v, dtype, (cudaStream_t)stream);
+}
+
 int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t max_tokens, size_t *bytes) {
     if (!desc_ok(desc) || !bytes || n_head_q <= 0 || n_head_q % desc->n_head_kv) return KVC_EINVAL;
     if (max_tokens <= 0 || max_tokens > desc->n_ctx) return KVC_ERANGE;

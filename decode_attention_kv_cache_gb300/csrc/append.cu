@@ -25,6 +25,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
+
 #include "kvc_internal.h"
 #include "ptx.cuh"
 
@@ -55,11 +57,35 @@ __device__ __forceinline__ void load8(const void *base, int64_t idx, float (&x)[
     }
 }
 
+// Where input token t goes: one cache, token t at position pos0 + t ...
+struct OneCache {
+    void *kq, *vq;
+    uint16_t *ks, *vs;
+    Geom g;
+    int pos0;
+    __device__ __forceinline__ int64_t pos(int t) const { return (int64_t)pos0 + t; }
+    __device__ __forceinline__ const Geom &geom(int) const { return g; }
+    __device__ __forceinline__ void *codes(bool is_v, int) const { return is_v ? vq : kq; }
+    __device__ __forceinline__ uint16_t *scales(bool is_v, int) const { return is_v ? vs : ks; }
+};
+// ... or one token per sequence: token t into cache t at position pos[t]
+constexpr int MAX_SEQ = 8;
+struct PerSeqCaches {
+    void *kq[MAX_SEQ], *vq[MAX_SEQ];
+    uint16_t *ks[MAX_SEQ], *vs[MAX_SEQ];
+    Geom g[MAX_SEQ];
+    int p[MAX_SEQ];
+    __device__ __forceinline__ int64_t pos(int t) const { return p[t]; }
+    __device__ __forceinline__ const Geom &geom(int t) const { return g[t]; }
+    __device__ __forceinline__ void *codes(bool is_v, int t) const { return is_v ? vq[t] : kq[t]; }
+    __device__ __forceinline__ uint16_t *scales(bool is_v, int t) const { return is_v ? vs[t] : ks[t]; }
+};
+
 // f16 cache: grid.x covers units of 8 values of one tensor; grid.y selects K (0) or V (1).
-template <int DT>
+template <int DT, class DST>
 __global__ void __launch_bounds__(256) append_f16_kernel(
     const void *__restrict__ k, const void *__restrict__ v, int64_t n_units, int units_per_tok,
-    int units_per_head, void *kq, void *vq, Geom g, int layer, int pos0) {
+    int units_per_head, const DST dst_of, int layer) {
     // a kernel launched after this one as a programmatic dependent (the decode split pass) may be
     // scheduled now; it waits for this grid's completion before it reads the cache
     asm volatile("griddepcontrol.launch_dependents;");
@@ -72,12 +98,13 @@ __global__ void __launch_bounds__(256) append_f16_kernel(
     const int c = rem % units_per_head;  // which 8-value group along head_dim
     float x[8];
     load8<DT>(is_v ? v : k, u * 8, x);
-    const int64_t pos = (int64_t)pos0 + tok;
+    const int64_t pos = dst_of.pos(tok);
+    const Geom &g = dst_of.geom(tok);
     const int64_t code_off = layer * g.c_layer + pos * g.c_tok + head * g.c_head + (int64_t)c * 8;
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = ptx::pack_half2(x[2 * i], x[2 * i + 1]);
-    uint16_t *dst = static_cast<uint16_t *>(is_v ? vq : kq) + code_off;
+    uint16_t *dst = static_cast<uint16_t *>(dst_of.codes(is_v, tok)) + code_off;
     *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -105,10 +132,10 @@ __device__ __forceinline__ void chunk_values(const uint4 &u, float *x) {
 __device__ __forceinline__ int stage_slot(int c) { return c ^ ((c >> 3) & 7); }
 
 // q8_0 cache: one thread per 32-value block; grid.y selects K (0) or V (1).
-template <int DT>
+template <int DT, class DST>
 __global__ void __launch_bounds__(256) append_q8_kernel(
-    const void *__restrict__ k, const void *__restrict__ v, int64_t n_blocks, int nb, int H, void *kq,
-    uint16_t *ks, void *vq, uint16_t *vs, Geom g, int layer, int pos0) {
+    const void *__restrict__ k, const void *__restrict__ v, int64_t n_blocks, int nb, int H, const DST dst_of,
+    int layer) {
     asm volatile("griddepcontrol.launch_dependents;");
     constexpr int ESZ = DT == KVC_IN_F32 ? 4 : 2;
     constexpr int CPB = 2 * ESZ;                   // 16-byte input chunks per block
@@ -174,32 +201,45 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
             packed[w] = __byte_perm(__byte_perm(q[4 * w], q[4 * w + 1], 0x0040),
                                     __byte_perm(q[4 * w + 2], q[4 * w + 3], 0x0040), 0x5410);
     }
-    const int64_t pos = (int64_t)pos0 + tok;
-    int8_t *dst = static_cast<int8_t *>(is_v ? vq : kq) + layer * g.c_layer + pos * g.c_tok + head * g.c_head + b * 32;
+    const int64_t pos = dst_of.pos(tok);
+    const Geom &g = dst_of.geom(tok);
+    int8_t *dst = static_cast<int8_t *>(dst_of.codes(is_v, tok)) + layer * g.c_layer + pos * g.c_tok +
+                  head * g.c_head + b * 32;
     reinterpret_cast<uint4 *>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     reinterpret_cast<uint4 *>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    (is_v ? vs : ks)[layer * g.s_layer + pos * g.s_tok + head * g.s_head + b] = __half_as_ushort(__float2half_rn(d));
+    dst_of.scales(is_v, tok)[layer * g.s_layer + pos * g.s_tok + head * g.s_head + b] =
+        __half_as_ushort(__float2half_rn(d));
 }
 
-template <int DT>
-void launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *k, const void *v,
+// n tokens of k and v ([n][H_kv][head_dim]) to the destinations dst_of gives them; desc: their shape
+template <int DT, class DST>
+void launch_t(const kvc_desc &desc, const DST &dst_of, int layer, int n, const void *k, const void *v,
               cudaStream_t s) {
-    const Geom g = geom_of(c.d);
     const int threads = 256;
-    if (c.d.type == KVC_Q8_0) {
-        const int nb = c.d.head_dim / 32;
-        const int64_t n_blocks = (int64_t)n * c.d.n_head_kv * nb;
+    if (desc.type == KVC_Q8_0) {
+        const int nb = desc.head_dim / 32;
+        const int64_t n_blocks = (int64_t)n * desc.n_head_kv * nb;
         dim3 grid((unsigned)((n_blocks + threads - 1) / threads), 2);
-        append_q8_kernel<DT><<<grid, threads, 0, s>>>(k, v, n_blocks, nb, c.d.n_head_kv, c.k_q, (uint16_t *)c.k_s,
-                                                      c.v_q, (uint16_t *)c.v_s, g, layer, pos0);
+        append_q8_kernel<DT, DST><<<grid, threads, 0, s>>>(k, v, n_blocks, nb, desc.n_head_kv, dst_of, layer);
     } else {
-        const int units_per_head = c.d.head_dim / 8;
-        const int units_per_tok = units_per_head * c.d.n_head_kv;
+        const int units_per_head = desc.head_dim / 8;
+        const int units_per_tok = units_per_head * desc.n_head_kv;
         const int64_t n_units = (int64_t)n * units_per_tok;
         dim3 grid((unsigned)((n_units + threads - 1) / threads), 2);
-        append_f16_kernel<DT><<<grid, threads, 0, s>>>(k, v, n_units, units_per_tok, units_per_head, c.k_q, c.v_q, g,
-                                                       layer, pos0);
+        append_f16_kernel<DT, DST><<<grid, threads, 0, s>>>(k, v, n_units, units_per_tok, units_per_head, dst_of,
+                                                            layer);
     }
+}
+
+template <class DST>
+int launch_dtype(const kvc_desc &desc, const DST &dst_of, int layer, int n, const void *k, const void *v, int dtype,
+                 cudaStream_t s) {
+    switch (dtype) {
+        case KVC_IN_F32: launch_t<KVC_IN_F32>(desc, dst_of, layer, n, k, v, s); break;
+        case KVC_IN_BF16: launch_t<KVC_IN_BF16>(desc, dst_of, layer, n, k, v, s); break;
+        default: launch_t<KVC_IN_F16>(desc, dst_of, layer, n, k, v, s); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 
 }  // namespace
@@ -207,12 +247,31 @@ void launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *k, con
 int launch_append(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *k,
                   const void *v, int dtype, cudaStream_t s) {
     if (n_tokens == 0) return KVC_OK;
-    switch (dtype) {
-        case KVC_IN_F32: launch_t<KVC_IN_F32>(c, layer, pos0, n_tokens, k, v, s); break;
-        case KVC_IN_BF16: launch_t<KVC_IN_BF16>(c, layer, pos0, n_tokens, k, v, s); break;
-        default: launch_t<KVC_IN_F16>(c, layer, pos0, n_tokens, k, v, s); break;
+    OneCache d;
+    d.kq = c.k_q;
+    d.vq = c.v_q;
+    d.ks = static_cast<uint16_t *>(c.k_s);
+    d.vs = static_cast<uint16_t *>(c.v_s);
+    d.g = geom_of(c.d);
+    d.pos0 = pos0;
+    return launch_dtype(c.d, d, layer, n_tokens, k, v, dtype, s);
+}
+
+int append_max_batch() { return MAX_SEQ; }
+
+int launch_append_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *k, const void *v,
+                        int dtype, cudaStream_t s) {
+    PerSeqCaches d;
+    memset(&d, 0, sizeof(d));
+    for (int i = 0; i < n_seq; ++i) {
+        d.kq[i] = caches[i].k_q;
+        d.vq[i] = caches[i].v_q;
+        d.ks[i] = static_cast<uint16_t *>(caches[i].k_s);
+        d.vs[i] = static_cast<uint16_t *>(caches[i].v_s);
+        d.g[i] = geom_of(caches[i].d);
+        d.p[i] = pos[i];
     }
-    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
+    return launch_dtype(caches[0].d, d, layer, n_seq, k, v, dtype, s);
 }
 
 }  // namespace kvc

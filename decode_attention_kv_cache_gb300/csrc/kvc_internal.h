@@ -43,6 +43,9 @@ int sm_count();
 // Launchers: arguments are already validated; return KVC_OK or KVC_ECUDA.
 int launch_append(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *k,
                   const void *v, int dtype, cudaStream_t s);
+int append_max_batch();
+int launch_append_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *k, const void *v,
+                        int dtype, cudaStream_t s);
 size_t prefill_scratch_bytes(const kvc_desc &d, int n_head_q, int max_tokens);
 int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, int dtype,
                    int n_head_q, float *out, void *scratch, size_t scratch_bytes, cudaStream_t s);

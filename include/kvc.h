@@ -139,6 +139,17 @@ int kvc_pipeline_chunk(int32_t n_tokens, int32_t cap, int32_t stages, double b_o
 int kv_cache_append(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens,
                     const void *k, const void *v, int32_t dtype, kvc_stream_t stream);
 
+/* Append one token to each of n_seq caches (1 <= n_seq <= 8) in one launch:
+ * row i of k and v ([n_seq][n_head_kv][head_dim] in `dtype`) goes to position
+ * pos[i] of `layer` of caches[i], quantised exactly as kv_cache_append does.
+ * This is the append half of a decode step of several sequences together (see
+ * decode_attn_batch).  caches: host array whose descriptors agree in n_head_kv,
+ * head_dim and type; pos: host array.  Errors: KVC_EINVAL (null, dtype, n_seq
+ * outside [1, 8], caches that disagree), KVC_ERANGE (layer or any pos[i] outside
+ * its cache). */
+int kv_cache_append_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *k,
+                          const void *v, int32_t dtype, kvc_stream_t stream);
+
 /* Bytes of the scratch buffer prefill_chunk_attn needs for chunks of up to
  * max_tokens rows anywhere in this cache: the float32 partial results
  * (output row, running max, sum) of the key splits, at least 256 bytes.  The

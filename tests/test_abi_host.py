@@ -140,6 +140,13 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     assert kvc.lib.decode_attn_batch(nine, 3, 0, p9, k, 1, 4, k, k, 3 * one.value - 16, S) == kvc.KVC_ENOSPC
     mixed = (kvc.kvc_cache * 2)(cb, c)                                                            # head_dim 128 and 64
     assert kvc.lib.decode_attn_batch(mixed, 2, 0, p9, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL
+    # batched append
+    assert kvc.lib.kv_cache_append_batch(nine, 9, 0, p9, k, k, 1, S) == kvc.KVC_EINVAL           # n_seq > 8
+    assert kvc.lib.kv_cache_append_batch(nine, 2, 0, bad, k, k, 1, S) == kvc.KVC_ERANGE          # pos[1] = n_ctx
+    assert kvc.lib.kv_cache_append_batch(nine, 2, 2, p9, k, k, 1, S) == kvc.KVC_ERANGE           # layer
+    assert kvc.lib.kv_cache_append_batch(mixed, 2, 0, p9, k, k, 1, S) == kvc.KVC_EINVAL
+    assert kvc.lib.kv_cache_append_batch(nine, 2, 0, p9, None, k, 1, S) == kvc.KVC_EINVAL
+    assert kvc.lib.kv_cache_append_batch(nine, 2, 0, p9, k, k, 7, S) == kvc.KVC_EINVAL           # dtype
     # unsupported head_dim for attention (append and state accept any multiple of 32)
     c96 = kvc.kvc_cache()
     d96 = kvc.make_desc(1, 64, 2, 96, "f16")

@@ -80,3 +80,42 @@ def test_batch_in_a_cuda_graph_replays(kvc):
     gr.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("cache,dtype", [("q8_0", "bf16"), ("f16", "f32"), ("q8_0", "f16")])
+def test_batched_append_equals_one_append_per_sequence(kvc, cache, dtype):
+    n_seq, hkv, d = 6, 8, 128
+    pos = [0, 4199, 17, 2048, 777, 3000]
+    w = si.small_workload("bappend", 40, hkv, d, cache, dtype, n_prompt=n_seq, chunk=n_seq, n_decode=0, seed=77,
+                          n_ctx=N_CTX, k_outlier_frac=0.01)
+    _, k, v = si.layer_qkv(w, 0)
+    k, v = k.cuda(), v.cuda()
+    a = [kvc.KVCache(2, N_CTX, hkv, d, cache, "head_major" if i % 2 else "layer_major") for i in range(n_seq)]
+    b = [kvc.KVCache(2, N_CTX, hkv, d, cache, "head_major" if i % 2 else "layer_major") for i in range(n_seq)]
+    for x, y in zip(a, b):
+        for kv in (0, 1):
+            x.codes(kv).zero_(); y.codes(kv).zero_()
+            if cache == "q8_0":
+                x.scales(kv).zero_(); y.scales(kv).zero_()
+    kvc.kv_cache_append_batch(a, 1, pos, k, v)
+    for i in range(n_seq):
+        kvc.kv_cache_append(b[i], 1, pos[i], k[i:i + 1], v[i:i + 1])
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        for kv in (0, 1):
+            assert torch.equal(x.codes(kv), y.codes(kv))
+            if cache == "q8_0":
+                assert torch.equal(x.scales(kv), y.scales(kv))
+    # and the appended rows are the oracle's bytes
+    for i in range(n_seq):
+        o = OracleCache(1, N_CTX, hkv, d, cache)
+        o.append(0, pos[i], np32(k[i:i + 1].cpu()), np32(v[i:i + 1].cpu()))
+        img = o.device_image("head_major")
+        for kv in (0, 1):
+            got = a[i].codes(kv)
+            got = got[:, 1, pos[i]] if a[i].layout == "head_major" else got[1, pos[i]]
+            ref = img[2 * kv][:, 0, pos[i]]
+            if cache == "q8_0":
+                assert np.array_equal(got.cpu().numpy(), ref)
+            else:
+                assert np.array_equal(got.cpu().view(torch.int16).numpy(), ref.view(np.int16))
