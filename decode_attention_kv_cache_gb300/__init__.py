@@ -63,6 +63,8 @@ def _load():
         "kv_cache_truncate": (ctypes.c_int, [P(kvc_cache), I32, VP]),
         "decode_attn_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, I32, I32, VP, VP, SZ, VP]),
         "kv_cache_append_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, VP, I32, VP]),
+        "kv_state_get_heads": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, SZ, VP]),
+        "kv_state_set_heads": (ctypes.c_int, [P(kvc_cache), I32, VP, SZ, P(I32), VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -281,6 +283,30 @@ def kv_state_set(cache, src, stream=None):
     st = _lib().kv_state_set(ctypes.byref(cache.c), _ptr(src), src.numel() * src.element_size(), ctypes.byref(n),
                           _stream(stream, cache.device))
     _check(st, "kv_state_set")
+    return n.value
+
+
+def kv_state_get_heads(cache, head0, n_head_total, n_tokens, dst=None, stream=None):
+    """Write the part of the whole state (n_head_total kv heads) that `cache`, holding kv heads
+    [head0, head0 + cache.n_head_kv), owns, plus the header, into dst; returns dst."""
+    whole = make_desc(cache.n_layer, cache.n_ctx, n_head_total, cache.head_dim, cache.cache_type, cache.layout)
+    n = _lib().kv_state_size(ctypes.byref(whole), n_tokens)
+    if dst is None:
+        dst = torch.zeros(max(n, 16), dtype=torch.uint8, device=cache.device)
+    _need(dst, "dst")
+    st = _lib().kv_state_get_heads(ctypes.byref(cache.c), head0, n_head_total, n_tokens, _ptr(dst),
+                                dst.numel() * dst.element_size(), _stream(stream, cache.device))
+    _check(st, "kv_state_get_heads")
+    return dst[:n]
+
+
+def kv_state_set_heads(cache, head0, src, stream=None):
+    """Restore kv heads [head0, head0 + cache.n_head_kv) of a whole state into `cache`; returns n_tokens."""
+    _need(src, "src")
+    n = ctypes.c_int32(-1)
+    st = _lib().kv_state_set_heads(ctypes.byref(cache.c), head0, _ptr(src), src.numel() * src.element_size(),
+                                ctypes.byref(n), _stream(stream, cache.device))
+    _check(st, "kv_state_set_heads")
     return n.value
 
 

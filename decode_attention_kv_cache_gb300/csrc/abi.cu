@@ -220,6 +220,41 @@ int kv_state_set(kvc_cache *cache, const void *src, size_t src_bytes, int32_t *n
     return rc;
 }
 
+int kv_state_get_heads(const kvc_cache *cache, int32_t head0, int32_t n_head_total, int32_t n_tokens, void *dst,
+                       size_t dst_bytes, kvc_stream_t stream) {
+    if (!cache_ok(cache) || !dst || !aligned16(dst) || n_tokens < 0) return KVC_EINVAL;
+    if (head0 < 0 || n_head_total <= 0 || (int64_t)head0 + cache->d.n_head_kv > n_head_total) return KVC_EINVAL;
+    if (n_tokens > cache->d.n_ctx) return KVC_ERANGE;
+    kvc_desc whole = cache->d;
+    whole.n_head_kv = n_head_total;
+    if (dst_bytes < kv_state_size(&whole, n_tokens)) return KVC_ENOSPC;
+    return launch_state_pack_heads(*cache, head0, n_head_total, n_tokens, static_cast<uint8_t *>(dst),
+                                   (cudaStream_t)stream);
+}
+
+int kv_state_set_heads(kvc_cache *cache, int32_t head0, const void *src, size_t src_bytes, int32_t *n_tokens_out,
+                       kvc_stream_t stream) {
+    if (!cache_ok(cache) || !src || !aligned16(src) || !n_tokens_out || head0 < 0) return KVC_EINVAL;
+    if (src_bytes < STATE_HEADER) return KVC_EFORMAT;
+    uint32_t h[8];
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(h, src, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVC_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_ECUDA;
+    const kvc_desc &d = cache->d;
+    if (h[0] != STATE_MAGIC || h[1] != STATE_VERSION) return KVC_EFORMAT;
+    if (h[2] != (uint32_t)d.n_layer || h[4] != (uint32_t)d.head_dim || h[5] != (uint32_t)d.type || h[7] != 0u)
+        return KVC_EFORMAT;
+    if (h[3] == 0u || h[3] > 65536u || (uint64_t)head0 + d.n_head_kv > h[3]) return KVC_EFORMAT;
+    if (h[6] > (uint32_t)d.n_ctx) return KVC_EFORMAT;
+    const int32_t n = (int32_t)h[6];
+    kvc_desc whole = d;
+    whole.n_head_kv = (int32_t)h[3];
+    if (src_bytes != kv_state_size(&whole, n)) return KVC_EFORMAT;
+    const int rc = launch_state_unpack_heads(*cache, head0, (int)h[3], n, static_cast<const uint8_t *>(src), s);
+    if (rc == KVC_OK) *n_tokens_out = n;
+    return rc;
+}
+
 int kv_cache_truncate(const kvc_cache *cache, int32_t n_tokens, kvc_stream_t stream) {
     if (!cache_ok(cache)) return KVC_EINVAL;
     const kvc_desc &d = cache->d;

@@ -60,6 +60,9 @@ int launch_decode_noalloc(const kvc_cache &c, int layer, int pos, const void *q,
                           float *out, cudaStream_t s);
 int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream_t s);
 int launch_state_unpack(const kvc_cache &c, int n_tokens, const uint8_t *src, cudaStream_t s);
+int launch_state_pack_heads(const kvc_cache &c, int head0, int H_total, int n_tokens, uint8_t *dst, cudaStream_t s);
+int launch_state_unpack_heads(const kvc_cache &c, int head0, int H_total, int n_tokens, const uint8_t *src,
+                              cudaStream_t s);
 
 // Device status word set by kernels that give up a bounded wait (all kernels' words, read and cleared).
 int read_and_clear_device_status(int32_t *status);

@@ -64,21 +64,6 @@ __device__ __forceinline__ BlockPos block_pos(const StateArgs &a, int64_t beta) 
     return p;
 }
 
-__device__ __forceinline__ void next_block(const StateArgs &a, BlockPos &p) {
-    if (++p.b < a.nb) return;
-    p.b = 0;
-    if (++p.h < a.H) return;
-    p.h = 0;
-    if (p.kv == 0) {
-        p.kv = 1;
-        return;
-    }
-    p.kv = 0;
-    if (++p.t < a.n_tokens) return;
-    p.t = 0;
-    ++p.layer;
-}
-
 __device__ __forceinline__ int64_t code_off(const StateArgs &a, const BlockPos &p) {
     return p.layer * a.g.c_layer + (int64_t)p.t * a.g.c_tok + p.h * a.g.c_head + p.b * 32;
 }
@@ -352,6 +337,84 @@ __global__ void write_header(uint8_t *dst, uint32_t n_layer, uint32_t H, uint32_
     w[7] = 0u;
 }
 
+// ---- a head range: the cache holds kv heads [head0, head0 + H) of a stream of H_total heads ----
+// A cache split by head (its kv heads spread over several caches, as over several devices) packs each
+// part into its place of one stream, and restores each part from it.  One thread moves one unit: a
+// q8_0 block (34 stream bytes, 17 halfwords: a block starts on an even stream offset) or an f16 chunk
+// of 8 values (16 bytes: a head's 2D stream bytes start 16-byte aligned).
+struct RangeArgs {
+    uint8_t *body;
+    uint8_t *kq, *vq;
+    uint16_t *ks, *vs;
+    Geom g;
+    int64_t n_units;    // units this cache holds: n_layer * n_tokens * 2 * H * units per head
+    int64_t rec;        // stream bytes of one record of all H_total heads
+    int n_tokens, H, head0, upr;   // upr: units per head (head_dim / 32 blocks, or head_dim / 8 chunks)
+    int bph;            // stream bytes per head
+};
+
+template <bool Q8, bool PACK>
+__global__ void __launch_bounds__(256) range_kernel(const RangeArgs a) {
+    const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= a.n_units) return;
+    const int64_t row = u / a.upr;                   // (layer, position, K/V, local head) in stream order
+    const int b = (int)(u - row * a.upr);
+    const int64_t rk = row / a.H;                    // (layer, position, K/V)
+    const int hl = (int)(row - rk * a.H);
+    const int kv = (int)(rk & 1);
+    const int64_t lt = rk >> 1;
+    const int layer = (int)(lt / a.n_tokens);
+    const int t = (int)(lt - (int64_t)layer * a.n_tokens);
+    const int64_t head_row = layer * a.g.c_layer + (int64_t)t * a.g.c_tok + hl * a.g.c_head;
+    uint8_t *s = a.body + rk * a.rec + (int64_t)(a.head0 + hl) * a.bph;
+    if constexpr (Q8) {
+        uint4 *codes = reinterpret_cast<uint4 *>((kv ? a.vq : a.kq) + head_row + 32 * b);
+        uint16_t *scale = (kv ? a.vs : a.ks) + layer * a.g.s_layer + (int64_t)t * a.g.s_tok + hl * a.g.s_head + b;
+        uint16_t *blk = reinterpret_cast<uint16_t *>(s + 34 * b);
+        if (PACK) {
+            const uint4 c0 = codes[0], c1 = codes[1];
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            blk[0] = *scale;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                blk[1 + 2 * i] = (uint16_t)(w[i] & 0xFFFFu);
+                blk[2 + 2 * i] = (uint16_t)(w[i] >> 16);
+            }
+        } else {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = (uint32_t)blk[1 + 2 * i] | ((uint32_t)blk[2 + 2 * i] << 16);
+            *scale = blk[0];
+            codes[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    } else {
+        uint4 *vals = reinterpret_cast<uint4 *>((kv ? a.vq : a.kq) + 2 * head_row) + b;
+        uint4 *chunk = reinterpret_cast<uint4 *>(s) + b;
+        if (PACK) *chunk = *vals;
+        else *vals = *chunk;
+    }
+}
+
+RangeArgs make_range_args(const kvc_cache &c, int head0, int H_total, int n_tokens, uint8_t *body) {
+    RangeArgs a = {};
+    const bool q8 = c.d.type == KVC_Q8_0;
+    a.body = body;
+    a.kq = static_cast<uint8_t *>(c.k_q);
+    a.vq = static_cast<uint8_t *>(c.v_q);
+    a.ks = static_cast<uint16_t *>(c.k_s);
+    a.vs = static_cast<uint16_t *>(c.v_s);
+    a.g = geom_of(c.d);
+    a.n_tokens = n_tokens;
+    a.H = c.d.n_head_kv;
+    a.head0 = head0;
+    a.upr = q8 ? c.d.head_dim / 32 : c.d.head_dim / 8;
+    a.bph = q8 ? (c.d.head_dim / 32) * 34 : c.d.head_dim * 2;
+    a.rec = (int64_t)H_total * a.bph;
+    a.n_units = (int64_t)c.d.n_layer * n_tokens * 2 * a.H * a.upr;
+    return a;
+}
+
 int grid_q8(int64_t n_blocks) {
     const int64_t per_cta = (int64_t)QW * WARP_BLOCKS;
     return (int)((n_blocks + per_cta - 1) / per_cta);
@@ -370,6 +433,30 @@ int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream
     if (n_tokens > 0) {
         if (q8) pack_q8_kernel<<<grid_q8(a.n_blocks), QW * 32, 0, s>>>(a);
         else copy_f16_kernel<true><<<grid_for(a.n_chunks, F16_CHUNKS), THREADS, 0, s>>>(a);
+    }
+    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
+}
+
+int launch_state_pack_heads(const kvc_cache &c, int head0, int H_total, int n_tokens, uint8_t *dst, cudaStream_t s) {
+    const bool q8 = c.d.type == KVC_Q8_0;
+    write_header<<<1, 1, 0, s>>>(dst, c.d.n_layer, H_total, c.d.head_dim, q8 ? 1u : 0u, n_tokens);
+    const RangeArgs a = make_range_args(c, head0, H_total, n_tokens, dst + 32);
+    if (a.n_units > 0) {
+        const int grid = (int)((a.n_units + 255) / 256);
+        if (q8) range_kernel<true, true><<<grid, 256, 0, s>>>(a);
+        else range_kernel<false, true><<<grid, 256, 0, s>>>(a);
+    }
+    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
+}
+
+int launch_state_unpack_heads(const kvc_cache &c, int head0, int H_total, int n_tokens, const uint8_t *src,
+                              cudaStream_t s) {
+    const bool q8 = c.d.type == KVC_Q8_0;
+    const RangeArgs a = make_range_args(c, head0, H_total, n_tokens, const_cast<uint8_t *>(src) + 32);
+    if (a.n_units > 0) {
+        const int grid = (int)((a.n_units + 255) / 256);
+        if (q8) range_kernel<true, false><<<grid, 256, 0, s>>>(a);
+        else range_kernel<false, false><<<grid, 256, 0, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }

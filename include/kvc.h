@@ -251,6 +251,27 @@ int kv_state_get(const kvc_cache *cache, int32_t n_tokens, void *dst, size_t dst
 int kv_state_set(kvc_cache *cache, const void *src, size_t src_bytes, int32_t *n_tokens_out,
                  kvc_stream_t stream);
 
+/* A cache split by head: its kv heads spread over several caches (as over several
+ * devices), each holding a contiguous range.  kv_state_get_heads writes the part
+ * of the stream that `cache`, holding kv heads [head0, head0 + its n_head_kv) of
+ * n_head_total, owns: those heads' blocks (or values) of every record, plus the
+ * header of the whole state (n_head_total heads), which every part writes
+ * identically.  Calls for parts that cover all heads, on one dst, produce the
+ * stream kv_state_get writes for the unsplit cache, byte for byte.
+ * kv_state_set_heads restores that range from a whole stream, however it was
+ * written (llama.cpp PR #59 "llama : switch the split mode of a live context",
+ * section "What this adds", step 1: a state restores into a cache split by
+ * layer or by head; llama.cpp PR #58 "completion : allow the prompt to be
+ * processed under its own split mode", section "The library version, for
+ * later", item 2).  dst/src: device memory sized for the whole state.
+ * Errors as kv_state_get / kv_state_set; KVC_EINVAL for a head range outside
+ * n_head_total; kv_state_set_heads gives KVC_EFORMAT when the header's head
+ * count does not cover the range. */
+int kv_state_get_heads(const kvc_cache *cache, int32_t head0, int32_t n_head_total, int32_t n_tokens, void *dst,
+                       size_t dst_bytes, kvc_stream_t stream);
+int kv_state_set_heads(kvc_cache *cache, int32_t head0, const void *src, size_t src_bytes, int32_t *n_tokens_out,
+                       kvc_stream_t stream);
+
 /* Rewind the cache to its first n_tokens positions: positions [n_tokens, n_ctx)
  * of every layer, codes and scales, are cleared to zero bytes, as in a zeroed
  * cache; earlier positions are untouched.  This is the undo of appends past

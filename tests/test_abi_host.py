@@ -121,6 +121,14 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     assert kvc.lib.kv_cache_truncate(ctypes.byref(c), -1, S) == kvc.KVC_ERANGE
     assert kvc.lib.kv_cache_truncate(ctypes.byref(c), 64, S) == kvc.KVC_OK      # nothing past n_ctx: no-op
     assert kvc.lib.kv_cache_truncate(None, 0, S) == kvc.KVC_EINVAL
+    # a head range of a split cache (c holds 2 kv heads)
+    assert kvc.lib.kv_state_get_heads(ctypes.byref(c), 1, 2, 10, k, 1 << 20, S) == kvc.KVC_EINVAL   # 1 + 2 > 2
+    assert kvc.lib.kv_state_get_heads(ctypes.byref(c), -1, 4, 10, k, 1 << 20, S) == kvc.KVC_EINVAL
+    assert kvc.lib.kv_state_get_heads(ctypes.byref(c), 2, 4, 65, k, 1 << 20, S) == kvc.KVC_ERANGE
+    assert kvc.lib.kv_state_get_heads(ctypes.byref(c), 2, 4, 10, k, 100, S) == kvc.KVC_ENOSPC
+    assert kvc.lib.kv_state_set_heads(ctypes.byref(c), -1, k, 1 << 20, ctypes.byref(ctypes.c_int32()), S) == \
+        kvc.KVC_EINVAL
+    assert kvc.lib.kv_state_set_heads(ctypes.byref(c), 0, k, 16, ctypes.byref(ctypes.c_int32()), S) == kvc.KVC_EFORMAT
     # batched decode: the checks of decode_attn per sequence, plus the batch's own
     big = 1 << 30
     d128 = kvc.make_desc(2, 64, 2, 128, "q8_0")
