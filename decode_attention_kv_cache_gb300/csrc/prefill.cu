@@ -242,6 +242,12 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int first_item = blockIdx.x, stride = gridDim.x;
+    // launched as a programmatic dependent of the kernel before it on the stream (normally the append
+    // of this chunk's keys): the set-up above overlapped that kernel's tail, and everything global
+    // (the cache, Q, the outputs) is read and written only past this wait.  The merge pass may be
+    // scheduled from now on; it waits for this grid in turn.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 
     if (warp < 4) setmaxnreg_dec<L::WG0_REGS>();  // producer, MMA issuer and the Q warps
     if (warp == 0) {
@@ -692,6 +698,8 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
     const int T = unit_tl(a, qt) / BN + 1;
     const int ns = (T + a.ST - 1) / a.ST;
     if (ns <= 1) return;
+    // launched as a programmatic dependent of the attention pass: wait until its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int r = rb * RPB + threadIdx.x / TPR, c4 = (threadIdx.x % TPR) * 4;
     const int row = qt * BM + r;
     if (row >= a.C) return;
@@ -825,10 +833,29 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
         attr_set = true;
     }
     const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
-    kern<<<grid, L::THREADS, L::ALLOC, s>>>(tq, tk, tv, a);
+    // both passes may be scheduled while the kernel before them finishes; each waits for it on the
+    // device before it touches global memory
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(L::THREADS);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a) != cudaSuccess) return KVC_ECUDA;
     if (p.smax > 1) {
         constexpr int BPU = BM / (256 / (D / 4));
-        prefill_merge_kernel<D><<<p.n_qt * n_head_q * BPU, 256, 0, s>>>(a);
+        cudaLaunchConfig_t cfg2 = {};
+        cfg2.gridDim = dim3(p.n_qt * n_head_q * BPU);
+        cfg2.blockDim = dim3(256);
+        cfg2.dynamicSmemBytes = 0;
+        cfg2.stream = s;
+        cfg2.attrs = attr;
+        cfg2.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg2, prefill_merge_kernel<D>, a) != cudaSuccess) return KVC_ECUDA;
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
