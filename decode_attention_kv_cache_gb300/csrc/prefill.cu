@@ -727,6 +727,37 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
         make_float4(acc.x * inv_l, acc.y * inv_l, acc.z * inv_l, acc.w * inv_l);
 }
 
+// ---- q8_0: the attended keys and values dequantised once per call --------------------------
+// fp16(d * q) of positions [0, kv_len) of one layer, K (grid.y 0) then V (1), each as [H][kv_len][D]:
+// the very values the in-kernel dequantiser writes into the operand tiles (same op, same rounding),
+// so the attention pass then runs as for an f16 cache and gives the same bits.  A thread converts 8
+// values (8 code bytes and their block's scale) into 16 bytes.  Launched normally after the append,
+// so it reads the chunk's keys; the attention pass may be scheduled as soon as it starts.
+template <int D>
+__global__ void __launch_bounds__(256) dequant_range_kernel(const int8_t *__restrict__ kq,
+                                                            const uint16_t *__restrict__ ks,
+                                                            const int8_t *__restrict__ vq,
+                                                            const uint16_t *__restrict__ vs, Geom g, int layer,
+                                                            int kv_len, int64_t n_units, __half *dk, __half *dv) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= n_units) return;
+    constexpr int UPR = D / 8;                       // 8-value units per head row
+    const bool is_v = blockIdx.y != 0;
+    const int64_t row = u / UPR;                     // (head, position)
+    const int c = (int)(u - row * UPR);
+    const int h = (int)(row / kv_len);
+    const int t = (int)(row - (int64_t)h * kv_len);
+    const int64_t src = layer * g.c_layer + (int64_t)t * g.c_tok + h * g.c_head + 8 * c;
+    const uint2 w = __ldg(reinterpret_cast<const uint2 *>((is_v ? vq : kq) + src));
+    const uint16_t sb = __ldg((is_v ? vs : ks) + layer * g.s_layer + (int64_t)t * g.s_tok + h * g.s_head + c / 4);
+    const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
+    uint32_t o[4];
+    dequant4(w.x, d2, o[0], o[1]);
+    dequant4(w.y, d2, o[2], o[3]);
+    *reinterpret_cast<uint4 *>((is_v ? dv : dk) + row * D + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // ---- host side ----------------------------------------------------------------------
 // The work decomposition of one call (see the file comment).
 struct Plan {
@@ -872,12 +903,18 @@ int launch_d(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
 
 }  // namespace
 
+// q8_0: bytes of the fp16 copy of one layer's keys and values (capacity n_ctx positions)
+size_t dequant_copy_bytes(const kvc_desc &d) {
+    return d.type == KVC_Q8_0 ? (size_t)2 * d.n_head_kv * d.n_ctx * d.head_dim * sizeof(__half) : 0;
+}
+
 size_t prefill_scratch_bytes(const kvc_desc &d, int n_head_q, int max_tokens) {
     // the largest plan over chunk positions: q-tiles grow with the chunk, splits with the context
     Plan p;
     if (!make_plan(d, n_head_q, d.n_ctx - max_tokens, max_tokens, p)) return 0;
-    return scratch_need(p);
+    return dequant_copy_bytes(d) + scratch_need(p);
 }
+
 
 int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, int dtype,
                    int n_head_q, float *out, void *scratch, size_t scratch_bytes, cudaStream_t s) {
@@ -886,6 +923,40 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
     if (!make_plan(c.d, n_head_q, pos0, n_tokens, p)) return KVC_EINVAL;
     if (scratch_need(p) > scratch_bytes) return KVC_ENOSPC;
     const bool q8 = c.d.type == KVC_Q8_0;
+    const size_t copy_bytes = dequant_copy_bytes(c.d);
+    if (q8 && scratch_bytes >= copy_bytes + scratch_need(p)) {
+        // the attended keys and values dequantised once into the scratch, then attention as for an f16
+        // cache laid out [head][position][D]; the plan (key splits) stays the q8_0 cache's own
+        const int kv_len = pos0 + n_tokens, H = c.d.n_head_kv, D = c.d.head_dim;
+        __half *dk = static_cast<__half *>(scratch);
+        __half *dv = dk + (size_t)H * c.d.n_ctx * D;
+        const int64_t n_units = (int64_t)H * kv_len * (D / 8);
+        const dim3 grid((unsigned)((n_units + 255) / 256), 2);
+        const Geom g = geom_of(c.d);
+        if (D == 128)
+            dequant_range_kernel<128><<<grid, 256, 0, s>>>(static_cast<const int8_t *>(c.k_q),
+                                                           static_cast<const uint16_t *>(c.k_s),
+                                                           static_cast<const int8_t *>(c.v_q),
+                                                           static_cast<const uint16_t *>(c.v_s), g, layer, kv_len,
+                                                           n_units, dk, dv);
+        else
+            dequant_range_kernel<64><<<grid, 256, 0, s>>>(static_cast<const int8_t *>(c.k_q),
+                                                          static_cast<const uint16_t *>(c.k_s),
+                                                          static_cast<const int8_t *>(c.v_q),
+                                                          static_cast<const uint16_t *>(c.v_s), g, layer, kv_len,
+                                                          n_units, dk, dv);
+        kvc_cache f = {};
+        f.d = c.d;
+        f.d.n_layer = 1;
+        f.d.n_ctx = kv_len;
+        f.d.type = KVC_F16;
+        f.d.layout = KVC_HEAD_MAJOR;
+        f.k_q = dk;
+        f.v_q = dv;
+        void *part = static_cast<uint8_t *>(scratch) + copy_bytes;
+        return D == 128 ? launch_d<128, false>(f, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s)
+                        : launch_d<64, false>(f, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s);
+    }
     if (c.d.head_dim == 128)
         return q8 ? launch_d<128, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s)
                   : launch_d<128, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s);

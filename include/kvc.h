@@ -152,8 +152,10 @@ int kv_cache_append_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer,
 
 /* Bytes of the scratch buffer prefill_chunk_attn needs for chunks of up to
  * max_tokens rows anywhere in this cache: the float32 partial results
- * (output row, running max, sum) of the key splits, at least 256 bytes.  The
- * contents need no initialisation; every call writes what it reads. */
+ * (output row, running max, sum) of the key splits, at least 256 bytes, and for
+ * a q8_0 cache in front of them room for an fp16 copy of one layer's keys and
+ * values (2 * n_head_kv * n_ctx * head_dim * 2 bytes).  The contents need no
+ * initialisation; every call writes what it reads. */
 int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t max_tokens, size_t *bytes);
 
 /* Causal attention of a chunk's query rows over the cache:
@@ -161,15 +163,21 @@ int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t ma
  * for i in [0, n_tokens), G = n_head_q / n_head_kv, khat/vhat the values the
  * cache holds for `layer` at positions [0, pos0 + n_tokens).  The chunk's own
  * K/V must have been appended (kv_cache_append earlier on the same stream).
- * Keys are processed in tiles of 128 and splits whose boundaries sit at
+ * Keys are processed in tiles of 256 and splits whose boundaries sit at
  * absolute positions (a size fixed by n_ctx); partial results of a row are
  * merged in split order, so a row's output is bitwise independent of how the
  * prompt is cut into chunks.  Computed with fp16 tensor-core products and
- * float32 accumulation and softmax.
+ * float32 accumulation and softmax.  A q8_0 cache's keys and values enter the
+ * products as fp16(d * q): with the full scratch of kvc_prefill_scratch_bytes,
+ * positions [0, pos0 + n_tokens) are first dequantised once into the scratch
+ * (one more kernel), and the attention reads that copy; with a scratch that
+ * holds only the partials, the attention kernel dequantises each tile in
+ * shared memory instead (slower: once per 128-row query tile).  Both give the
+ * same bits.
  * q: [n_tokens][n_head_q][head_dim] in dtype (f32, bf16 or f16); out float32.
- * Two kernels on `stream`: the attention (partials of rows whose keys span
- * several splits go to scratch) and, when any row has several splits, the
- * merge.  scratch: device buffer of scratch_bytes >=
+ * Kernels on `stream`: for q8_0 with the full scratch the dequantising pass,
+ * then the attention (partials of rows whose keys span several splits go to
+ * scratch) and, when any row has several splits, the merge.  scratch: device buffer of scratch_bytes >=
  * kvc_prefill_scratch_bytes(desc, n_head_q, n_tokens); calls on one scratch
  * buffer must not overlap on the GPU.
  * Errors: KVC_EINVAL (null, dtype, head_dim not 64/128, heads), KVC_ERANGE,

@@ -173,7 +173,11 @@ def test_prefill_scratch_query(kvc):
     assert out.value < big
     small = kvc.make_desc(1, 512, 2, 64, "q8_0")
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 4, 64, ctypes.byref(out)) == kvc.KVC_OK
-    assert out.value == 256        # one split: no partials, the minimum size
+    # one split: no partials, the minimum 256 bytes, behind the fp16 copy of K and V (2 * 2 * 512 * 64 * 2)
+    assert out.value == 2 * 2 * 512 * 64 * 2 + 256
+    small16 = kvc.make_desc(1, 512, 2, 64, "f16")
+    assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small16), 4, 64, ctypes.byref(out)) == kvc.KVC_OK
+    assert out.value == 256
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 4, 513, ctypes.byref(out)) == kvc.KVC_ERANGE
     assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(small), 3, 64, ctypes.byref(out)) == kvc.KVC_EINVAL
 

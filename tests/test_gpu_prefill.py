@@ -1,6 +1,8 @@
 """prefill_chunk_attn on the GPU: within tolerance of the oracle, and bitwise
 independent of the chunking and of the cache layout."""
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -133,3 +135,30 @@ def test_scratch_reused_after_a_short_chunk(kvc):
         fresh = g.prefill_scratch(w.n_head_q, 1024).fill_(0xA5)
         b = kvc.prefill_chunk_attn(g, 0, p, q[p:p + 1024], scratch=fresh)
         assert torch.equal(a, b), "chunk at %d" % p
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f32")])
+def test_q8_0_dequantised_copy_and_in_kernel_dequant_agree_bitwise(kvc, d, dtype):
+    # the full scratch dequantises the attended keys once and attends over that fp16 copy; a scratch
+    # holding only the partials makes the attention kernel dequantise each tile in shared memory.
+    # Both enter fp16(d * q) into the same products in the same order.
+    w = si.small_workload("twopath", 10, 2, d, "q8_0", "bf16" if dtype == "bf16" else "f32", n_prompt=5000,
+                          chunk=1000, n_decode=0, seed=91, k_outlier_frac=0.01)
+    q, k, v = (t.cuda() for t in si.layer_qkv(w, 0))
+    g = kvc.KVCache(1, w.n_ctx, w.n_head_kv, w.head_dim, "q8_0", "head_major")
+    full = g.prefill_scratch(w.n_head_q, 1000)
+    d16 = kvc.make_desc(1, w.n_ctx, w.n_head_kv, w.head_dim, "f16", "head_major")
+    n = ctypes.c_size_t()
+    assert kvc.lib.kvc_prefill_scratch_bytes(ctypes.byref(d16), w.n_head_q, 1000, ctypes.byref(n)) == 0
+    small = torch.empty(n.value, dtype=torch.uint8, device="cuda")
+    assert small.numel() < full.numel()
+    outs = []
+    for scratch in (full, small):
+        out = torch.empty(w.n_prompt, w.n_head_q, w.head_dim, device="cuda")
+        for p, c in w.chunks(1000):
+            kvc.kv_cache_append(g, 0, p, k[p:p + c], v[p:p + c])
+            kvc.prefill_chunk_attn(g, 0, p, q[p:p + c], out=out[p:p + c], scratch=scratch)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    assert kvc.kvc_device_status() == 0
