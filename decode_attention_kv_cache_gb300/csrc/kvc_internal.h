@@ -37,8 +37,11 @@ inline int dtype_bytes(int dtype) { return dtype == KVC_IN_F32 ? 4 : 2; }
 bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
                  uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
                  uint32_t b2, CUtensorMapSwizzle sw);
-// Streaming multiprocessors of the current device (cached after the first call).
+// Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+// Raise `kernel`'s dynamic shared memory limit to `bytes` on the current device, once per device (the
+// attribute belongs to the device's context).  KVC_OK or KVC_ECUDA.
+int allow_dynamic_smem(const void *kernel, int bytes);
 
 // Launchers: arguments are already validated; return KVC_OK or KVC_ECUDA.
 int launch_append(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *k,

@@ -857,12 +857,7 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     for (int i = 0; i <= MAX_SPLITS; ++i) a.cum[i] = i <= p.smax ? p.cum[i] : p.n_items;
     for (int i = 0; i < MAX_SPLITS; ++i) a.qtmin[i] = i < p.smax ? p.qtmin[i] : p.n_qt;
     auto kern = prefill_kernel<D, Q8, QDT>;
-    static bool attr_set = false;  // per instantiation
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
-            return KVC_ECUDA;
-        attr_set = true;
-    }
+    if (allow_dynamic_smem((const void *)kern, L::ALLOC) != KVC_OK) return KVC_ECUDA;
     const int grid = p.n_items < sm_count() ? p.n_items : sm_count();
     // both passes may be scheduled while the kernel before them finishes; each waits for it on the
     // device before it touches global memory

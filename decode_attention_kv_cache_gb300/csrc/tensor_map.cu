@@ -4,7 +4,10 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "kvc_internal.h"
 
@@ -41,15 +44,30 @@ bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
 }
 
 int sm_count() {
-    static int n = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 148;
-    });
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    static std::mutex mu;
+    static std::map<int, int> count;   // per device
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = count.find(dev);
+    if (it != count.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    count[dev] = n;
     return n;
+}
+
+int allow_dynamic_smem(const void *kernel, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ECUDA;
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;   // (kernel, device) pairs already raised
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kernel, dev})) return KVC_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return KVC_ECUDA;
+    done.insert({kernel, dev});
+    return KVC_OK;
 }
 
 }  // namespace kvc
