@@ -317,6 +317,15 @@ def l2_flush(torch, buf):
     buf.add_(1)
 
 
+def workload_config(w):
+    """The bench line's config: the workload by name and shape (both arms print the same)."""
+    return {"workload": w.name, "n_layer": w.n_layer, "n_head_q": w.n_head_q, "n_head_kv": w.n_head_kv,
+            "head_dim": w.head_dim, "cache": w.cache, "in_dtype": w.in_dtype, "n_ctx": w.n_ctx,
+            "n_prompt": w.n_prompt, "chunk": w.chunk, "n_decode": w.n_decode,
+            "parallelism": "replicas (one independent layer stack per GPU)",
+            "l2": "flushed (256 MiB write) before each timed step", "decode_loop": "CUDA graph"}
+
+
 def run_gpu(args, rank, world, local):
     import torch
     import decode_attention_kv_cache_gb300 as kvc
@@ -399,11 +408,7 @@ def run_gpu(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16xf16->f32 (tensor), f32 softmax; int8/f16 cache", "data": "synthetic (seeded N(0,1))",
-        "config": {"workload": w.name, "n_layer": w.n_layer, "n_head_q": w.n_head_q, "n_head_kv": w.n_head_kv,
-                   "head_dim": w.head_dim, "cache": w.cache, "in_dtype": w.in_dtype, "n_ctx": w.n_ctx,
-                   "n_prompt": w.n_prompt, "chunk": w.chunk, "n_decode": w.n_decode,
-                   "parallelism": "replicas (one independent layer stack per GPU)",
-                   "l2": "flushed (256 MiB write) before each timed step", "decode_loop": "CUDA graph"},
+        "config": workload_config(w),
         "phases": phases, "roofline": roof, "e2e": e2e, "gpu_launches": req.launches_per_step() * K,
         "clocks": clk,
     }
@@ -675,7 +680,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic (seeded N(0,1))",
-            "config": {"workload": w.name, "n_layer": 1, "n_prompt": w.n_prompt, "n_decode": w.n_decode},
+            "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": samp},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
