@@ -339,9 +339,7 @@ __global__ void write_header(uint8_t *dst, uint32_t n_layer, uint32_t H, uint32_
 
 // ---- a head range: the cache holds kv heads [head0, head0 + H) of a stream of H_total heads ----
 // A cache split by head (its kv heads spread over several caches, as over several devices) packs each
-// part into its place of one stream, and restores each part from it.  One thread moves one unit: a
-// q8_0 block (34 stream bytes, 17 halfwords: a block starts on an even stream offset) or an f16 chunk
-// of 8 values (16 bytes: a head's 2D stream bytes start 16-byte aligned).
+// part into its place of one stream, and restores each part from it.
 struct RangeArgs {
     uint8_t *body;
     uint8_t *kq, *vq;
@@ -353,8 +351,10 @@ struct RangeArgs {
     int bph;            // stream bytes per head
 };
 
-template <bool Q8, bool PACK>
-__global__ void __launch_bounds__(256) range_kernel(const RangeArgs a) {
+// f16 head range: one thread moves one 16-byte chunk of 8 values (a head's 2 * head_dim stream bytes
+// start 16-byte aligned).
+template <bool PACK>
+__global__ void __launch_bounds__(256) range_f16_kernel(const RangeArgs a) {
     const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (u >= a.n_units) return;
     const int64_t row = u / a.upr;                   // (layer, position, K/V, local head) in stream order
@@ -366,34 +366,79 @@ __global__ void __launch_bounds__(256) range_kernel(const RangeArgs a) {
     const int layer = (int)(lt / a.n_tokens);
     const int t = (int)(lt - (int64_t)layer * a.n_tokens);
     const int64_t head_row = layer * a.g.c_layer + (int64_t)t * a.g.c_tok + hl * a.g.c_head;
-    uint8_t *s = a.body + rk * a.rec + (int64_t)(a.head0 + hl) * a.bph;
-    if constexpr (Q8) {
-        uint4 *codes = reinterpret_cast<uint4 *>((kv ? a.vq : a.kq) + head_row + 32 * b);
-        uint16_t *scale = (kv ? a.vs : a.ks) + layer * a.g.s_layer + (int64_t)t * a.g.s_tok + hl * a.g.s_head + b;
-        uint16_t *blk = reinterpret_cast<uint16_t *>(s + 34 * b);
-        if (PACK) {
-            const uint4 c0 = codes[0], c1 = codes[1];
-            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            blk[0] = *scale;
+    uint4 *vals = reinterpret_cast<uint4 *>((kv ? a.vq : a.kq) + 2 * head_row) + b;
+    uint4 *chunk = reinterpret_cast<uint4 *>(a.body + rk * a.rec + (int64_t)(a.head0 + hl) * a.bph) + b;
+    if (PACK) *chunk = *vals;
+    else *vals = *chunk;
+}
+
+// q8_0 head range, pack: one warp per record run.  The part's H heads of one (layer, position, K/V)
+// record are H * head_dim/32 consecutive 34-byte blocks of the stream, a run that starts on a 4-byte
+// boundary (32-byte header; records and heads of 34 * head_dim/32 bytes, a multiple of 4).  The warp
+// assembles the run in shared memory, one block per lane, then stores it in 4-byte words with
+// consecutive lanes on consecutive words (halfword stores straight to the stream measured 4x slower).
+constexpr int RUN_WARPS = 8;
+__global__ void __launch_bounds__(RUN_WARPS * 32) range_q8_pack_kernel(const RangeArgs a, int run_bytes) {
+    extern __shared__ __align__(16) uint8_t run_smem[];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t rk = (int64_t)blockIdx.x * RUN_WARPS + wid;         // (layer, position, K/V)
+    const int64_t n_runs = a.n_units / ((int64_t)a.H * a.upr);
+    if (rk >= n_runs) return;   // the whole warp
+    uint16_t *run = reinterpret_cast<uint16_t *>(run_smem + wid * run_bytes);
+    const int kv = (int)(rk & 1);
+    const int64_t lt = rk >> 1;
+    const int layer = (int)(lt / a.n_tokens);
+    const int t = (int)(lt - (int64_t)layer * a.n_tokens);
+    uint32_t *s = reinterpret_cast<uint32_t *>(a.body + rk * a.rec + (int64_t)a.head0 * a.bph);
+    const int n_blocks = a.H * a.upr, n_words = run_bytes / 4;
+    auto block_ptrs = [&](int j, uint4 *&codes, uint16_t *&scale) {
+        const int hl = j / a.upr, b = j - hl * a.upr;
+        codes = reinterpret_cast<uint4 *>((kv ? a.vq : a.kq) + layer * a.g.c_layer + (int64_t)t * a.g.c_tok +
+                                          hl * a.g.c_head + 32 * b);
+        scale = (kv ? a.vs : a.ks) + layer * a.g.s_layer + (int64_t)t * a.g.s_tok + hl * a.g.s_head + b;
+    };
+    for (int j = lane; j < n_blocks; j += 32) {
+        uint4 *codes;
+        uint16_t *scale;
+        block_ptrs(j, codes, scale);
+        const uint4 c0 = codes[0], c1 = codes[1];
+        const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint16_t *blk = run + 17 * j;
+        blk[0] = *scale;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                blk[1 + 2 * i] = (uint16_t)(w[i] & 0xFFFFu);
-                blk[2 + 2 * i] = (uint16_t)(w[i] >> 16);
-            }
-        } else {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = (uint32_t)blk[1 + 2 * i] | ((uint32_t)blk[2 + 2 * i] << 16);
-            *scale = blk[0];
-            codes[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        for (int i = 0; i < 8; ++i) {
+            blk[1 + 2 * i] = (uint16_t)(w[i] & 0xFFFFu);
+            blk[2 + 2 * i] = (uint16_t)(w[i] >> 16);
         }
-    } else {
-        uint4 *vals = reinterpret_cast<uint4 *>((kv ? a.vq : a.kq) + 2 * head_row) + b;
-        uint4 *chunk = reinterpret_cast<uint4 *>(s) + b;
-        if (PACK) *chunk = *vals;
-        else *vals = *chunk;
     }
+    __syncwarp();
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(run);
+    for (int i = lane; i < n_words; i += 32) s[i] = src[i];
+}
+
+// q8_0 head range, unpack: one thread per block, 17 halfword loads from the stream (a block starts on
+// an even offset), then the 32 codes and the scale to the cache (measured faster than staging runs).
+__global__ void __launch_bounds__(256) range_q8_unpack_kernel(const RangeArgs a) {
+    const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= a.n_units) return;
+    const int64_t row = u / a.upr;                   // (layer, position, K/V, local head) in stream order
+    const int b = (int)(u - row * a.upr);
+    const int64_t rk = row / a.H;                    // (layer, position, K/V)
+    const int hl = (int)(row - rk * a.H);
+    const int kv = (int)(rk & 1);
+    const int64_t lt = rk >> 1;
+    const int layer = (int)(lt / a.n_tokens);
+    const int t = (int)(lt - (int64_t)layer * a.n_tokens);
+    const uint16_t *blk = reinterpret_cast<const uint16_t *>(a.body + rk * a.rec + (int64_t)(a.head0 + hl) * a.bph +
+                                                             34 * b);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = (uint32_t)blk[1 + 2 * i] | ((uint32_t)blk[2 + 2 * i] << 16);
+    uint4 *codes = reinterpret_cast<uint4 *>((kv ? a.vq : a.kq) + layer * a.g.c_layer + (int64_t)t * a.g.c_tok +
+                                             hl * a.g.c_head + 32 * b);
+    (kv ? a.vs : a.ks)[layer * a.g.s_layer + (int64_t)t * a.g.s_tok + hl * a.g.s_head + b] = blk[0];
+    codes[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 RangeArgs make_range_args(const kvc_cache &c, int head0, int H_total, int n_tokens, uint8_t *body) {
@@ -442,9 +487,17 @@ int launch_state_pack_heads(const kvc_cache &c, int head0, int H_total, int n_to
     write_header<<<1, 1, 0, s>>>(dst, c.d.n_layer, H_total, c.d.head_dim, q8 ? 1u : 0u, n_tokens);
     const RangeArgs a = make_range_args(c, head0, H_total, n_tokens, dst + 32);
     if (a.n_units > 0) {
-        const int grid = (int)((a.n_units + 255) / 256);
-        if (q8) range_kernel<true, true><<<grid, 256, 0, s>>>(a);
-        else range_kernel<false, true><<<grid, 256, 0, s>>>(a);
+        if (q8) {
+            const int run_bytes = a.H * a.bph;
+            const int64_t n_runs = (int64_t)c.d.n_layer * n_tokens * 2;
+            const size_t smem = (size_t)RUN_WARPS * run_bytes;
+            if (smem > 48 * 1024 && allow_dynamic_smem((const void *)range_q8_pack_kernel, (int)smem) != KVC_OK)
+                return KVC_ECUDA;
+            range_q8_pack_kernel<<<(unsigned)((n_runs + RUN_WARPS - 1) / RUN_WARPS), RUN_WARPS * 32, smem, s>>>(
+                a, run_bytes);
+        } else {
+            range_f16_kernel<true><<<(int)((a.n_units + 255) / 256), 256, 0, s>>>(a);
+        }
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
@@ -454,9 +507,11 @@ int launch_state_unpack_heads(const kvc_cache &c, int head0, int H_total, int n_
     const bool q8 = c.d.type == KVC_Q8_0;
     const RangeArgs a = make_range_args(c, head0, H_total, n_tokens, const_cast<uint8_t *>(src) + 32);
     if (a.n_units > 0) {
-        const int grid = (int)((a.n_units + 255) / 256);
-        if (q8) range_kernel<true, false><<<grid, 256, 0, s>>>(a);
-        else range_kernel<false, false><<<grid, 256, 0, s>>>(a);
+        if (q8) {
+            range_q8_unpack_kernel<<<(int)((a.n_units + 255) / 256), 256, 0, s>>>(a);
+        } else {
+            range_f16_kernel<false><<<(int)((a.n_units + 255) / 256), 256, 0, s>>>(a);
+        }
     }
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
