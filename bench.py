@@ -229,13 +229,15 @@ class GpuRequest:
         return layer if self.w.n_layer == 1 else 0
 
     def launches_per_step(self):
-        """Kernels one step launches: per chunk an append and the attention, plus the split merge when
+        """Kernels one step launches: per chunk an append and the attention (q8_0: and the pass that
+        dequantises the attended keys into the prefill scratch), plus the split merge when
         the chunk's last row reaches past the first key split; per decode step append, split pass and
         combine; the state header, pack and unpack."""
         w = self.w
         keys = prefill_split_keys(w.n_ctx)
         merges = sum(1 for p, c in self.chunks if p + c - 1 >= keys)
-        return w.n_layer * (2 * len(self.chunks) + merges + 3 * w.n_decode) + 3
+        per_chunk = 3 if w.cache == "q8_0" else 2
+        return w.n_layer * (per_chunk * len(self.chunks) + merges + 3 * w.n_decode) + 3
 
     def _decode_loop(self, layer):
         kvc, w = self.kvc, self.w
