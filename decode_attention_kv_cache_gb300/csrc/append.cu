@@ -87,8 +87,11 @@ __global__ void __launch_bounds__(256) append_f16_kernel(
     const void *__restrict__ k, const void *__restrict__ v, int64_t n_units, int units_per_tok,
     int units_per_head, const DST dst_of, int layer) {
     // a kernel launched after this one as a programmatic dependent (the decode split pass) may be
-    // scheduled now; it waits for this grid's completion before it reads the cache
+    // scheduled now; it waits for this grid's completion before it reads the cache.  This grid is
+    // itself launched as a programmatic dependent: it waits for the kernel before it to complete
+    // before it reads its inputs or writes the cache.
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool is_v = blockIdx.y != 0;
     const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (u >= n_units) return;
@@ -137,6 +140,7 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
     const void *__restrict__ k, const void *__restrict__ v, int64_t n_blocks, int nb, int H, const DST dst_of,
     int layer) {
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // as in append_f16_kernel
     constexpr int ESZ = DT == KVC_IN_F32 ? 4 : 2;
     constexpr int CPB = 2 * ESZ;                   // 16-byte input chunks per block
     __shared__ uint4 stage[8][32 * CPB];
@@ -212,34 +216,47 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
 }
 
 // n tokens of k and v ([n][H_kv][head_dim]) to the destinations dst_of gives them; desc: their shape
+// Launched as a programmatic dependent of the kernel before it in the stream: its launch overlaps
+// that kernel's tail, and the kernel waits on the device (griddepcontrol.wait) before touching memory.
 template <int DT, class DST>
-void launch_t(const kvc_desc &desc, const DST &dst_of, int layer, int n, const void *k, const void *v,
-              cudaStream_t s) {
+cudaError_t launch_t(const kvc_desc &desc, const DST &dst_of, int layer, int n, const void *k, const void *v,
+                     cudaStream_t s) {
     const int threads = 256;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (desc.type == KVC_Q8_0) {
         const int nb = desc.head_dim / 32;
         const int64_t n_blocks = (int64_t)n * desc.n_head_kv * nb;
-        dim3 grid((unsigned)((n_blocks + threads - 1) / threads), 2);
-        append_q8_kernel<DT, DST><<<grid, threads, 0, s>>>(k, v, n_blocks, nb, desc.n_head_kv, dst_of, layer);
+        cfg.gridDim = dim3((unsigned)((n_blocks + threads - 1) / threads), 2);
+        return cudaLaunchKernelEx(&cfg, append_q8_kernel<DT, DST>, k, v, n_blocks, nb, (int)desc.n_head_kv, dst_of,
+                                  layer);
     } else {
         const int units_per_head = desc.head_dim / 8;
         const int units_per_tok = units_per_head * desc.n_head_kv;
         const int64_t n_units = (int64_t)n * units_per_tok;
-        dim3 grid((unsigned)((n_units + threads - 1) / threads), 2);
-        append_f16_kernel<DT, DST><<<grid, threads, 0, s>>>(k, v, n_units, units_per_tok, units_per_head, dst_of,
-                                                            layer);
+        cfg.gridDim = dim3((unsigned)((n_units + threads - 1) / threads), 2);
+        return cudaLaunchKernelEx(&cfg, append_f16_kernel<DT, DST>, k, v, n_units, units_per_tok, units_per_head,
+                                  dst_of, layer);
     }
 }
 
 template <class DST>
 int launch_dtype(const kvc_desc &desc, const DST &dst_of, int layer, int n, const void *k, const void *v, int dtype,
                  cudaStream_t s) {
+    cudaError_t e;
     switch (dtype) {
-        case KVC_IN_F32: launch_t<KVC_IN_F32>(desc, dst_of, layer, n, k, v, s); break;
-        case KVC_IN_BF16: launch_t<KVC_IN_BF16>(desc, dst_of, layer, n, k, v, s); break;
-        default: launch_t<KVC_IN_F16>(desc, dst_of, layer, n, k, v, s); break;
+        case KVC_IN_F32: e = launch_t<KVC_IN_F32>(desc, dst_of, layer, n, k, v, s); break;
+        case KVC_IN_BF16: e = launch_t<KVC_IN_BF16>(desc, dst_of, layer, n, k, v, s); break;
+        default: e = launch_t<KVC_IN_F16>(desc, dst_of, layer, n, k, v, s); break;
     }
-    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? KVC_OK : KVC_ECUDA;
 }
 
 }  // namespace

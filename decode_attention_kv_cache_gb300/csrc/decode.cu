@@ -515,6 +515,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS
     __shared__ float s_M, s_L;
     const int h = blockIdx.x, d = threadIdx.x;
     const int hkv = h / group, row = h % group;
+    // the next kernel (the next step's append) may be scheduled now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
     // launched as a programmatic dependent of the split pass: wait until its partials are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *part_o = part;

@@ -692,6 +692,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
 // 256 / (D/4) rows of one unit.
 template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
+    // the next kernel (the next chunk's append) may be scheduled now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
     constexpr int TPR = D / 4, RPB = 256 / TPR, BPU = BM / RPB;
     const int rb = blockIdx.x % BPU, unit = blockIdx.x / BPU;
     const int qt = unit / a.H_q, h = unit % a.H_q;
