@@ -499,20 +499,18 @@ __global__ void __maxnreg__(200)
     if (threadIdx.x == 0 && *s_abort) atomicExch(&g_decode_status, 1);
 }
 
-// One CTA per query head, one thread per output value.  The split maxima,
-// weights and weighted softmax denominators are computed in parallel into shared
-// memory; the denominators are then added in split order by one thread (from
-// shared memory), and each thread sums its value over the splits in split order
-// (independent loads, unrolled), so the result is deterministic.
+// One CTA per query head, one thread per output value.  With up to MC splits (one wave of split
+// CTAs gives at most 19 per kv head at 8 kv heads) a thread issues every split's (m, l) pair and
+// partial value at once, so the pass costs one round trip to L2 and no block barrier; more splits
+// take the same steps in rounds of 8.  The weights are ex2(m_i - M) (M the largest split maximum),
+// the denominator and the value are summed in split order, so the result is deterministic.
 template <int D, int NS>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS> cb, int group, int n_head_kv) {
+    constexpr int MC = 24;
     const int seq = NS == 1 ? 0 : (int)blockIdx.y;
     const float *__restrict__ part = cb.part[seq];
     float *__restrict__ out = cb.out[seq];
     const int n_split = cb.n_split[seq];
-    __shared__ float s_w[MAX_SPLIT], s_wl[MAX_SPLIT];
-    __shared__ float s_red[D / 32];
-    __shared__ float s_M, s_L;
     const int h = blockIdx.x, d = threadIdx.x;
     const int hkv = h / group, row = h % group;
     // the next kernel (the next step's append) may be scheduled now; it waits for this grid
@@ -522,44 +520,59 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS
     const float *part_o = part;
     const float *part_ml = part + (int64_t)n_head_kv * MAX_SPLIT * group * D;
     const int64_t p0 = ((int64_t)hkv * MAX_SPLIT) * group + row;   // partial index of split 0
-    // maximum over splits
-    float m = -INFINITY;
-    for (int i = d; i < n_split; i += D) m = fmaxf(m, part_ml[(p0 + (int64_t)i * group) * 2]);
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((d & 31) == 0) s_red[d >> 5] = m;
-    __syncthreads();
-    if (d == 0) {
-        float M = s_red[0];
-        for (int w = 1; w < D / 32; ++w) M = fmaxf(M, s_red[w]);
-        s_M = M;
-    }
-    __syncthreads();
-    const float M = s_M;
-    // split weights and weighted denominators
-    for (int i = d; i < n_split; i += D) {
-        const float2 ml = *reinterpret_cast<const float2 *>(part_ml + (p0 + (int64_t)i * group) * 2);
-        const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
-        s_w[i] = w;
-        s_wl[i] = w * ml.y;
-    }
-    __syncthreads();
-    if (d == 0) {
-        float L = 0.f;
-        for (int i = 0; i < n_split; ++i) L += s_wl[i];
-        s_L = L;
-    }
-    float acc = 0.f;
-    int i = 0;
-    for (; i + 8 <= n_split; i += 8) {
-        float v[8];
+    const float2 *ml_src = reinterpret_cast<const float2 *>(part_ml) + p0;   // split i at + i * group
+    const float *o_src = part_o + p0 * D + d;                                 // split i at + i * group * D
+    const int64_t o_step = (int64_t)group * D;
+    float M = -INFINITY, L = 0.f, acc = 0.f;
+    if (n_split <= MC) {
+        float2 ml[MC];
+        float v[MC];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = part_o[(p0 + (int64_t)(i + u) * group) * D + d];
+        for (int i = 0; i < MC; ++i) {
+            if (i < n_split) {
+                ml[i] = __ldcg(ml_src + (int64_t)i * group);
+                v[i] = __ldcg(o_src + (int64_t)i * o_step);
+            } else {
+                ml[i] = make_float2(-INFINITY, 0.f);
+                v[i] = 0.f;
+            }
+        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc += s_w[i + u] * v[u];
+        for (int i = 0; i < MC; ++i) M = fmaxf(M, ml[i].x);
+#pragma unroll
+        for (int i = 0; i < MC; ++i) {
+            if (i < n_split) {
+                const float w = (ml[i].x == -INFINITY) ? 0.f : ex2(ml[i].x - M);
+                L = __fadd_rn(L, __fmul_rn(w, ml[i].y));
+                acc = fmaf(w, v[i], acc);
+            }
+        }
+    } else {
+        for (int i = 0; i < n_split; ++i) M = fmaxf(M, __ldcg(ml_src + (int64_t)i * group).x);
+        for (int i0 = 0; i0 < n_split; i0 += 8) {
+            float2 ml[8];
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (i0 + u < n_split) {
+                    ml[u] = __ldcg(ml_src + (int64_t)(i0 + u) * group);
+                    v[u] = __ldcg(o_src + (int64_t)(i0 + u) * o_step);
+                } else {
+                    ml[u] = make_float2(-INFINITY, 0.f);
+                    v[u] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (i0 + u < n_split) {
+                    const float w = (ml[u].x == -INFINITY) ? 0.f : ex2(ml[u].x - M);
+                    L = __fadd_rn(L, __fmul_rn(w, ml[u].y));
+                    acc = fmaf(w, v[u], acc);
+                }
+            }
+        }
     }
-    for (; i < n_split; ++i) acc += s_w[i] * part_o[(p0 + (int64_t)i * group) * D + d];
-    __syncthreads();
-    out[(int64_t)h * D + d] = acc / s_L;
+    out[(int64_t)h * D + d] = acc / L;
 }
 
 // ---- tensor-core split pass for head_dim 128 ---------------------------------------------
