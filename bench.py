@@ -610,14 +610,15 @@ def chunk_sweep(kvc, torch, w, req, device, flush, reps):
 
 
 # --------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
-def oracle_sample(w, max_chunks=16, rows_per_chunk=64, decode_samples=32):
+def oracle_sample(w, max_chunks=16, rows_per_chunk=64, decode_samples=32, sample_offset=0):
     """Time the oracle on a bounded sample of one layer's request; extrapolate to the whole request.
 
     Appends (quantisation) of every token and the state pack/unpack are timed
     whole.  Prefill: for up to `max_chunks` evenly spaced chunks, the cache
     dequantisation (scaled by cache length) and the attention of
     `rows_per_chunk` rows (scaled by the causal row work sum (t+1)).  Decode:
-    `decode_samples` steps, scaled by sum (pos+1).
+    `decode_samples` steps, scaled by sum (pos+1).  `sample_offset` picks another seeded set of
+    sampled rows (independent samples for concurrent processes).
     """
     from oracle import state as ostate
     from oracle.attention import attend
@@ -634,7 +635,7 @@ def oracle_sample(w, max_chunks=16, rows_per_chunk=64, decode_samples=32):
         o.append(0, p, kf[p:p + 1], vf[p:p + 1])
     t_append = time.perf_counter() - t0
     pick = sorted(set(np.linspace(0, len(chunks) - 1, min(max_chunks, len(chunks))).round().astype(int).tolist()))
-    rng = np.random.default_rng(w.seed)
+    rng = np.random.default_rng(w.seed + 7919 * sample_offset)
     t_deq = t_att = 0.0
     deq_units = att_units = 0.0
     for ci in pick:
@@ -678,20 +679,85 @@ def oracle_sample(w, max_chunks=16, rows_per_chunk=64, decode_samples=32):
                                                      min(decode_samples, w.n_decode), w.n_decode)}
 
 
-def cpu_baseline(workload):
-    """The oracle in a child process restricted to one thread (so `cores` is exact)."""
+def _oracle_env():
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[k] = "1"
     env.pop("WORLD_SIZE", None)
     env.pop("RANK", None)
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", workload],
-                       capture_output=True, text=True, env=env, timeout=900)
+    return env
+
+
+def _oracle_cmd(workload, offset):
+    return [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", workload,
+            "--oracle-offset", str(offset)]
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _mem_available_gb():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) / (1 << 20)
+    except OSError:
+        pass
+    return None
+
+
+def oracle_all_cores(workload, gb_per_process):
+    """The oracle on every host core: one single-threaded oracle process per core (at most 16, and
+    no more than the available memory holds at gb_per_process each), started together, each on its
+    own seeded sample of the workload.  Independent requests share nothing, so the host's rate is the
+    sum of the processes' rates, each measured while all of them run."""
+    n = min(_host_cores(), 16)
+    mem = _mem_available_gb()
+    if mem is not None:
+        n = max(1, min(n, int(mem // gb_per_process)))
+    env = _oracle_env()
+    procs = [subprocess.Popen(_oracle_cmd(workload, i + 1), stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                              text=True, env=env) for i in range(n)]
+    vals, err = [], None
+    for p in procs:
+        try:
+            out, e = p.communicate(timeout=900)
+        except subprocess.TimeoutExpired:
+            p.kill()
+            out, e = p.communicate()
+        if p.returncode == 0:
+            vals.append(json.loads(out.strip().splitlines()[-1])["value"])
+        else:
+            err = (e or "")[-400:]
+    if len(vals) != n:
+        return {"value": None, "unit": "tok/s", "cores": n, "kind": "oracle", "error": err}
+    return {"value": float(sum(vals)), "unit": "tok/s", "cores": n, "kind": "oracle",
+            "sample": "%d concurrent single-threaded oracle processes, each on its own seeded sample of the "
+                      "workload (the single-thread sample); value = the sum of their rates" % n}
+
+
+def cpu_baseline(workload):
+    """The oracle in a child process restricted to one thread (so `cores` is exact), then on every
+    host core (oracle_all_cores)."""
+    r = subprocess.run(_oracle_cmd(workload, 0), capture_output=True, text=True, env=_oracle_env(), timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["value"], "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": d["sample"],
-            "seconds_measured": d["seconds_measured"], "parts_s": d["parts_s"]}
+    out = {"value": d["value"], "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": d["sample"],
+           "seconds_measured": d["seconds_measured"], "parts_s": d["parts_s"]}
+    w = si.WORKLOADS[workload]
+    # float64 dequantised K and V of the whole context, plus the sampled rows' score matrices
+    gb = 2.0 + 2 * w.n_ctx * w.n_head_kv * w.head_dim * 8 * 3 / 1e9
+    try:
+        out["all_cores"] = oracle_all_cores(workload, gb)
+    except Exception as e:   # the single-thread figure stands on its own
+        out["all_cores"] = {"value": None, "error": repr(e)[-400:]}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -732,10 +798,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--npl", default="", help="also time batched decode for these sequence counts, e.g. 1,2,4,8")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-offset", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
 
     if args.oracle_child:
-        print(json.dumps(oracle_sample(si.WORKLOADS[args.workload])))
+        print(json.dumps(oracle_sample(si.WORKLOADS[args.workload], sample_offset=args.oracle_offset)))
         return
     rank, world, local = dist_init()
     if args.impl == "reference":
