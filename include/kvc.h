@@ -33,11 +33,13 @@
  *     working context, PR #58 section "Memory"; PR #59 section "What this
  *     adds").  Errors of asynchronous work surface at the caller's next
  *     synchronisation; the kernels contain no unbounded waits.
- *   - Kernels are launched with programmatic dependent launch: one may be
- *     scheduled while the kernel before it on `stream` is finishing, and it
- *     waits on the device (griddepcontrol.wait) for that kernel to complete
- *     before it reads or writes memory.  Stream order therefore holds exactly
- *     as for ordinary launches, also inside a captured CUDA graph.
+ *   - The append, prefill attention (and its split merge) and decode kernels
+ *     are launched with programmatic dependent launch: one may be scheduled
+ *     while the kernel before it on `stream` is finishing, and it waits on the
+ *     device (griddepcontrol.wait) for that kernel to complete before it reads
+ *     or writes memory.  Stream order therefore holds exactly as for ordinary
+ *     launches, also inside a captured CUDA graph.  The state kernels and the
+ *     q8_0 prefill's dequantising pass are ordinary launches.
  *
  * Cache contents.  A cache holds n_layer layers of n_ctx positions of
  * n_head_kv heads of head_dim values, for K and for V.  Cache types:
