@@ -65,6 +65,7 @@ def _load():
         "kv_cache_append_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, VP, I32, VP]),
         "kv_state_get_heads": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, SZ, VP]),
         "kv_state_set_heads": (ctypes.c_int, [P(kvc_cache), I32, VP, SZ, P(I32), VP]),
+        "kvc_test_arm_wait_timeout": (ctypes.c_int, [I32, ctypes.c_uint64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -317,7 +318,19 @@ def kv_cache_truncate(cache, n_tokens, stream=None):
 
 
 def kvc_device_status():
-    """Synchronise and read/clear the device status word (non-zero: a kernel gave up a bounded wait)."""
+    """Synchronise and read/clear the device status word (non-zero: a kernel gave up a bounded wait,
+    which the C call reports as KVC_EDEVICE)."""
     s = ctypes.c_int32(0)
-    _check(_lib().kvc_device_status(ctypes.byref(s)), "kvc_device_status")
+    rc = _lib().kvc_device_status(ctypes.byref(s))
+    if rc != KVC_EDEVICE:
+        _check(rc, "kvc_device_status")
     return s.value
+
+
+TEST_PREFILL, TEST_DECODE = 0, 1
+
+
+def arm_test_wait_timeout(which, limit_ns):
+    """Test hook: the next launch of the prefill (TEST_PREFILL) or head_dim-128 decode (TEST_DECODE)
+    tensor-core kernel waits on a barrier nothing arrives at, gives up after limit_ns and unwinds."""
+    _check(_lib().kvc_test_arm_wait_timeout(which, limit_ns), "kvc_test_arm_wait_timeout")

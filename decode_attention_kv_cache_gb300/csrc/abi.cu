@@ -9,11 +9,20 @@
 // caller keeps a working context).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "kvc_internal.h"
 
 using namespace kvc;
+
+namespace kvc {
+namespace {
+std::atomic<uint64_t> g_test_stall[2];   // per kernel kind: wait limit of the armed stall, 0 = none
+}  // namespace
+void arm_test_stall(int which, uint64_t limit_ns) { g_test_stall[which].store(limit_ns); }
+uint64_t take_test_stall(int which) { return g_test_stall[which].exchange(0); }
+}  // namespace kvc
 
 namespace {
 
@@ -31,6 +40,17 @@ bool desc_ok(const kvc_desc *d) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// True when p is device memory of the current device (or managed memory the runtime attributes to it).
+bool on_current_device(const void *p) {
+    int dev = -1;
+    cudaPointerAttributes at;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();   // a failed query leaves no sticky error behind
+        return false;
+    }
+    return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
+}
 
 bool cache_ok(const kvc_cache *c) {
     if (!c || !desc_ok(&c->d)) return false;
@@ -165,6 +185,8 @@ int decode_attn_noalloc(const kvc_cache *cache, int32_t layer, int32_t pos, cons
     size_t need = 0;
     kvc_scratch_bytes(&cache->d, n_head_q, &need);
     if (need > decode_noalloc_capacity()) return KVC_ENOSPC;  // more partials than the fixed array holds
+    // the partials go to the current device's array: the cache and the output must live there too
+    if (!on_current_device(cache->k_q) || !on_current_device(out)) return KVC_EINVAL;
     return launch_decode_noalloc(*cache, layer, pos, q, dtype, n_head_q, out, (cudaStream_t)stream);
 }
 
@@ -294,7 +316,15 @@ const char *kvc_strerror(int status) {
 
 int kvc_device_status(int32_t *status) {
     if (!status) return KVC_EINVAL;
-    return read_and_clear_device_status(status);
+    const int rc = read_and_clear_device_status(status);
+    if (rc != KVC_OK) return rc;
+    return *status != 0 ? KVC_EDEVICE : KVC_OK;
+}
+
+int kvc_test_arm_wait_timeout(int32_t which, uint64_t limit_ns) {
+    if (which != KVC_TEST_PREFILL && which != KVC_TEST_DECODE) return KVC_EINVAL;
+    arm_test_stall(which, limit_ns);
+    return KVC_OK;
 }
 
 }  // extern "C"

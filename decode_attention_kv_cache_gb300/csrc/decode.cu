@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "kvc_internal.h"
@@ -123,6 +124,7 @@ struct DecodeArgs {
     Geom g;
     int layer, n_keys, group, split_len, n_split, n_head_kv;
     float scale_log2;
+    uint64_t stall_ns;   // test hook (tensor-core pass): > 0 makes the MMA thread's first P wait one that runs out
 };
 
 // Several sequences decoded by one launch: each has its own cache (and so its own tensor maps),
@@ -620,10 +622,11 @@ struct TCfg {
 };
 
 enum TcBar {
-    T_QREADY, T_SFULL0, T_SFULL1, T_PFULL0, T_PFULL1, T_ODONE0, T_ODONE1, T_XCHG, T_DRAIN,
+    T_QREADY, T_SFULL0, T_SFULL1, T_PFULL0, T_PFULL1, T_ODONE0, T_ODONE1, T_XCHG, T_DRAIN, T_STALL,
     T_KFULL, T_KEMPTY = T_KFULL + 4, T_VFULL = T_KEMPTY + 4, T_VEMPTY = T_VFULL + 4, T_RFULL = T_VEMPTY + 4,
     T_REMPTY = T_RFULL + 4, T_NBAR = T_REMPTY + 4
 };
+static_assert(T_NBAR * 8 + 8 <= 512, "barrier area too small");
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
     uint32_t u[16];
@@ -704,6 +707,7 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
         }
         mbar_init(&bars[T_XCHG], 128);
         mbar_init(&bars[T_DRAIN], 1);
+        mbar_init(&bars[T_STALL], 1);   // nothing arrives here: only the test hook waits on it
         for (int s = 0; s < L::NK; ++s) {
             mbar_init(&bars[T_KFULL + s], Q8 ? L::NDQ : 1);
             mbar_init(&bars[T_KEMPTY + s], 1);
@@ -829,6 +833,13 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
                 commit_s(j);
             }
             for (int k = 0; ok && k < T; ++k) {
+                // test hook: a bounded wait on a barrier nothing arrives at, in place of the first P
+                // wait; it gives up after stall_ns (raising the abort flag) with S MMAs in flight
+                if (a.stall_ns != 0 && k == 0) {
+                    mbar_wait(&bars[T_STALL], 0, s_abort, a.stall_ns);
+                    ok = false;
+                    break;
+                }
                 if (!mbar_wait(&bars[T_PFULL0 + (k & 1)], (k >> 1) & 1, s_abort)) { ok = false; break; }
                 const int vs = k % L::NV;
                 if (!mbar_wait(&bars[T_VFULL + vs], (k / L::NV) & 1, s_abort)) { ok = false; break; }
@@ -968,6 +979,7 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
             mbar_arrive(&bars[T_PFULL0 + (k & 1)]);
         }
         // ---- epilogue: this split's (m, l, O) per head of the group
+        bool wrote = false;
         if (ok && T > 0 && wait_pv(T - 1)) {
             float o[NH], o_hi[NH];
             tmem_ld16(tmem + COL_O + lane_base, o);
@@ -1003,7 +1015,16 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
                     part_ml[(pbase + L0) * 2] = mv;
                     part_ml[(pbase + L0) * 2 + 1] = ((w4.x + w4.y) + w4.z) + w4.w;
                 }
+                wrote = true;
             }
+        }
+        if (!wrote && L0 < G) {
+            // a split that gave up leaves an empty partial (m = -inf, l = 0), which the combine
+            // weighs 0, rather than another call's leftovers
+            float *part_ml = a.part + (int64_t)a.n_head_kv * MAX_SPLIT * G * D;
+            const int64_t pi = ((int64_t)hkv * MAX_SPLIT + split) * G + L0;
+            part_ml[pi * 2] = -INFINITY;
+            part_ml[pi * 2 + 1] = 0.f;
         }
     } else if constexpr (Q8) {
         // ------------------------------------------------------------------ dequantise (q8_0)
@@ -1134,6 +1155,8 @@ int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_he
         cb.n_split[i] = n_split;
         if (n_split > max_split) max_split = n_split;
     }
+    const uint64_t stall_ns = take_test_stall(KVC_TEST_DECODE);
+    for (int i = 0; i < n_seq; ++i) b.a[i].stall_ns = stall_ns;
     const int group = a0[0].group, n_head_kv = a0[0].n_head_kv;
     auto kern = group <= 8 ? decode_tc_kernel<Q8, DT, 8, NS> : decode_tc_kernel<Q8, DT, 16, NS>;
     if (allow_dynamic_smem((const void *)kern, L::ALLOC) != KVC_OK) return KVC_ECUDA;
@@ -1177,6 +1200,7 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
     a.n_head_kv = c.d.n_head_kv;
     a.group = n_head_q / c.d.n_head_kv;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
+    a.stall_ns = 0;
     if constexpr (D == 128) {
         return launch_tc<Q8, DT, 1>(&c, &a, 1, n_head_q, &out, s);
     } else {
@@ -1255,22 +1279,53 @@ int launch_d(const kvc_cache &c, int layer, int pos, const void *q, int dtype, i
 constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)8 << 20;  // 8 MiB
 static __device__ __align__(256) float g_noalloc_scratch[NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
-// The array's device address on the current device.  In host code the symbol
-// name is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) through cudaGetSymbolAddress and cached.
-int noalloc_scratch_address(float **out) {
-    constexpr int MAX_DEVICES = 64;
-    static std::mutex mu;
-    static float *addr[MAX_DEVICES] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KVC_ECUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+// The context the calling thread has current, by its process-unique id (cuCtxGetId, fetched through the
+// runtime like the tensor-map encoder, so the library links no libcuda); 0 when there is none yet.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KVC_ECUDA;
-        addr[dev] = static_cast<float *>(p);
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// The array's device address in the calling thread's current context.  In host code the symbol
+// name is only a host-side stand-in, so the address is looked up through cudaGetSymbolAddress
+// with the device current, once per context, and cached under the context's id: a context
+// created again after a reset of the device (which may place the array elsewhere) has a new id
+// and gets a fresh lookup.
+int noalloc_scratch_address(float **out) {
+    static std::mutex mu;
+    static std::map<unsigned long long, float *> addr;   // context id -> address
+    std::lock_guard<std::mutex> lock(mu);
+    const unsigned long long id = current_context_id();
+    if (id != 0) {
+        auto it = addr.find(id);
+        if (it != addr.end()) {
+            *out = it->second;
+            return KVC_OK;
+        }
     }
-    *out = addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KVC_ECUDA;
+    const unsigned long long id2 = current_context_id();   // the lookup may have made the context current
+    if (id2 != 0) addr[id2] = static_cast<float *>(p);
+    *out = static_cast<float *>(p);
     return KVC_OK;
 }
 
@@ -1322,6 +1377,7 @@ int launch_batch_t(const kvc_cache *caches, int n_seq, int layer, const int *pos
         a[i].group = n_head_q / c.d.n_head_kv;
         a[i].split_len = a[i].n_split = 0;
         a[i].scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
+        a[i].stall_ns = 0;
         outs[i] = out + (size_t)i * n_head_q * D;
     }
     return launch_tc<Q8, DT, MAX_BATCH>(caches, a, n_seq, n_head_q, outs, s);

@@ -67,6 +67,11 @@ int launch_state_pack_heads(const kvc_cache &c, int head0, int H_total, int n_to
 int launch_state_unpack_heads(const kvc_cache &c, int head0, int H_total, int n_tokens, const uint8_t *src,
                               cudaStream_t s);
 
+// Test hook of the failure path: the wait limit (ns) of a stall armed for the next launch of a kernel
+// kind (KVC_TEST_PREFILL / KVC_TEST_DECODE), 0 when none; take_ consumes it.
+void arm_test_stall(int which, uint64_t limit_ns);
+uint64_t take_test_stall(int which);
+
 // Device status word set by kernels that give up a bounded wait (all kernels' words, read and cleared).
 int read_and_clear_device_status(int32_t *status);
 int read_and_clear_decode_status(int32_t *status);

@@ -106,7 +106,7 @@ struct Cfg {
 };
 
 enum Bar {
-    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN,
+    B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN, B_STALL,
     B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
     B_RAW_EMPTY = B_RAW_FULL + 8, NBAR = B_RAW_EMPTY + 8
 };
@@ -121,6 +121,7 @@ struct Args {
     int layer, pos0, C, kv_len, H_q, G, H_kv, n_qt, ST, smax, n_items;
     int v8;                    // out and part are 32-byte aligned: rows are stored 32 bytes at a time
     float scale_log2;
+    uint64_t stall_ns;         // test hook: > 0 makes the MMA thread's first P wait one that runs out
     int cum[MAX_SPLITS + 1];   // items before split index s
     int qtmin[MAX_SPLITS];     // first q-tile whose keys reach split s
 };
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         // mailbox words start with flag bit 1: the first value written to each slot carries flag 0
         for (int i = 0; i < 2 * 2 * BM; ++i) reinterpret_cast<uint32_t *>(sm + L::OFF_RED)[i] = 1u;
         mbar_init(&bars[B_DRAIN], 1);
+        mbar_init(&bars[B_STALL], 1);   // nothing arrives here: only the test hook waits on it
         for (int s = 0; s < L::NS; ++s) {
             mbar_init(&bars[B_RING_FULL + s], Q8 ? 128 : 1);
             mbar_init(&bars[B_RING_EMPTY + s], 1);
@@ -366,6 +368,13 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                     if (k + 1 < it.k1) {
                         if (!issue_s()) { ok = false; break; }
                         if (k + 2 == it.k1) umma_commit(&bars[B_QEMPTY]);
+                    }
+                    // test hook: a bounded wait on a barrier nothing arrives at, in place of the first
+                    // P wait; it gives up after stall_ns (raising the abort flag) with S MMAs in flight
+                    if (a.stall_ns != 0 && p_seq == 0) {
+                        mbar_wait(&bars[B_STALL], 0, s_abort, a.stall_ns);
+                        ok = false;
+                        break;
                     }
                     // an item's first PV starts a new O: the softmax has read the previous one out of TMEM
                     // before it signals that P is ready
@@ -856,6 +865,7 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     a.smax = p.smax;
     a.n_items = p.n_items;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
+    a.stall_ns = take_test_stall(KVC_TEST_PREFILL);
     for (int i = 0; i <= MAX_SPLITS; ++i) a.cum[i] = i <= p.smax ? p.cum[i] : p.n_items;
     for (int i = 0; i < MAX_SPLITS; ++i) a.qtmin[i] = i < p.smax ? p.qtmin[i] : p.n_qt;
     auto kern = prefill_kernel<D, Q8, QDT>;

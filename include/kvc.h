@@ -237,12 +237,17 @@ int decode_attn_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, con
  * the process exits): calls whose kvc_scratch_bytes(desc, n_head_q) exceeds
  * 8 MiB (n_head_q * 256 * (head_dim + 2) * 4 bytes, i.e. n_head_q > 63 at
  * head_dim 128) are rejected with KVC_ENOSPC before anything is launched.
- * The call allocates nothing.  Its first call on a device looks up that
- * array's device address (cudaGetSymbolAddress) with the device current;
- * make that first call before capturing a stream into a CUDA graph.  All
- * calls share the one array: calls that overlap on the GPU (other streams,
- * other threads) race and must be serialised by the caller.  Arguments,
- * result and errors otherwise as decode_attn. */
+ * The call allocates nothing.  Its first call in a device's context looks up
+ * that array's device address (cudaGetSymbolAddress) with the device current
+ * and caches it under the context's id, so a context created again after a
+ * device reset gets a fresh lookup; make that first call before capturing a
+ * stream into a CUDA graph.  The cache, q, out and the stream must belong to
+ * the current device: a cache or output on another device is rejected with
+ * KVC_EINVAL.  All calls share the one array: calls that overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.
+ * When kvc_device_status() reports a non-zero status after a call, that
+ * call's out is undefined.  Arguments, result and errors otherwise as
+ * decode_attn. */
 int decode_attn_noalloc(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, int32_t dtype,
                         int32_t n_head_q, float *out, kvc_stream_t stream);
 
@@ -307,9 +312,27 @@ int kv_cache_truncate(const kvc_cache *cache, int32_t n_tokens, kvc_stream_t str
 const char *kvc_strerror(int status);
 
 /* Synchronise the current device, then read and clear the device-side status
- * word that kernels set when a bounded wait gives up (0 = none).  Returns
- * KVC_ECUDA if the synchronisation fails. */
+ * word that kernels set when a bounded wait gives up (0 = none) into *status.
+ * Returns KVC_OK when the word was 0, KVC_EDEVICE when a kernel gave up a wait
+ * since the last read (the outputs of that call are undefined; the cache, the
+ * context and later calls stay usable), KVC_ECUDA if the synchronisation
+ * fails. */
 int kvc_device_status(int32_t *status);
+
+/* Test hook for the failure path.  Arms one bounded wait that nothing will
+ * satisfy in the next launch of the chosen tensor-core kernel on any device:
+ * which = KVC_TEST_PREFILL (the prefill attention pass, head_dim 64 or 128) or
+ * KVC_TEST_DECODE (the decode split pass for head_dim 128).  In that launch the
+ * thread that issues the MMAs waits on a barrier nothing arrives at, in place
+ * of its first wait for a softmax tile; after limit_ns the wait gives up, as
+ * any bounded wait does, and every CTA unwinds: the TMA copies and MMAs in
+ * flight are let finish, tensor memory is freed, the kernel returns and
+ * kvc_device_status reports KVC_EDEVICE.  limit_ns = 0 disarms.  One launch
+ * consumes the arm.  The pages define no such call: it exists so that a test
+ * can show a wait that gives up leaves a usable context. */
+#define KVC_TEST_PREFILL 0
+#define KVC_TEST_DECODE 1
+int kvc_test_arm_wait_timeout(int32_t which, uint64_t limit_ns);
 
 #ifdef __cplusplus
 }
