@@ -578,85 +578,97 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS
 }
 
 // ---- tensor-core split pass for head_dim 128 ---------------------------------------------
-// Tiles of 128 keys.  S^T = K Q^T with M = 128 keys, N = 16 (the G query heads of the group,
-// zero-padded), both operands in shared memory; O^T += V^T P^T with M = 128 head-dim rows, N = 16,
-// V as an MN-major operand and P^T written to shared memory by the softmax threads.  Accumulators
-// live in tensor memory (S double-buffered), so the warps hold no MMA state.  A chain of dependent
-// N = 16 MMAs advances about one step per 220 cycles, while independent chains issued interleaved
-// overlap (MMAs of one kind: interleaving S and PV steps costs more than it saves); so S is
-// accumulated as two partial sums (head-dim halves) and O^T as two (key halves of each tile), and the
-// MMA issuer interleaves the two chains of each.
-//   warp 0      TMA producer: K and V tiles (f16) or their int8 codes (q8_0)
-//   warp 1      allocates TMEM; one lane issues the MMAs: S(0), S(1), then per tile PV(k), S(k+2)
-//   warps 2-5   softmax: thread = key of the tile (TMEM lane); per-head tile maxima are combined
-//               across the four warps through shared memory; P^T to shared memory; O^T rescaled
-//               (thread = head-dim row) when a running max grows by more than 2^8
-//   warps 6-9   (q8_0) dequantise K and V rows into fp16 d*q, separate K and V rings (one thread
-//               per key row; NDQ = 256 gives two per row, one per head-dim half)
+// Measured on this part: one thread issues a tcgen05.mma about every 90 cycles whatever its N (16 to
+// 128), MMAs that accumulate into the same tensor-memory columns advance only about one per 200
+// cycles, and two issuing threads run side by side.  So the pass has two MMA issuers and keeps its
+// dependent chains short.  Per key tile (128 keys):
+//   S  = Q' K^T      M = 128 rows, N = 128 keys, two chains of 4 MMAs (head dims [0, 64) and
+//                    [64, 128)), A = Q' and B = K in shared memory (both K-major); the softmax adds them
+//   O' += P' V       M = 128 rows, N = 256, K = 64: 4 MMAs, A = P' and B = V in shared memory (V
+//                    MN-major) with the tile's two 64-key halves side by side along N
+// Q' holds the G query heads of the group (head slots 0..15, slots >= G zero) eight times over:
+// row r = 16 rep + h.  Replica rep owns the 16 keys 16 rep .. 16 rep + 15 of every tile; the thread
+// on TMEM lane r keeps the online softmax of row r over those keys alone (its own running max m and
+// sum l), so no exchange between threads is needed per tile.  P' row r holds that thread's
+// probabilities at its keys' positions within their half and zeros elsewhere (cleared once at the
+// start, never written there again), so O' row r accumulates exactly its keys: the columns of the
+// row's own half (0..127 for keys 0..63, 128..255 for keys 64..127) hold sum_j p_j V_j, the other
+// half is unused.  At the end the eight rows of each head are merged (in replica order) into the
+// split's (m, l, O) partial.  A thread rescales its own O' row when its running max grows by more
+// than 2^8.
+//   warp 0      one lane copies the group's query rows (one bulk copy, first in the queue), then loads
+//               K tiles (f16) or their int8 codes (q8_0) by TMA
+//   warp 1      allocates TMEM; one lane issues S(k + 1) once the softmax has read S(k)
+//   warp 2      one lane issues PV(k) once P'(k) and V(k) are ready
+//   warp 3      one lane loads V tiles or codes by TMA (K and V run ahead independently)
+//   warps 4-7   softmax, thread = TMEM lane = row of Q' / P' / O'; they also build Q' and merge
+//   warps 8-11  (q8_0) dequantise K rows in place into fp16 d*q, one thread per key row
+//   warps 12-15 (q8_0) the same for V rows
 constexpr int TK = 128;                 // keys per tile
-constexpr int NH = 16;                  // MMA N: query heads of a group, padded
-// TMEM: S buffer b, half hh at column 32 b + 16 hh; O^T part hh at COL_O + 16 hh
-constexpr uint32_t TC_COLS = 128;
-constexpr uint32_t COL_O = 64;
+constexpr int TKH = TK / 2;             // keys per half tile (the PV contraction)
+// TMEM columns: S chain 0 (head dims [0, 64)) [0, 128), chain 1 [128, 256), O' [256, 512)
+constexpr uint32_t TC_COLS = 512;
+constexpr uint32_t COL_S = 0, COL_O = 256;
 constexpr float TC_RESCALE_LOG2 = 8.0f;
 
-template <bool Q8>
+// HS: head slots per replica (8 when the group has at most 8 query heads, else 16).  With 8 slots a
+// replica is exactly one 8-row group of the 128-byte-swizzled Q' operand, so Q' is stored once (8 rows)
+// and the S MMA reads it for every replica with a zero stride between row groups; the 30 KB saved buy a
+// third V slot (V's refill waits for the PV of two tiles before, the longest wait of the pipeline).
+template <bool Q8, int HS>
 struct TCfg {
     static constexpr int D = 128;
-    static constexpr int OPT = TK * D * 2;                 // one fp16 K or V tile: 32 KB
-    static constexpr int RAWT = 2 * TK * D;                // int8 K and V codes of a tile: 32 KB
-    static constexpr int NK = Q8 ? 2 : 3, NV = Q8 ? 2 : 3, NR = Q8 ? 2 : 0;
-    static constexpr int OFF_K = 0;
+    static constexpr int NREP = 128 / HS;                   // row replicas of the query heads
+    static constexpr int RKEYS = TK / NREP;                 // keys of a tile each row owns (= HS)
+    static constexpr int QROWS = HS == 8 ? 8 : 128;         // Q' rows stored
+    static constexpr int QB = QROWS * D * 2;                // Q' operand: [64-dim block][QROWS][128 B]
+    static constexpr int QBLK = QROWS * 128;                // bytes of one 64-dim block of Q'
+    static constexpr int OPT = TK * D * 2;                  // fp16 K tile [64-dim block][128 keys][128 B], or
+                                                            // V tile [half][64-dim block][64 keys][128 B]
+    static constexpr int PB = 128 * TKH * 2;                // P' operand: [128 rows][64 keys], 16 KB
+    static constexpr int NP = HS == 8 ? 1 : 2;              // P' buffers
+    static constexpr int RAWB = TK * D;                     // int8 codes of a K or V tile: 16 KB
+    static constexpr int NK = 3, NV = HS == 8 ? 3 : 2;      // ring slots; q8_0 codes land in place
+    static constexpr int QSB = HS == 8 ? 8 * D * 4 : 0;     // staging of the query rows (else P' buffer 1)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + QB;
     static constexpr int OFF_V = OFF_K + NK * OPT;
-    static constexpr int OFF_RAW = OFF_V + NV * OPT;
-    static constexpr int OFF_QT = OFF_RAW + NR * RAWT;      // Q^T operand: 16 rows x 128, 4 KB
-    static constexpr int OFF_PT = OFF_QT + NH * D * 2;      // two P^T operands: 16 rows x 128 keys
-    static constexpr int OFF_RED = OFF_PT + 2 * NH * TK * 2;  // [parity][warp][head] floats
-    static constexpr int OFF_BAR = OFF_RED + 2 * 4 * NH * 4;
+    static constexpr int OFF_P = OFF_V + NV * OPT;
+    static constexpr int OFF_QS = HS == 8 ? OFF_P + NP * PB : OFF_P + PB;
+    static constexpr int OFF_BAR = OFF_P + NP * PB + QSB;
     static constexpr int USED = OFF_BAR + 512;
     static constexpr int ALLOC = USED + 1024;
     static_assert(ALLOC <= 232448, "shared memory plan too large");
-    static constexpr int NDQ = 128;                         // dequantising threads (q8_0): 1 or 2 per key
-    static constexpr int THREADS = Q8 ? 192 + NDQ : 192;
-    static constexpr int CTAS = 1;                          // CTAs per SM
+    // the merge at the end reuses the K ring (128 rows of 128 floats) and P' buffer 0 (m and l)
+    static constexpr int OFF_MRG = OFF_K;
+    static constexpr int OFF_ML = OFF_P;
+    static_assert(128 * D * 4 <= NK * OPT && 128 * 8 <= PB, "merge area must fit in the freed buffers");
+    static constexpr int NDQ = 128;                         // dequantising threads per K or V (q8_0)
+    static constexpr int THREADS = Q8 ? 512 : 256;
+    static constexpr int CTAS = 1;                          // CTAs per SM (all 512 TMEM columns)
 };
 
+// q8_0 codes land inside the fp16 slot they are dequantised into, at the bytes of the fp16 row's first
+// 64-dim block: K codes as one 128-key box at the slot's start (code row t at t * 128), V codes as two
+// 64-key boxes at the starts of the blocks (half 0, dims 0-63) and (half 1, dims 0-63).  A thread reads
+// its whole code row before it writes its fp16 row, whose first block covers exactly those bytes and
+// whose second block lies where no codes are, so no thread overwrites another thread's codes.
 enum TcBar {
-    T_QREADY, T_SFULL0, T_SFULL1, T_PFULL0, T_PFULL1, T_ODONE0, T_ODONE1, T_XCHG, T_DRAIN, T_STALL,
-    T_KFULL, T_KEMPTY = T_KFULL + 4, T_VFULL = T_KEMPTY + 4, T_VEMPTY = T_VFULL + 4, T_RFULL = T_VEMPTY + 4,
-    T_REMPTY = T_RFULL + 4, T_NBAR = T_REMPTY + 4
+    T_QREADY, T_QRAW, T_SFULL, T_SFREE, T_PFULL0, T_PFULL1, T_ODONE0, T_ODONE1, T_XCHG, T_DRAIN, T_DRAIN2, T_STALL,
+    T_KFULL, T_KEMPTY = T_KFULL + 4, T_VFULL = T_KEMPTY + 4, T_VEMPTY = T_VFULL + 4, T_KRAW = T_VEMPTY + 4,
+    T_VRAW = T_KRAW + 4, T_NBAR = T_VRAW + 4
 };
 static_assert(T_NBAR * 8 + 8 <= 512, "barrier area too small");
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
-    uint32_t u[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
-          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
-        : "r"(taddr));
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
-}
-__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(__float_as_uint(r[0])), "r"(__float_as_uint(r[1])), "r"(__float_as_uint(r[2])), "r"(__float_as_uint(r[3])),
-        "r"(__float_as_uint(r[4])), "r"(__float_as_uint(r[5])), "r"(__float_as_uint(r[6])), "r"(__float_as_uint(r[7])),
-        "r"(__float_as_uint(r[8])), "r"(__float_as_uint(r[9])), "r"(__float_as_uint(r[10])), "r"(__float_as_uint(r[11])),
-        "r"(__float_as_uint(r[12])), "r"(__float_as_uint(r[13])), "r"(__float_as_uint(r[14])), "r"(__float_as_uint(r[15]))
-        : "memory");
-}
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    umma_f16_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
-}
 // byte offset of 16-byte chunk c of row r in a 128-byte-swizzled block of 128-byte rows
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+// the fp16 K tile: head dims [64 cb, 64 cb + 64) of key row r, chunk c (8 dims) of that block
+__device__ __forceinline__ uint32_t k_off(int r, int cb, int c) { return (uint32_t)(cb * (TK * 128)) + sw128(r, c); }
+// the fp16 V tile: key row r lies in half r / 64 at row r % 64
+__device__ __forceinline__ uint32_t v_off(int r, int cb, int c) {
+    return (uint32_t)((2 * (r / TKH) + cb) * (TKH * 128)) + sw128(r % TKH, c);
 }
 // 4 int8 codes times the fp16 scale, as two fp16x2 words (one rounding each): the sign bit flipped
 // makes each code q + 128 as an unsigned byte, which under the high byte 0x64 is the fp16 value
@@ -671,13 +683,36 @@ __device__ __forceinline__ void dequant4(uint32_t w, __half2 d2, uint32_t &lo, u
     lo = *reinterpret_cast<uint32_t *>(&ra);
     hi = *reinterpret_cast<uint32_t *>(&rb);
 }
+// 8 query values (chunk i of the loaded 16-byte words) as fp32
+template <int DT, int N>
+__device__ __forceinline__ void to_f32x8(const uint4 (&raw)[N], int i, float (&x)[8]) {
+    if constexpr (DT == KVC_IN_F32) {
+        const uint4 a = raw[2 * i], b = raw[2 * i + 1];
+        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y); x[2] = __uint_as_float(a.z);
+        x[3] = __uint_as_float(a.w); x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+        x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+    } else {
+        const uint4 u = raw[i];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (DT == KVC_IN_BF16) {
+                x[2 * e] = __uint_as_float(w[e] << 16);
+                x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            } else {
+                x[2 * e] = __half2float(__ushort_as_half((unsigned short)(w[e] & 0xFFFFu)));
+                x[2 * e + 1] = __half2float(__ushort_as_half((unsigned short)(w[e] >> 16)));
+            }
+        }
+    }
+}
 
-// GM: heads the softmax loops cover (8 when the group has at most 8 query heads, else 16)
 // NS: sequences of a batch the parameters hold (1, or MAX_BATCH for a batched call; grid z = sequence)
-template <bool Q8, int DT, int GM, int NS>
-__global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
+template <bool Q8, int DT, int NS, int HS>
+__global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ TcBatch<NS> b) {
-    using L = TCfg<Q8>;
+    using L = TCfg<Q8, HS>;
+    constexpr int NREP = L::NREP, RKEYS = L::RKEYS;
     constexpr int D = 128;
     const int seq = NS == 1 ? 0 : (int)blockIdx.z;
     const DecodeArgs &a = b.a[seq];
@@ -689,7 +724,6 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + T_NBAR);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
-    float *s_red = reinterpret_cast<float *>(sm + L::OFF_RED);
     const int split = blockIdx.x, hkv = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.group;
@@ -700,13 +734,16 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
     if (threadIdx.x == 0) {
         *s_abort = 0;
         mbar_init(&bars[T_QREADY], 128);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars[T_SFULL0 + b], 1);
-            mbar_init(&bars[T_PFULL0 + b], 128);
-            mbar_init(&bars[T_ODONE0 + b], 1);
+        mbar_init(&bars[T_QRAW], 1);
+        mbar_init(&bars[T_SFULL], 1);
+        mbar_init(&bars[T_SFREE], 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[T_PFULL0 + i], 128);
+            mbar_init(&bars[T_ODONE0 + i], 1);
         }
         mbar_init(&bars[T_XCHG], 128);
         mbar_init(&bars[T_DRAIN], 1);
+        mbar_init(&bars[T_DRAIN2], 1);
         mbar_init(&bars[T_STALL], 1);   // nothing arrives here: only the test hook waits on it
         for (int s = 0; s < L::NK; ++s) {
             mbar_init(&bars[T_KFULL + s], Q8 ? L::NDQ : 1);
@@ -716,12 +753,8 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
             mbar_init(&bars[T_VFULL + s], Q8 ? L::NDQ : 1);
             mbar_init(&bars[T_VEMPTY + s], 1);
         }
-        if constexpr (Q8) {
-            for (int s = 0; s < L::NR; ++s) {
-                mbar_init(&bars[T_RFULL + s], 1);
-                mbar_init(&bars[T_REMPTY + s], L::NDQ);
-            }
-        }
+        for (int s = 0; s < (Q8 ? L::NK : 0); ++s) mbar_init(&bars[T_KRAW + s], 1);
+        for (int s = 0; s < (Q8 ? L::NV : 0); ++s) mbar_init(&bars[T_VRAW + s], 1);
         fence_mbar_init();
         tma_prefetch_desc(tm_k);
         tma_prefetch_desc(tm_v);
@@ -738,123 +771,91 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ producer
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------------------------ producers (K: warp 0, V: warp 3)
+        // Each loads its tiles into ring slots as soon as the MMAs that read a slot's previous tile have
+        // completed; q8_0 codes complete on the slot's raw barrier (the dequantisers then fill the slot),
+        // fp16 values on its full barrier.  Warp 0 first copies the group's query rows (G x 128 values in
+        // the input type, contiguous) into a staging area, where the softmax threads build Q' from them.
         if (lane == 0) {
-            int kn = 0, vn = 0;   // tiles whose K (or raw) and V copies have been issued
+            const bool is_v = warp == 3;
+            const int n = is_v ? L::NV : L::NK;
+            const int bar_fill = is_v ? (Q8 ? T_VRAW : T_VFULL) : (Q8 ? T_KRAW : T_KFULL);
+            const int bar_empty = is_v ? T_VEMPTY : T_KEMPTY;
+            uint8_t *ring = sm + (is_v ? L::OFF_V : L::OFF_K);
+            bool q_issued = false;
+            if (!is_v) {
+                constexpr uint32_t QE = DT == KVC_IN_F32 ? 4 : 2;
+                const uint32_t qbytes = (uint32_t)G * D * QE;
+                mbar_arrive_expect_tx(&bars[T_QRAW], qbytes);
+                bulk_load(sm + L::OFF_QS, static_cast<const uint8_t *>(a.q) + (size_t)hkv * qbytes, qbytes,
+                          &bars[T_QRAW]);
+                q_issued = true;
+            }
+            int issued = 0;
             for (int k = 0; k < T; ++k) {
                 const int j = j_begin + k * TK;
+                const int s = k % n;
+                if (k >= n && !mbar_wait(&bars[bar_empty + s], ((k / n) - 1) & 1, s_abort)) break;
+                uint8_t *dst = ring + s * L::OPT;
                 if constexpr (Q8) {
-                    const int rs = k % L::NR;
-                    if (k >= L::NR && !mbar_wait(&bars[T_REMPTY + rs], ((k / L::NR) - 1) & 1, s_abort)) break;
-                    uint8_t *dst = sm + L::OFF_RAW + rs * L::RAWT;
-                    mbar_arrive_expect_tx(&bars[T_RFULL + rs], L::RAWT);
-                    tma_load_3d(dst, tm_k, &bars[T_RFULL + rs], 0, j, hkv);
-                    tma_load_3d(dst + TK * D, tm_v, &bars[T_RFULL + rs], 0, j, hkv);
-                    ++kn;
+                    mbar_arrive_expect_tx(&bars[bar_fill + s], L::RAWB);
+                    if (!is_v) {
+                        tma_load_3d(dst, tm_k, &bars[bar_fill + s], 0, j, hkv);
+                    } else {
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_3d(dst + v_off(hf * TKH, 0, 0), tm_v, &bars[bar_fill + s], 0, j + hf * TKH, hkv);
+                    }
                 } else {
-                    const int ks = k % L::NK, vs = k % L::NV;
-                    if (k >= L::NK && !mbar_wait(&bars[T_KEMPTY + ks], ((k / L::NK) - 1) & 1, s_abort)) break;
-                    mbar_arrive_expect_tx(&bars[T_KFULL + ks], L::OPT);
-                    for (int dh = 0; dh < 2; ++dh)
-                        tma_load_3d(sm + L::OFF_K + ks * L::OPT + dh * TK * 128, tm_k, &bars[T_KFULL + ks], dh * 64, j,
-                                    hkv);
-                    ++kn;
-                    if (k >= L::NV && !mbar_wait(&bars[T_VEMPTY + vs], ((k / L::NV) - 1) & 1, s_abort)) break;
-                    mbar_arrive_expect_tx(&bars[T_VFULL + vs], L::OPT);
-                    for (int dh = 0; dh < 2; ++dh)
-                        tma_load_3d(sm + L::OFF_V + vs * L::OPT + dh * TK * 128, tm_v, &bars[T_VFULL + vs], dh * 64, j,
-                                    hkv);
-                    ++vn;
+                    mbar_arrive_expect_tx(&bars[bar_fill + s], L::OPT);
+                    if (!is_v) {
+                        for (int cb = 0; cb < 2; ++cb)
+                            tma_load_3d(dst + k_off(0, cb, 0), tm_k, &bars[bar_fill + s], cb * 64, j, hkv);
+                    } else {
+                        for (int hf = 0; hf < 2; ++hf)
+                            for (int cb = 0; cb < 2; ++cb)
+                                tma_load_3d(dst + v_off(hf * TKH, cb, 0), tm_v, &bars[bar_fill + s], cb * 64,
+                                            j + hf * TKH, hkv);
+                    }
                 }
+                ++issued;
             }
             if (*s_abort) {
                 // after a wait gave up: let the copies still in flight land before the CTA exits
                 volatile int never = 0;
-                auto drain = [&](int first_bar, int stages, int n) {
-                    for (int st = 0; st < stages && st < n; ++st) {
-                        const int last = st + ((n - 1 - st) / stages) * stages;
-                        mbar_wait(&bars[first_bar + st], (last / stages) & 1, &never, 200000000ull);
-                    }
-                };
-                if constexpr (Q8) {
-                    drain(T_RFULL, L::NR, kn);
-                } else {
-                    drain(T_KFULL, L::NK, kn);
-                    drain(T_VFULL, L::NV, vn);
+                for (int st = 0; st < n && st < issued; ++st) {
+                    const int last = st + ((issued - 1 - st) / n) * n;
+                    mbar_wait(&bars[bar_fill + st], (last / n) & 1, &never, 200000000ull);
                 }
+                if (q_issued) mbar_wait(&bars[T_QRAW], 0, &never, 200000000ull);
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------------ S issuer
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_f16(128, NH, 0, 0);   // A = K (K-major), B = Q (K-major)
-            constexpr uint32_t IDESC_O = idesc_f16(128, NH, 1, 0);   // A = V^T (MN-major), B = P^T (K-major)
-            const uint32_t sK = smem_u32(sm + L::OFF_K), sV = smem_u32(sm + L::OFF_V);
-            const uint32_t sQ = smem_u32(sm + L::OFF_QT), sP = smem_u32(sm + L::OFF_PT);
+            constexpr uint32_t IDESC_S = idesc_f16(128, TK, 0, 0);      // A = Q' (K-major), B = K (K-major)
+            const uint32_t sQ = smem_u32(sm + L::OFF_Q), sK = smem_u32(sm + L::OFF_K);
             bool ok = mbar_wait(&bars[T_QREADY], 0, s_abort);
             tc_fence_after();
-            auto wait_k = [&](int j) -> bool {
-                if (!mbar_wait(&bars[T_KFULL + j % L::NK], (j / L::NK) & 1, s_abort)) return false;
-                tc_fence_after();
-                return true;
-            };
-            // step s (0..3) of both halves of S(j): head-dim k-steps s and 4 + s
-            auto s_mma = [&](int j, int s) {
-                const uint32_t kb = sK + (j % L::NK) * L::OPT;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int ks = 4 * hh + s;
-                    const uint32_t kk = (ks & 3) * 32;
-                    umma_ss(tmem + 32 * (j & 1) + 16 * hh, sdesc_sw128(kb + (ks >> 2) * (TK * 128) + kk, 16, 1024),
-                            sdesc_sw128(sQ + (ks >> 2) * (NH * 128) + kk, 16, 1024), IDESC_S, s > 0);
-                }
-            };
-            // step s of both key halves of PV(k): key k-steps s and 4 + s
-            auto pv_mma = [&](int k, int s) {
-                const uint32_t vb = sV + (k % L::NV) * L::OPT, pb = sP + (k & 1) * (NH * TK * 2);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int ks = 4 * hh + s;
-                    umma_ss(tmem + COL_O + 16 * hh, sdesc_sw128(vb + ks * 16 * 128, TK * 128, 1024),
-                            sdesc_sw128(pb + (ks >> 2) * (NH * 128) + (ks & 3) * 32, 16, 1024), IDESC_O,
-                            (k > 0 || s > 0) ? 1u : 0u);
-                }
-            };
-            auto commit_s = [&](int j) {
-                umma_commit(&bars[T_SFULL0 + (j & 1)]);
-                umma_commit(&bars[T_KEMPTY + j % L::NK]);
-            };
-            // S(0) and S(1) (S(1) into the other buffer), then per tile PV(k) with S(k + 2)
-            for (int j = 0; ok && j < 2 && j < T; ++j) {
-                if (!wait_k(j)) { ok = false; break; }
-#pragma unroll
-                for (int s = 0; s < 4; ++s) s_mma(j, s);
-                commit_s(j);
-            }
             for (int k = 0; ok && k < T; ++k) {
-                // test hook: a bounded wait on a barrier nothing arrives at, in place of the first P
-                // wait; it gives up after stall_ns (raising the abort flag) with S MMAs in flight
-                if (a.stall_ns != 0 && k == 0) {
-                    mbar_wait(&bars[T_STALL], 0, s_abort, a.stall_ns);
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(&bars[T_PFULL0 + (k & 1)], (k >> 1) & 1, s_abort)) { ok = false; break; }
-                const int vs = k % L::NV;
-                if (!mbar_wait(&bars[T_VFULL + vs], (k / L::NV) & 1, s_abort)) { ok = false; break; }
+                // S(k) into the S columns once every softmax thread has read S(k - 1)
+                if (k > 0 && !mbar_wait(&bars[T_SFREE], (k - 1) & 1, s_abort)) { ok = false; break; }
+                const int st = k % L::NK;
+                if (!mbar_wait(&bars[T_KFULL + st], (k / L::NK) & 1, s_abort)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t kb = sK + st * L::OPT;
+                // two independent chains, interleaved: head dims [0, 64) into columns [0, 128), [64, 128)
+                // into [128, 256); k-step i of chain c covers head dims 64 c + 16 i .. + 15
 #pragma unroll
-                for (int s = 0; s < 4; ++s) pv_mma(k, s);
-                umma_commit(&bars[T_ODONE0 + (k & 1)]);
-                umma_commit(&bars[T_VEMPTY + vs]);
-                // S(k + 2) reuses S(k)'s buffer, which the softmax read before publishing P(k)
-                if (k + 2 < T) {
-                    if (!wait_k(k + 2)) { ok = false; break; }
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) s_mma(k + 2, s);
-                    commit_s(k + 2);
-                }
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t qo = (uint32_t)(c * L::QBLK + i * 32), ko = (uint32_t)(c * (TK * 128) + i * 32);
+                        umma_f16_ss(tmem + COL_S + 128 * c, sdesc_sw128(sQ + qo, 16, HS == 8 ? 0 : 1024),
+                                    sdesc_sw128(kb + ko, 16, 1024), IDESC_S, i > 0);
+                    }
+                umma_commit(&bars[T_SFULL]);
+                umma_commit(&bars[T_KEMPTY + st]);
             }
             if (*s_abort) {
                 // after a wait gave up: let the MMAs in flight finish before TMEM is freed
@@ -864,242 +865,280 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ------------------------------------------------------------------ softmax
-        const int quarter = warp & 3;
-        const int L0 = quarter * 32 + lane;      // TMEM lane: key of the tile / head-dim row of O^T
+    } else if (warp == 2) {
+        // ------------------------------------------------------------------ PV issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_O = idesc_f16(128, 2 * D, 0, 1);   // A = P' (K-major), B = V (MN-major)
+            const uint32_t sP = smem_u32(sm + L::OFF_P), sV = smem_u32(sm + L::OFF_V);
+            bool ok = true;
+            for (int k = 0; ok && k < T; ++k) {
+                // test hook: a bounded wait on a barrier nothing arrives at, in place of the first P
+                // wait; it gives up after stall_ns (raising the abort flag) with S MMAs in flight
+                if (a.stall_ns != 0 && k == 0) {
+                    mbar_wait(&bars[T_STALL], 0, s_abort, a.stall_ns);
+                    ok = false;
+                    break;
+                }
+                // O' += P'(k) V(k): k-step ks covers keys [16 ks, 16 ks + 16) of both halves
+                if (!mbar_wait(&bars[T_PFULL0 + k % L::NP], (k / L::NP) & 1, s_abort)) { ok = false; break; }
+                const int vs = k % L::NV;
+                if (!mbar_wait(&bars[T_VFULL + vs], (k / L::NV) & 1, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t pb = sP + (k % L::NP) * L::PB, vb = sV + vs * L::OPT;
+#pragma unroll
+                for (int ks = 0; ks < TKH / 16; ++ks)
+                    umma_f16_ss(tmem + COL_O, sdesc_sw128(pb + ks * 32, 16, 1024),
+                                sdesc_sw128(vb + ks * 16 * 128, TKH * 128, 1024), IDESC_O, (k > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(&bars[T_ODONE0 + (k & 1)]);
+                umma_commit(&bars[T_VEMPTY + vs]);
+            }
+            if (*s_abort) {
+                volatile int never = 0;
+                umma_commit(&bars[T_DRAIN2]);
+                mbar_wait(&bars[T_DRAIN2], 0, &never, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------------ softmax (row per thread)
+        const int quarter = warp & 3;                   // this warp's TMEM lanes: 32 quarter .. + 31
+        const int r = quarter * 32 + lane;              // row of Q', P' and O'
+        const int rep = r / HS, h = r % HS;             // replica, head slot
+        const int hf = quarter >> 1;                    // the half of the tile its keys lie in
+        const int sub = lane / HS;                      // which of the warp's replicas (its 32 keys)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        // Q^T operand (rows >= G zero) and both P^T operands cleared (their rows >= G stay zero)
+        bool ok = true;
         {
-            uint8_t *qt = sm + L::OFF_QT;
-            const int h = L0 >> 3, c = L0 & 7;
+            // Q' row r (head slot h of the group, zero for h >= G; with 8 slots only rows 0-7 are stored)
+            // from the staged query rows; row r of P' buffer 0 cleared (with two buffers, buffer 1 held
+            // the staged rows and is cleared before its first use, once every thread has read them)
+            ok = mbar_wait(&bars[T_QRAW], 0, s_abort);
+            uint8_t *qt = sm + L::OFF_Q;
+            constexpr int QW = DT == KVC_IN_F32 ? 2 : 1;        // 16-byte words per 8 values
+            const uint8_t *qs = sm + L::OFF_QS + h * D * (DT == KVC_IN_F32 ? 4 : 2);
+#pragma unroll 4
+            for (int cc = 0; cc < (r < L::QROWS ? D / 8 : 0); ++cc) {
+                uint4 raw[QW];
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
+                for (int i = 0; i < QW; ++i)
+                    raw[i] = (ok && h < G) ? *reinterpret_cast<const uint4 *>(qs + (cc * QW + i) * 16)
+                                           : make_uint4(0u, 0u, 0u, 0u);
                 float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x[e] = h < G ? load_q<DT>(a.q, ((int64_t)hkv * G + h) * D + blk * 64 + c * 8 + e) : 0.f;
-                *reinterpret_cast<uint4 *>(qt + blk * (NH * 128) + sw128(h, c)) =
+                to_f32x8<DT>(raw, 0, x);
+                *reinterpret_cast<uint4 *>(qt + (cc >> 3) * L::QBLK + sw128(r, cc & 7)) =
                     make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
                                pack_half2(x[6], x[7]));
             }
-            uint4 *pt = reinterpret_cast<uint4 *>(sm + L::OFF_PT);
+            uint4 *prow = reinterpret_cast<uint4 *>(sm + L::OFF_P + r * 128);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) pt[L0 + 128 * i] = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < 8; ++c) prow[c] = make_uint4(0u, 0u, 0u, 0u);
             fence_proxy_async_smem();
             mbar_arrive(&bars[T_QREADY]);
         }
-        float m_run[GM], l_part[GM];
-#pragma unroll
-        for (int h = 0; h < GM; ++h) {
-            m_run[h] = -INFINITY;
-            l_part[h] = 0.f;
-        }
-        uint32_t x_seq = 0;
+        float m_run = -INFINITY, l_run = 0.f;
         int pv_seen[2] = {0, 0};
-        bool ok = true;
         auto wait_pv = [&](int j) -> bool {  // PV(j) and every MMA before it have completed
-            const int b = j & 1, n = j >> 1;
-            if (pv_seen[b] > n) return true;
-            if (!mbar_wait(&bars[T_ODONE0 + b], n & 1, s_abort)) return false;
-            pv_seen[b] = n + 1;
+            const int bb = j & 1, n = j >> 1;
+            if (pv_seen[bb] > n) return true;
+            if (!mbar_wait(&bars[T_ODONE0 + bb], n & 1, s_abort)) return false;
+            pv_seen[bb] = n + 1;
             tc_fence_after();
             return true;
         };
         const float sl2 = a.scale_log2;
-        for (int k = 0; k < T; ++k) {
-            if (!mbar_wait(&bars[T_SFULL0 + (k & 1)], (k >> 1) & 1, s_abort)) { ok = false; break; }
+        for (int k = 0; ok && k < T; ++k) {
+            if (!mbar_wait(&bars[T_SFULL], k & 1, s_abort)) { ok = false; break; }
             tc_fence_after();
-            float sc[NH], sc_hi[NH];
-            tmem_ld16(tmem + 32 * (k & 1) + lane_base, sc);
-            tmem_ld16(tmem + 32 * (k & 1) + 16 + lane_base, sc_hi);
+            // the warp's 32 key columns (its two replicas' keys) of both chains, then S may be overwritten
+            uint32_t s0[32], s1[32];
+            tmem_ld32(tmem + COL_S + 32 * quarter + lane_base, s0);
+            tmem_ld32(tmem + COL_S + 128 + 32 * quarter + lane_base, s1);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[T_SFREE]);
+            const int key0 = j_begin + k * TK + RKEYS * rep;   // absolute position of my first key
+            float x[RKEYS];
 #pragma unroll
-            for (int h = 0; h < NH; ++h) sc[h] += sc_hi[h];
-            const bool valid = j_begin + k * TK + L0 < j_end;
-            // branch-free over the 16 padded heads: heads >= G score -inf, offset 0, so p = 0 exactly
-            float x[GM];
+            for (int i = 0; i < RKEYS; ++i) {
+                // the warp's 32 columns hold its replicas' keys in order: mine are sub * RKEYS + i
+                float s = __uint_as_float(s0[i]) + __uint_as_float(s1[i]);
 #pragma unroll
-            for (int h = 0; h < GM; ++h) x[h] = (valid && h < G) ? sc[h] * sl2 : -INFINITY;
-            // per-head maximum over the warp (one warp reduction per head), then over the four warps;
-            // the four values of a head are adjacent ([head][warp]) and read as one 16-byte load
-            float *slot = s_red + (x_seq & 1) * 4 * NH;
-            {
-                float v = -INFINITY;
-#pragma unroll
-                for (int h = 0; h < GM; ++h) {
-                    float mx;
-                    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(x[h]));
-                    v = lane == h ? mx : v;
-                }
-                if (lane < GM) slot[lane * 4 + quarter] = v;
+                for (int q = 1; q < 32 / RKEYS; ++q)
+                    if (sub == q) s = __uint_as_float(s0[q * RKEYS + i]) + __uint_as_float(s1[q * RKEYS + i]);
+                x[i] = key0 + i < j_end ? s * sl2 : -INFINITY;
             }
-            mbar_arrive(&bars[T_XCHG]);
-            if (!mbar_wait(&bars[T_XCHG], x_seq & 1, s_abort)) { ok = false; break; }
-            ++x_seq;
-            bool rescale = false;
-            float alpha[GM];
+            float mx = fmax3(x[0], x[1], x[2]);
 #pragma unroll
-            for (int h = 0; h < GM; ++h) {
-                const float4 w4 = *reinterpret_cast<const float4 *>(slot + 4 * h);
-                const float M = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w));
-                // the split's first key is visible, so M is finite on the first tile for heads < G
-                const bool grow = k > 0 && M > m_run[h] + TC_RESCALE_LOG2;
-                alpha[h] = grow ? ex2(m_run[h] - M) : 1.f;
-                m_run[h] = (k == 0 || grow) ? M : m_run[h];
-                rescale |= grow;
+            for (int i = 3; i < RKEYS; i += 2) mx = fmax3(mx, x[i], i + 1 < RKEYS ? x[i + 1] : x[i]);
+            // lazy rescale: the running max moves only when it grows by more than 2^8 (a row that has
+            // seen no visible key yet takes the first maximum; its O' row is still zero)
+            float alpha = 1.f;
+            bool grow = false;
+            if (m_run == -INFINITY) {
+                m_run = mx;
+            } else if (mx > m_run + TC_RESCALE_LOG2) {
+                alpha = ex2(m_run - mx);
+                m_run = mx;
+                grow = true;
             }
-            float p[GM];
+            const float m_sub = m_run == -INFINITY ? 0.f : m_run;   // all keys masked so far: p = 0
+            uint32_t pk[RKEYS / 2];
+            float rs = 0.f;
 #pragma unroll
-            for (int h = 0; h < GM; ++h) {
-                const float m_sub = m_run[h] == -INFINITY ? 0.f : m_run[h];
-                p[h] = ex2(x[h] - m_sub);
-                l_part[h] = l_part[h] * alpha[h] + p[h];
+            for (int i = 0; i < RKEYS; i += 2) {
+                const float p0 = ex2(x[i] - m_sub), p1 = ex2(x[i + 1] - m_sub);
+                rs += p0 + p1;
+                pk[i / 2] = pack_half2(p0, p1);
             }
-            // P^T buffer k & 1 was last read by PV(k - 2); O^T must hold PV(k - 1) before a rescale
-            if (k >= 2 && !wait_pv(k - 2)) { ok = false; break; }
-            if (rescale && k >= 1) {
-                if (!wait_pv(k - 1)) { ok = false; break; }
+            l_run = l_run * alpha + rs;
+            // P' buffer k % NP was last read by PV(k - NP); O' must hold PV(k - 1) before a rescale
+            if (k >= L::NP && !wait_pv(k - L::NP)) { ok = false; break; }
+            if (__any_sync(0xffffffffu, grow)) {
+                if (k >= 1 && !wait_pv(k - 1)) { ok = false; break; }
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    const uint32_t ta = tmem + COL_O + 128 * hf + 32 * c + lane_base;
+                    tmem_ld32(ta, o);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float o[NH];
-                    tmem_ld16(tmem + COL_O + 16 * hh + lane_base, o);
-#pragma unroll
-                    for (int h = 0; h < GM; ++h) o[h] *= alpha[h];
-                    tmem_st16f(tmem + COL_O + 16 * hh + lane_base, o);
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(ta, o);
                 }
                 tmem_st_wait();
             }
-            uint8_t *pt = sm + L::OFF_PT + (k & 1) * (NH * TK * 2) + (L0 >> 6) * (NH * 128);
-            const int kc = (L0 & 63) >> 3, kb = (L0 & 7) * 2;
+            // my RKEYS probabilities at my keys' positions in row r of P' buffer k % NP: my keys are
+            // RKEYS (rep % (NREP / 2)) .. + RKEYS - 1 of my half, 16-byte chunks c0 .. c0 + RKEYS / 8 - 1
+            {
+                uint8_t *prow = sm + L::OFF_P + (k % L::NP) * L::PB + r * 128;
+                if (L::NP == 2 && k == 1) {
+                    // buffer 1 held the staged query rows: clear my row once every thread has read them
+                    if (!mbar_wait(&bars[T_QREADY], 0, s_abort)) { ok = false; break; }
 #pragma unroll
-            for (int h = 0; h < GM; ++h)
-                if (h < G) *reinterpret_cast<__half *>(pt + sw128(h, kc) + kb) = __float2half_rn(p[h]);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars[T_PFULL0 + (k & 1)]);
-        }
-        // ---- epilogue: this split's (m, l, O) per head of the group
-        bool wrote = false;
-        if (ok && T > 0 && wait_pv(T - 1)) {
-            float o[NH], o_hi[NH];
-            tmem_ld16(tmem + COL_O + lane_base, o);
-            tmem_ld16(tmem + COL_O + 16 + lane_base, o_hi);
-#pragma unroll
-            for (int h = 0; h < NH; ++h) o[h] += o_hi[h];
-            // row sums: over the warp (fixed tree), then the four warps in order
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                for (int h = 0; h < GM; ++h) l_part[h] += __shfl_xor_sync(0xffffffffu, l_part[h], off);
-            float *slot = s_red + (x_seq & 1) * 4 * NH;
-            if (lane < GM) {
-                float v = l_part[0];
-#pragma unroll
-                for (int h = 1; h < GM; ++h) v = lane == h ? l_part[h] : v;
-                slot[lane * 4 + quarter] = v;
-            }
-            mbar_arrive(&bars[T_XCHG]);
-            if (mbar_wait(&bars[T_XCHG], x_seq & 1, s_abort)) {
-                ++x_seq;
-                const int64_t pbase = ((int64_t)hkv * MAX_SPLIT + split) * G;
-                float *part_o = a.part;
-                float *part_ml = a.part + (int64_t)a.n_head_kv * MAX_SPLIT * G * D;
-#pragma unroll
-                for (int h = 0; h < GM; ++h)
-                    if (h < G) part_o[(pbase + h) * D + L0] = o[h];
-                if (L0 < G) {
-                    float mv = m_run[0];
-#pragma unroll
-                    for (int h = 1; h < GM; ++h) mv = L0 == h ? m_run[h] : mv;
-                    const float4 w4 = *reinterpret_cast<const float4 *>(slot + 4 * L0);
-                    part_ml[(pbase + L0) * 2] = mv;
-                    part_ml[(pbase + L0) * 2 + 1] = ((w4.x + w4.y) + w4.z) + w4.w;
+                    for (int c = 0; c < 8; ++c) reinterpret_cast<uint4 *>(prow)[c] = make_uint4(0u, 0u, 0u, 0u);
                 }
-                wrote = true;
+                const int c0 = (RKEYS / 8) * (rep % (NREP / 2));
+#pragma unroll
+                for (int c = 0; c < RKEYS / 8; ++c)
+                    *reinterpret_cast<uint4 *>(prow + (((c0 + c) ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[T_PFULL0 + k % L::NP]);
         }
-        if (!wrote && L0 < G) {
+        // ---- epilogue: every row's (m, l, O) to shared memory (the operand rings are free once the
+        // last PV has completed), then one thread per head dim merges the eight rows of each head
+        float *mrg = reinterpret_cast<float *>(sm + L::OFF_MRG);   // [row][128], float4 chunks rotated
+        float *mls = reinterpret_cast<float *>(sm + L::OFF_ML);    // [row][2]
+        if (ok && T > 0 && wait_pv(T - 1)) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tmem + COL_O + 128 * hf + 32 * c + lane_base, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int ch = c * 8 + e;
+                    *reinterpret_cast<float4 *>(mrg + r * D + 4 * (ch ^ (r & 31))) =
+                        make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                    __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                }
+            }
+            mls[2 * r] = m_run;
+            mls[2 * r + 1] = l_run;
+        } else {
+            ok = false;
+        }
+        mbar_arrive(&bars[T_XCHG]);
+        bool wrote = false;
+        if (ok && mbar_wait(&bars[T_XCHG], 0, s_abort) && !*s_abort) {
+            const int d = r;   // head dim
+            const int64_t pbase = ((int64_t)hkv * MAX_SPLIT + split) * G;
+            float *part_o = a.part;
+            float *part_ml = a.part + (int64_t)a.n_head_kv * MAX_SPLIT * G * D;
+            for (int hh = 0; hh < G; ++hh) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < NREP; ++q) M = fmaxf(M, mls[2 * (HS * q + hh)]);
+                float acc = 0.f, lsum = 0.f;
+#pragma unroll
+                for (int q = 0; q < NREP; ++q) {
+                    const int row = HS * q + hh;
+                    const float mr = mls[2 * row];
+                    const float w = mr == -INFINITY ? 0.f : ex2(mr - M);
+                    lsum += w * mls[2 * row + 1];
+                    acc += w * mrg[row * D + 4 * ((d >> 2) ^ (row & 31)) + (d & 3)];
+                }
+                part_o[(pbase + hh) * D + d] = acc;
+                if (d == 0) {
+                    part_ml[(pbase + hh) * 2] = M;
+                    part_ml[(pbase + hh) * 2 + 1] = lsum;
+                }
+            }
+            wrote = true;
+        }
+        if (!wrote && r < G) {
             // a split that gave up leaves an empty partial (m = -inf, l = 0), which the combine
             // weighs 0, rather than another call's leftovers
             float *part_ml = a.part + (int64_t)a.n_head_kv * MAX_SPLIT * G * D;
-            const int64_t pi = ((int64_t)hkv * MAX_SPLIT + split) * G + L0;
+            const int64_t pi = ((int64_t)hkv * MAX_SPLIT + split) * G + r;
             part_ml[pi * 2] = -INFINITY;
             part_ml[pi * 2 + 1] = 0.f;
         }
     } else if constexpr (Q8) {
         // ------------------------------------------------------------------ dequantise (q8_0)
-        constexpr int HPT = 256 / L::NDQ;               // head-dim halves per thread
-        const int dt = threadIdx.x - 192;
-        const int r = dt & (TK - 1), hd0 = dt / TK;   // key row of the tile, first head-dim half
-        constexpr int NB = D / 32;
-        bool ok = true;
-        uint32_t sk_n[HPT], sv_n[HPT];
-        // the fp16 scales of blocks 2 hd and 2 hd + 1 of my key's K and V rows, for my halves hd
-        auto scales = [&](int k, uint32_t (&sk)[HPT], uint32_t (&sv)[HPT]) {
-            const int key = min(j_begin + k * TK + r, a.n_keys - 1);  // keys past the end: any finite scale
-            const int64_t srow = a.layer * a.g.s_layer + hkv * a.g.s_head + (int64_t)key * a.g.s_tok;
+        if (warp >= 8) {
+            const int kv = warp >= 12;              // warps 8-11: K rows, warps 12-15: V rows
+            const int t = (threadIdx.x - 256) & 127;   // key row of the tile
+            const uint16_t *scl = kv ? a.vs : a.ks;
+            const int n = kv ? L::NV : L::NK;
+            const int bar_full = kv ? T_VFULL : T_KFULL;
+            uint8_t *ring = sm + (kv ? L::OFF_V : L::OFF_K);
+            // the four fp16 scales of my key's row (keys past the end: any finite scale, their codes are
+            // zero-filled), loaded through L2: the append before this kernel may have written them
+            auto scales = [&](int k) -> uint2 {
+                const int key = min(j_begin + k * TK + t, a.n_keys - 1);
+                return __ldcg(reinterpret_cast<const uint2 *>(scl + a.layer * a.g.s_layer + hkv * a.g.s_head +
+                                                               (int64_t)key * a.g.s_tok));
+            };
+            const int bar_raw = kv ? T_VRAW : T_KRAW;
+            uint2 sw_n = T > 0 ? scales(0) : make_uint2(0u, 0u);
+            for (int k = 0; k < T; ++k) {
+                const uint2 sw = sw_n;
+                if (k + 1 < T) sw_n = scales(k + 1);
+                const int s = k % n;
+                if (!mbar_wait(&bars[bar_raw + s], (k / n) & 1, s_abort)) break;
+                uint8_t *slot = ring + s * L::OPT;
+                // my row's 128 codes (in the bytes of my fp16 row's first block): 16-byte chunk i holds head
+                // dims 16 i .. 16 i + 15 (block i / 2); all read before any write
+                uint4 q[D / 16];
 #pragma unroll
-            for (int hh = 0; hh < HPT; ++hh) {
-                sk[hh] = __ldg(reinterpret_cast<const uint32_t *>(a.ks + srow) + hd0 + hh);
-                sv[hh] = __ldg(reinterpret_cast<const uint32_t *>(a.vs + srow) + hd0 + hh);
-            }
-        };
-        if (T > 0) scales(0, sk_n, sv_n);
-        for (int k = 0; ok && k < T; ++k) {
-            uint32_t sk[HPT], sv[HPT];
+                for (int i = 0; i < D / 16; ++i)
+                    q[i] = *reinterpret_cast<const uint4 *>(slot + (kv ? v_off(t, 0, i) : k_off(t, 0, i)));
 #pragma unroll
-            for (int hh = 0; hh < HPT; ++hh) {
-                sk[hh] = sk_n[hh];
-                sv[hh] = sv_n[hh];
-            }
-            if (k + 1 < T) scales(k + 1, sk_n, sv_n);
-            const int rs = k % L::NR;
-            if (!mbar_wait(&bars[T_RFULL + rs], (k / L::NR) & 1, s_abort)) { ok = false; break; }
-            const uint8_t *raw = sm + L::OFF_RAW + rs * L::RAWT;
-#pragma unroll 1
-            for (int kv = 0; kv < 2; ++kv) {
-                const int s = k % (kv ? L::NV : L::NK);
-                const int n = kv ? L::NV : L::NK;
-                if (k >= n && !mbar_wait(&bars[(kv ? T_VEMPTY : T_KEMPTY) + s], ((k / n) - 1) & 1, s_abort)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *src = raw + kv * (TK * D);
-                uint8_t *dst = sm + (kv ? L::OFF_V : L::OFF_K) + s * L::OPT;
-#pragma unroll
-                for (int hh = 0; hh < HPT; ++hh) {
-                const int hd = hd0 + hh;
-                const uint32_t sw = kv ? sv[hh] : sk[hh];
-                // my half row: 16-byte code chunks 4 hd .. 4 hd + 3 (two 32-value blocks)
-                uint4 q[D / 32];
-#pragma unroll
-                for (int i = 0; i < D / 32; ++i) q[i] = *reinterpret_cast<const uint4 *>(src + sw128(r, 4 * hd + i));
-#pragma unroll
-                for (int i = 0; i < D / 32; ++i) {
-                    const int c = 4 * hd + i;
-                    const unsigned short sb = (unsigned short)(sw >> (16 * (i >> 1)));
+                for (int i = 0; i < D / 16; ++i) {
+                    const int blk = i >> 1;
+                    const uint32_t w2 = blk < 2 ? sw.x : sw.y;
+                    const unsigned short sb = (unsigned short)(w2 >> (16 * (blk & 1)));
                     const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
                     uint32_t o[8];
                     dequant4(q[i].x, d2, o[0], o[1]);
                     dequant4(q[i].y, d2, o[2], o[3]);
                     dequant4(q[i].z, d2, o[4], o[5]);
                     dequant4(q[i].w, d2, o[6], o[7]);
-                    // fp16 chunk 2c and 2c + 1 of the row: column block (2c) / 8, chunk (2c) % 8 inside it
-                    *reinterpret_cast<uint4 *>(dst + (c >> 2) * (TK * 128) + sw128(r, (2 * c) & 7)) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4 *>(dst + (c >> 2) * (TK * 128) + sw128(r, (2 * c + 1) & 7)) =
-                        make_uint4(o[4], o[5], o[6], o[7]);
+                    // fp16 chunks 2 i and 2 i + 1 of the row: 64-dim block i / 4, chunk (2 i) % 8 in it
+                    const int cb = i >> 2, c0 = (2 * i) & 7;
+                    const uint32_t o0 = kv ? v_off(t, cb, c0) : k_off(t, cb, c0);
+                    const uint32_t o1 = kv ? v_off(t, cb, c0 + 1) : k_off(t, cb, c0 + 1);
+                    *reinterpret_cast<uint4 *>(slot + o0) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(slot + o1) = make_uint4(o[4], o[5], o[6], o[7]);
                 }
-                }
-                // order the operand writes before the MMA (async proxy) reads them
+                // order the operand writes before the MMA (async proxy) reads them, and before the next
+                // TMA into this slot (which comes after those MMAs)
                 fence_proxy_async_smem();
-                mbar_arrive(&bars[(kv ? T_VFULL : T_KFULL) + s]);
+                mbar_arrive(&bars[bar_full + s]);
             }
-            if (!ok) break;
-            // the raw stage's generic reads are ordered by the fence above before its TMA refill
-            mbar_arrive(&bars[T_REMPTY + rs]);
         }
-        (void)NB;
     }
 
     tc_fence_before();
@@ -1118,7 +1157,7 @@ __global__ void __launch_bounds__(TCfg<Q8>::THREADS, TCfg<Q8>::CTAS)
 template <bool Q8, int DT, int NS>
 int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_head_q, float *const *outs,
               cudaStream_t s) {
-    using L = TCfg<Q8>;
+    using L = TCfg<Q8, 16>;   // the larger shared-memory plan; both variants take the same launch shape
     constexpr int D = 128;
     TcBatch<NS> b;
     CombineBatch<NS> cb;
@@ -1144,10 +1183,11 @@ int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_he
         const uint8_t *kb = static_cast<const uint8_t *>(c.k_q), *vb = static_cast<const uint8_t *>(c.v_q);
         const CUtensorMapDataType dt = Q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const uint32_t box0 = 128 / eb;   // 128-byte rows: all 128 codes (q8_0) or 64 halves (f16)
+        // K by 128-key tiles, V by 64-key halves (the halves sit side by side along the PV MMA's N)
         if (!make_map_3d(&b.tk[i], dt, kb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv,
                          eb * g.c_tok, eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map_3d(&b.tv[i], dt, vb + (int64_t)eb * a.layer * g.c_layer, D, a.n_keys, a.n_head_kv,
-                         eb * g.c_tok, eb * g.c_head, box0, TK, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+                         eb * g.c_tok, eb * g.c_head, box0, TKH, 1, CU_TENSOR_MAP_SWIZZLE_128B))
             return KVC_ECUDA;
         b.a[i] = a;
         cb.part[i] = a.part;
@@ -1158,8 +1198,9 @@ int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_he
     const uint64_t stall_ns = take_test_stall(KVC_TEST_DECODE);
     for (int i = 0; i < n_seq; ++i) b.a[i].stall_ns = stall_ns;
     const int group = a0[0].group, n_head_kv = a0[0].n_head_kv;
-    auto kern = group <= 8 ? decode_tc_kernel<Q8, DT, 8, NS> : decode_tc_kernel<Q8, DT, 16, NS>;
-    if (allow_dynamic_smem((const void *)kern, L::ALLOC) != KVC_OK) return KVC_ECUDA;
+    auto kern = group <= 8 ? decode_tc_kernel<Q8, DT, NS, 8> : decode_tc_kernel<Q8, DT, NS, 16>;
+    const int smem = group <= 8 ? TCfg<Q8, 8>::ALLOC : TCfg<Q8, 16>::ALLOC;
+    if (allow_dynamic_smem((const void *)kern, smem) != KVC_OK) return KVC_ECUDA;
     // both passes may start while the previous kernel of the stream finishes; each waits for it on
     // the device before reading what it wrote
     cudaLaunchAttribute attr[1];
@@ -1168,7 +1209,7 @@ int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_he
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(max_split, n_head_kv, n_seq);
     cfg.blockDim = dim3(L::THREADS);
-    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
