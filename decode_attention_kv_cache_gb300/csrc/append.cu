@@ -37,11 +37,11 @@ template <int DT>
 __device__ __forceinline__ void load8(const void *base, int64_t idx, float (&x)[8]) {
     if constexpr (DT == KVC_IN_F32) {
         const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + idx);
-        float4 a = __ldg(p), b = __ldg(p + 1);
+        float4 a = __ldcg(p), b = __ldcg(p + 1);
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     } else {
-        uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + idx));
+        uint4 u = __ldcg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + idx));
         uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
 #pragma unroll
         for (int m = 0; m < CPB; ++m) {
             const int c = 32 * m + lane;
-            t[m] = c < nwc ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            t[m] = c < nwc ? __ldcg(src + c) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int m = 0; m < CPB; ++m) S[stage_slot(32 * m + lane)] = t[m];

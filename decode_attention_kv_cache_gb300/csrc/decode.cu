@@ -108,9 +108,9 @@ __device__ __forceinline__ uint32_t codes_to_half2(uint32_t t) {
 
 template <int DT>
 __device__ __forceinline__ float load_q(const void *q, int64_t i) {
-    if constexpr (DT == KVC_IN_F32) return __ldg(static_cast<const float *>(q) + i);
+    if constexpr (DT == KVC_IN_F32) return __ldcg(static_cast<const float *>(q) + i);
     else {
-        const uint16_t u = __ldg(static_cast<const uint16_t *>(q) + i);
+        const uint16_t u = __ldcg(static_cast<const unsigned short *>(q) + i);
         if constexpr (DT == KVC_IN_BF16) return __uint_as_float((uint32_t)u << 16);
         else return __half2float(__ushort_as_half(u));
     }
@@ -180,13 +180,13 @@ __device__ __forceinline__ void load_scales(const DecodeArgs &a, int hkv, int j0
         const int key = min(j0 + 4 * cq + r, last);
         const int64_t srow = base_s + (int64_t)key * a.g.s_tok;
         if constexpr (NB == 4) {
-            const uint2 wk = __ldg(reinterpret_cast<const uint2 *>(a.ks + srow));
-            const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(a.vs + srow));
+            const uint2 wk = __ldcg(reinterpret_cast<const uint2 *>(a.ks + srow));
+            const uint2 wv = __ldcg(reinterpret_cast<const uint2 *>(a.vs + srow));
             S.sk[r][0] = wk.x; S.sk[r][1] = wk.y;
             S.sv[r][0] = wv.x; S.sv[r][1] = wv.y;
         } else {
-            S.sk[r][0] = __ldg(reinterpret_cast<const uint32_t *>(a.ks + srow));
-            S.sv[r][0] = __ldg(reinterpret_cast<const uint32_t *>(a.vs + srow));
+            S.sk[r][0] = __ldcg(reinterpret_cast<const unsigned int *>(a.ks + srow));
+            S.sv[r][0] = __ldcg(reinterpret_cast<const unsigned int *>(a.vs + srow));
         }
     }
 }
@@ -1026,8 +1026,9 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             fence_proxy_async_smem();
             mbar_arrive(&bars[T_PFULL0 + k % L::NP]);
         }
-        // ---- epilogue: every row's (m, l, O) to shared memory (the operand rings are free once the
-        // last PV has completed), then one thread per head dim merges the eight rows of each head
+        // ---- epilogue: the rows of real heads store (m, l, O) in shared memory (the operand rings are
+        // free once the last PV has completed); then each warp merges whole heads, a lane per four head
+        // dims, the replicas taken in order
         float *mrg = reinterpret_cast<float *>(sm + L::OFF_MRG);   // [row][128], float4 chunks rotated
         float *mls = reinterpret_cast<float *>(sm + L::OFF_ML);    // [row][2]
         if (ok && T > 0 && wait_pv(T - 1)) {
@@ -1036,12 +1037,14 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                 uint32_t o[32];
                 tmem_ld32(tmem + COL_O + 128 * hf + 32 * c + lane_base, o);
                 tmem_ld_wait();
+                if (h < G) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int ch = c * 8 + e;
-                    *reinterpret_cast<float4 *>(mrg + r * D + 4 * (ch ^ (r & 31))) =
-                        make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                    __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    for (int e = 0; e < 8; ++e) {
+                        const int ch = c * 8 + e;
+                        *reinterpret_cast<float4 *>(mrg + r * D + 4 * (ch ^ (r & 31))) =
+                            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                        __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    }
                 }
             }
             mls[2 * r] = m_run;
@@ -1052,28 +1055,29 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
         mbar_arrive(&bars[T_XCHG]);
         bool wrote = false;
         if (ok && mbar_wait(&bars[T_XCHG], 0, s_abort) && !*s_abort) {
-            const int d = r;   // head dim
             const int64_t pbase = ((int64_t)hkv * MAX_SPLIT + split) * G;
             float *part_o = a.part;
             float *part_ml = a.part + (int64_t)a.n_head_kv * MAX_SPLIT * G * D;
-            for (int hh = 0; hh < G; ++hh) {
+            for (int hh = quarter; hh < G; hh += 4) {
                 float M = -INFINITY;
 #pragma unroll
                 for (int q = 0; q < NREP; ++q) M = fmaxf(M, mls[2 * (HS * q + hh)]);
-                float acc = 0.f, lsum = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lsum = 0.f;
 #pragma unroll
                 for (int q = 0; q < NREP; ++q) {
                     const int row = HS * q + hh;
-                    const float mr = mls[2 * row];
-                    const float w = mr == -INFINITY ? 0.f : ex2(mr - M);
-                    lsum += w * mls[2 * row + 1];
-                    acc += w * mrg[row * D + 4 * ((d >> 2) ^ (row & 31)) + (d & 3)];
+                    const float2 ml = *reinterpret_cast<const float2 *>(mls + 2 * row);
+                    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+                    lsum += w * ml.y;
+                    const float4 v = *reinterpret_cast<const float4 *>(mrg + row * D + 4 * (lane ^ (row & 31)));
+                    acc.x += w * v.x;
+                    acc.y += w * v.y;
+                    acc.z += w * v.z;
+                    acc.w += w * v.w;
                 }
-                part_o[(pbase + hh) * D + d] = acc;
-                if (d == 0) {
-                    part_ml[(pbase + hh) * 2] = M;
-                    part_ml[(pbase + hh) * 2 + 1] = lsum;
-                }
+                *reinterpret_cast<float4 *>(part_o + (pbase + hh) * D + 4 * lane) = acc;
+                if (lane == 0) *reinterpret_cast<float2 *>(part_ml + (pbase + hh) * 2) = make_float2(M, lsum);
             }
             wrote = true;
         }

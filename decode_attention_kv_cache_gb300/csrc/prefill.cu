@@ -413,8 +413,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                         float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
                         if (row < a.C) {
                             const float *src = a.q_f32 + ((int64_t)row * a.H_q + it.h) * D + cc * 8;
-                            x0 = __ldg(reinterpret_cast<const float4 *>(src));
-                            x1 = __ldg(reinterpret_cast<const float4 *>(src + 4));
+                            x0 = __ldcg(reinterpret_cast<const float4 *>(src));
+                            x1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
                         }
                         *p = make_uint4(pack_half2(x0.x, x0.y), pack_half2(x0.z, x0.w), pack_half2(x1.x, x1.y),
                                         pack_half2(x1.z, x1.w));
@@ -631,11 +631,11 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 for (int b = 0; b < NB / 2; ++b) sw[h][b] = 0u;
                 if (key < a.kv_len) {
                     if (NB == 4) {
-                        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(sp));
+                        const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(sp));
                         sw[h][0] = u.x;
                         sw[h][NB / 2 - 1] = u.y;
                     } else {
-                        sw[h][0] = __ldg(reinterpret_cast<const uint32_t *>(sp));
+                        sw[h][0] = __ldcg(reinterpret_cast<const unsigned int *>(sp));
                     }
                 }
             }
@@ -742,8 +742,10 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
 // fp16(d * q) of positions [0, kv_len) of one layer, K (grid.y 0) then V (1), each as [H][kv_len][D]:
 // the very values the in-kernel dequantiser writes into the operand tiles (same op, same rounding),
 // so the attention pass then runs as for an f16 cache and gives the same bits.  A thread converts 8
-// values (8 code bytes and their block's scale) into 16 bytes.  Launched normally after the append,
-// so it reads the chunk's keys; the attention pass may be scheduled as soon as it starts.
+// values (8 code bytes and their block's scale) into 16 bytes.  Launched normally after the append, so
+// the append has completed before it starts: it reads the chunk's keys, and its codes and scales are
+// read-only for its lifetime (read-only-path loads).  The attention pass may be scheduled as soon as it
+// starts.
 template <int D>
 __global__ void __launch_bounds__(256) dequant_range_kernel(const int8_t *__restrict__ kq,
                                                             const uint16_t *__restrict__ ks,
