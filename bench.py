@@ -65,20 +65,20 @@ def prefill_flops(w, chunks=None):
 # Entries: kernel -> {"sources": {file: sha16}, workload: (bytes per call, what was captured)}.
 TRAFFIC = {
     # the step's 29 attention calls (dequantising pass, attention, split merge), mean per call
-    "prefill": {"sources": {"prefill.cu": "9682bafba5ab4613"},
-                "q8_0_58k": (536457684, "mean per call over the 29 chunk calls of one step (all three kernels)")},
-    "append_chunk": {"sources": {"append.cu": "57915ca647353f7b"},
-                     "q8_0_58k": (8412698, "one 2048-token chunk append (writes still in L2 at the launch end)")},
-    "append_prompt": {"sources": {"append.cu": "57915ca647353f7b"},
-                      "q8_0_58k": (330907930, "the 58,300-token prompt in one append")},
-    "decode_attn": {"sources": {"decode.cu": "ad0b5108f74ba7d4"},
-                    "q8_0_58k": (128016794, "split pass + combine at position 58,555")},
-    "decode_step": {"sources": {"decode.cu": "ad0b5108f74ba7d4", "append.cu": "57915ca647353f7b"},
-                    "q8_0_58k": (128044467, "append + split pass + combine at position 58,555")},
+    "prefill": {"sources": {"prefill.cu": "86597859b4f808fb"},
+                "q8_0_58k": (535487390, "mean per call over the 29 chunk calls of one step (all three kernels)")},
+    "append_chunk": {"sources": {"append.cu": "a6f9e705a1d20ea1"},
+                     "q8_0_58k": (8411981, "one 2048-token chunk append (writes still in L2 at the launch end)")},
+    "append_prompt": {"sources": {"append.cu": "a6f9e705a1d20ea1"},
+                      "q8_0_58k": (330838784, "the 58,300-token prompt in one append")},
+    "decode_attn": {"sources": {"decode.cu": "c86cba417ecffa5b"},
+                    "q8_0_58k": (128015770, "split pass + combine at position 58,555")},
+    "decode_step": {"sources": {"decode.cu": "c86cba417ecffa5b", "append.cu": "a6f9e705a1d20ea1"},
+                    "q8_0_58k": (128079130, "append + split pass + combine at position 58,555")},
     "state_pack": {"sources": {"state.cu": "e0853a7210054393"},
-                   "q8_0_58k": (201629593, "header + pack of 58,556 tokens")},
+                   "q8_0_58k": (201684634, "header + pack of 58,556 tokens")},
     "state_unpack": {"sources": {"state.cu": "e0853a7210054393"},
-                     "q8_0_58k": (202273459, "unpack of 58,556 tokens")},
+                     "q8_0_58k": (202314982, "unpack of 58,556 tokens")},
 }
 
 

@@ -53,6 +53,20 @@ namespace {
 // set by a split pass that gave up a bounded wait (read and cleared with the other kernels' status)
 __device__ int g_decode_status;
 
+// Diagnostic build (-DKVC_TRACE, see build.py): the tensor-core split pass records clock64 stamps of its
+// pipeline events in CTA (0, 0) - event e of tile k in g_trace[e][k] (e = 1..13), overall events in
+// g_trace[0][.] - for kvc_trace_read.  The stamps change no work; a normal build compiles them away.
+#ifdef KVC_TRACE
+__device__ unsigned long long g_trace[16][64];
+#define KVC_TR(ev, k)                                                                   \
+    do {                                                                              \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (k) < 64)          \
+            g_trace[ev][k] = clock64();                                               \
+    } while (0)
+#else
+#define KVC_TR(ev, k) do { } while (0)
+#endif
+
 using namespace ptx;
 
 constexpr int MAX_SPLIT = 256;
@@ -718,6 +732,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
     const DecodeArgs &a = b.a[seq];
     const CUtensorMap *tm_k = &b.tk[seq], *tm_v = &b.tv[seq];
     if ((int)blockIdx.x >= a.n_split) return;   // a batch's shorter sequences use fewer splits
+    if (threadIdx.x == 0) KVC_TR(0, 0);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -770,6 +785,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
     // inputs written by the kernels before this one are read only past this point
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    if (threadIdx.x == 0) KVC_TR(0, 1);
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------------------------ producers (K: warp 0, V: warp 3)
@@ -797,6 +813,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                 const int j = j_begin + k * TK;
                 const int s = k % n;
                 if (k >= n && !mbar_wait(&bars[bar_empty + s], ((k / n) - 1) & 1, s_abort)) break;
+                KVC_TR(1 + (int)is_v, k);
                 uint8_t *dst = ring + s * L::OPT;
                 if constexpr (Q8) {
                     mbar_arrive_expect_tx(&bars[bar_fill + s], L::RAWB);
@@ -837,12 +854,14 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             const uint32_t sQ = smem_u32(sm + L::OFF_Q), sK = smem_u32(sm + L::OFF_K);
             bool ok = mbar_wait(&bars[T_QREADY], 0, s_abort);
             tc_fence_after();
+            KVC_TR(0, 2);
             for (int k = 0; ok && k < T; ++k) {
                 // S(k) into the S columns once every softmax thread has read S(k - 1)
                 if (k > 0 && !mbar_wait(&bars[T_SFREE], (k - 1) & 1, s_abort)) { ok = false; break; }
                 const int st = k % L::NK;
                 if (!mbar_wait(&bars[T_KFULL + st], (k / L::NK) & 1, s_abort)) { ok = false; break; }
                 tc_fence_after();
+                KVC_TR(3, k);
                 const uint32_t kb = sK + st * L::OPT;
                 // two independent chains, interleaved: head dims [0, 64) into columns [0, 128), [64, 128)
                 // into [128, 256); k-step i of chain c covers head dims 64 c + 16 i .. + 15
@@ -856,6 +875,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                     }
                 umma_commit(&bars[T_SFULL]);
                 umma_commit(&bars[T_KEMPTY + st]);
+                KVC_TR(4, k);
             }
             if (*s_abort) {
                 // after a wait gave up: let the MMAs in flight finish before TMEM is freed
@@ -884,6 +904,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                 const int vs = k % L::NV;
                 if (!mbar_wait(&bars[T_VFULL + vs], (k / L::NV) & 1, s_abort)) { ok = false; break; }
                 tc_fence_after();
+                KVC_TR(5, k);
                 const uint32_t pb = sP + (k % L::NP) * L::PB, vb = sV + vs * L::OPT;
 #pragma unroll
                 for (int ks = 0; ks < TKH / 16; ++ks)
@@ -891,6 +912,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                                 sdesc_sw128(vb + ks * 16 * 128, TKH * 128, 1024), IDESC_O, (k > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(&bars[T_ODONE0 + (k & 1)]);
                 umma_commit(&bars[T_VEMPTY + vs]);
+                KVC_TR(6, k);
             }
             if (*s_abort) {
                 volatile int never = 0;
@@ -934,6 +956,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             for (int c = 0; c < 8; ++c) prow[c] = make_uint4(0u, 0u, 0u, 0u);
             fence_proxy_async_smem();
             mbar_arrive(&bars[T_QREADY]);
+            if (threadIdx.x == 128) KVC_TR(0, 6);
         }
         float m_run = -INFINITY, l_run = 0.f;
         int pv_seen[2] = {0, 0};
@@ -949,6 +972,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
         for (int k = 0; ok && k < T; ++k) {
             if (!mbar_wait(&bars[T_SFULL], k & 1, s_abort)) { ok = false; break; }
             tc_fence_after();
+            if (threadIdx.x == 128) KVC_TR(7, k);
             // the warp's 32 key columns (its two replicas' keys) of both chains, then S may be overwritten
             uint32_t s0[32], s1[32];
             tmem_ld32(tmem + COL_S + 32 * quarter + lane_base, s0);
@@ -956,6 +980,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&bars[T_SFREE]);
+            if (threadIdx.x == 128) KVC_TR(8, k);
             const int key0 = j_begin + k * TK + RKEYS * rep;   // absolute position of my first key
             float x[RKEYS];
 #pragma unroll
@@ -1025,10 +1050,12 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars[T_PFULL0 + k % L::NP]);
+            if (threadIdx.x == 128) KVC_TR(9, k);
         }
         // ---- epilogue: the rows of real heads store (m, l, O) in shared memory (the operand rings are
         // free once the last PV has completed); then each warp merges whole heads, a lane per four head
         // dims, the replicas taken in order
+        if (threadIdx.x == 128) KVC_TR(0, 3);
         float *mrg = reinterpret_cast<float *>(sm + L::OFF_MRG);   // [row][128], float4 chunks rotated
         float *mls = reinterpret_cast<float *>(sm + L::OFF_ML);    // [row][2]
         if (ok && T > 0 && wait_pv(T - 1)) {
@@ -1052,6 +1079,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
         } else {
             ok = false;
         }
+        if (threadIdx.x == 128) KVC_TR(0, 7);
         mbar_arrive(&bars[T_XCHG]);
         bool wrote = false;
         if (ok && mbar_wait(&bars[T_XCHG], 0, s_abort) && !*s_abort) {
@@ -1081,6 +1109,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             }
             wrote = true;
         }
+        if (threadIdx.x == 128) KVC_TR(0, 4);
         if (!wrote && r < G) {
             // a split that gave up leaves an empty partial (m = -inf, l = 0), which the combine
             // weighs 0, rather than another call's leftovers
@@ -1112,6 +1141,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                 if (k + 1 < T) sw_n = scales(k + 1);
                 const int s = k % n;
                 if (!mbar_wait(&bars[bar_raw + s], (k / n) & 1, s_abort)) break;
+                if (t == 0) KVC_TR(10 + 2 * kv, k);
                 uint8_t *slot = ring + s * L::OPT;
                 // my row's 128 codes (in the bytes of my fp16 row's first block): 16-byte chunk i holds head
                 // dims 16 i .. 16 i + 15 (block i / 2); all read before any write
@@ -1141,12 +1171,14 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                 // TMA into this slot (which comes after those MMAs)
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[bar_full + s]);
+                if (t == 0) KVC_TR(11 + 2 * kv, k);
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) KVC_TR(0, 5);
     if (threadIdx.x == 0 && *s_abort) atomicExch(&g_decode_status, 1);
     if (warp == 1) {
         tc_fence_after();
@@ -1469,3 +1501,14 @@ int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dty
 }
 
 }  // namespace kvc
+
+#ifdef KVC_TRACE
+// Diagnostic build only: clear, or copy out (16 x 64 uint64), the split pass's clock stamps.
+extern "C" int kvc_trace_clear() {
+    static unsigned long long z[16 * 64] = {};
+    return cudaMemcpyToSymbol(kvc::g_trace, z, sizeof(z)) == cudaSuccess ? 0 : -1;
+}
+extern "C" int kvc_trace_read(unsigned long long *host) {
+    return cudaMemcpyFromSymbol(host, kvc::g_trace, sizeof(kvc::g_trace)) == cudaSuccess ? 0 : -1;
+}
+#endif
