@@ -9,7 +9,7 @@ the quantiser depends on IEEE division.
 
 build(trace=True) makes the diagnostic variant libkvc_trace.so (objects in
 _build_trace/), compiled with -DKVC_TRACE: the decode split pass then records
-clock stamps of its pipeline events (see trace_decode.py).  The product build
+clock stamps of its pipeline events (see trace_kernels.py).  The product build
 never defines it.
 """
 

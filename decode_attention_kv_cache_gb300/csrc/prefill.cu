@@ -67,6 +67,19 @@ __device__ int g_device_status;
 
 namespace {
 
+// Diagnostic build (-DKVC_TRACE, see build.py): CTA 0 of the attention pass records clock64 stamps of its
+// pipeline events, event e of its n-th key tile in g_ptrace[e][n], for kvc_ptrace_read.  The stamps change
+// no work; a normal build compiles them away.
+#ifdef KVC_TRACE
+__device__ unsigned long long g_ptrace[16][128];
+#define KVC_PTR(ev, n)                                                           \
+    do {                                                                       \
+        if (blockIdx.x == 0 && (n) < 128) g_ptrace[ev][n] = clock64();          \
+    } while (0)
+#else
+#define KVC_PTR(ev, n) do { } while (0)
+#endif
+
 using namespace ptx;
 
 constexpr int BM = 128;           // query rows per unit
@@ -275,6 +288,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                     if (ring_seq >= (uint32_t)L::NS &&
                         !mbar_wait(&bars[B_RING_EMPTY + st], ((ring_seq / L::NS) - 1) & 1, s_abort))
                         return false;
+                    KVC_PTR(12, ring_seq);
                     mbar_arrive_expect_tx(&bars[B_RING_FULL + st], L::ST_BYTES);
                     for (int dh = 0; dh < D / 64; ++dh)
                         tma_load_3d(sm + L::OFF_RING + st * L::ST_BYTES + dh * BN * 128, m, &bars[B_RING_FULL + st],
@@ -328,8 +342,10 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             // softmax must have read out (s_free).
             auto issue_s = [&]() -> bool {
                 if (s_issued > 0 && !mbar_wait(&bars[B_SFREE], (s_issued - 1) & 1, s_abort)) return false;
+                KVC_PTR(1, s_issued);
                 const uint32_t seq = ring_seq++;
                 if (!ring_wait(seq)) return false;
+                KVC_PTR(2, s_issued);
                 const uint32_t kb = sRing + (seq % L::NS) * L::ST_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -339,12 +355,14 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 }
                 umma_commit(&bars[B_SFULL]);
                 umma_commit(&bars[B_RING_EMPTY + seq % L::NS]);
+                KVC_PTR(3, s_issued);
                 ++s_issued;
                 return true;
             };
             // O (+)= P V: P fp16 from TMEM, V MN-major in the ring stage
             auto issue_pv = [&](bool acc) -> bool {
                 const uint32_t seq = ring_seq++;
+                KVC_PTR(4, p_seq - 1);
                 if (!ring_wait(seq)) return false;
                 const uint32_t vb = sRing + (seq % L::NS) * L::ST_BYTES;
 #pragma unroll
@@ -353,6 +371,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                                 IDESC_O, (acc || ks > 0) ? 1u : 0u);
                 umma_commit(&bars[B_ODONE]);
                 umma_commit(&bars[B_RING_EMPTY + seq % L::NS]);
+                KVC_PTR(5, p_seq - 1);
                 return true;
             };
             for (int i = first_item; ok && i < a.n_items; i += stride) {
@@ -478,6 +497,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             float m_ref = -INFINITY, l = 0.f;
             for (int k = it.k0; k < it.k1; ++k) {
                 if (!mbar_wait(&bars[B_SFULL], s_seq & 1, s_abort)) { ok = false; break; }
+                if (threadIdx.x == 128) KVC_PTR(6, s_seq);
+                if (threadIdx.x == 256) KVC_PTR(10, s_seq);
                 ++s_seq;
                 tc_fence_after();
                 // my half of the S row in registers (one TMEM round trip), then S may be overwritten
@@ -487,6 +508,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&bars[B_SFREE]);
+                if (threadIdx.x == 128) KVC_PTR(7, s_seq - 1);
                 const int key0 = k * BN + 128 * grp;
                 if (key0 + 127 > it.tf) {
 #pragma unroll
@@ -510,6 +532,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                     fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 float mx_other;
                 if (!exchange(mx_own, mx_other)) { ok = false; break; }
+                if (threadIdx.x == 128) KVC_PTR(8, s_seq - 1);
                 const float mx = grp == 0 ? fmaxf(mx_own, mx_other) : fmaxf(mx_other, mx_own);
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 float m_use = m_ref, alpha = 1.f;
@@ -569,6 +592,8 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bars[B_PFULL]);
+                if (threadIdx.x == 128) KVC_PTR(9, s_seq - 1);
+                if (threadIdx.x == 256) KVC_PTR(11, s_seq - 1);
                 m_ref = m_use;
             }
             if (!ok) break;
@@ -985,3 +1010,14 @@ int read_and_clear_device_status(int32_t *status) {
 }
 
 }  // namespace kvc
+
+#ifdef KVC_TRACE
+// Diagnostic build only: clear, or copy out (16 x 128 uint64), the attention pass's clock stamps.
+extern "C" int kvc_ptrace_clear() {
+    static unsigned long long z[16 * 128] = {};
+    return cudaMemcpyToSymbol(kvc::g_ptrace, z, sizeof(z)) == cudaSuccess ? 0 : -1;
+}
+extern "C" int kvc_ptrace_read(unsigned long long *host) {
+    return cudaMemcpyFromSymbol(host, kvc::g_ptrace, sizeof(kvc::g_ptrace)) == cudaSuccess ? 0 : -1;
+}
+#endif
