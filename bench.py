@@ -65,7 +65,7 @@ def prefill_flops(w, chunks=None):
 # Entries: kernel -> {"sources": {file: sha16}, workload: (bytes per call, what was captured)}.
 TRAFFIC = {
     # the step's 29 attention calls (dequantising pass, attention, split merge), mean per call
-    "prefill": {"sources": {"prefill.cu": "86597859b4f808fb"},
+    "prefill": {"sources": {"prefill.cu": "900fe085b81b05bd"},
                 "q8_0_58k": (535487390, "mean per call over the 29 chunk calls of one step (all three kernels)")},
     "append_chunk": {"sources": {"append.cu": "a6f9e705a1d20ea1"},
                      "q8_0_58k": (8411981, "one 2048-token chunk append (writes still in L2 at the launch end)")},
