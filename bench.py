@@ -3,8 +3,8 @@
 
 One step = one request on every layer of the workload: the prompt prefilled in
 chunks (kv_cache_append + prefill_chunk_attn per chunk), the decode steps
-(kv_cache_append + decode_attn per token, the loop captured once in a CUDA
-graph), then the cache state serialised from the head-major cache
+(decode_step per token: the split pass stores the token and attends, then the
+combine; the loop captured once in a CUDA graph), then the cache state serialised from the head-major cache
 (kv_state_get) and restored into a layer-major cache (kv_state_set).
 
 `value` is the whole request's throughput per attention layer: (prompt +
@@ -252,21 +252,22 @@ class GpuRequest:
     def launches_per_step(self):
         """Kernels one step launches: per chunk an append and the attention (q8_0: and the pass that
         dequantises the attended keys into the prefill scratch), plus the split merge when
-        the chunk's last row reaches past the first key split; per decode step append, split pass and
-        combine; the state header, pack and unpack."""
+        the chunk's last row reaches past the first key split; per decode step the split pass (which
+        stores the token) and the combine (head_dim 64: also the append); the state header, pack and
+        unpack."""
         w = self.w
         keys = prefill_split_keys(w.n_ctx)
         merges = sum(1 for p, c in self.chunks if p + c - 1 >= keys)
         per_chunk = 3 if w.cache == "q8_0" else 2
-        return w.n_layer * (per_chunk * len(self.chunks) + merges + 3 * w.n_decode) + 3
+        per_decode = 2 if w.head_dim == 128 else 3
+        return w.n_layer * (per_chunk * len(self.chunks) + merges + per_decode * w.n_decode) + 3
 
     def _decode_loop(self, layer):
         kvc, w = self.kvc, self.w
         q, k, v = self.dev_in[layer]
         for i in range(w.n_decode):
             pos = w.n_prompt + i
-            kvc.kv_cache_append(self.src, layer, pos, k[pos:pos + 1], v[pos:pos + 1])
-            kvc.decode_attn(self.src, layer, pos, q[pos], out=self.out_d[self.out_slot(layer), i],
+            kvc.decode_step(self.src, layer, pos, q[pos], k[pos], v[pos], out=self.out_d[self.out_slot(layer), i],
                             scratch=self.scratch)
 
     def attention_only(self):
@@ -535,11 +536,10 @@ def kernel_rooflines(kvc, torch, w, req, flush, reps, peak_gbs, peak_src):
                                                          scratch=req.scratch),
                                  "decode_attn at position %d (split pass + combine)" % pos)
 
-        def step():
-            kvc.kv_cache_append(req.src, 0, pos, k[pos:pos + 1], v[pos:pos + 1])
-            kvc.decode_attn(req.src, 0, pos, q[pos], out=req.out_d[0, -1], scratch=req.scratch)
-        out["decode_step"] = obj("decode_step", dec + row_in + bt, step,
-                                 "one decode step at position %d: append of the token + decode_attn" % pos)
+        out["decode_step"] = obj("decode_step", dec + row_in + bt,
+                                 lambda: kvc.decode_step(req.src, 0, pos, q[pos], k[pos], v[pos], out=req.out_d[0, -1],
+                                                         scratch=req.scratch),
+                                 "decode_step at position %d: split pass storing the token + combine" % pos)
     sb = req.state.numel()
     out["state_pack"] = obj("state_pack", 2 * sb - 32,
                             lambda: kvc.kv_state_get(req.src, w.n_tokens, dst=req.state),
@@ -551,10 +551,10 @@ def kernel_rooflines(kvc, torch, w, req, flush, reps, peak_gbs, peak_src):
 
 
 def batched_decode(kvc, torch, w, device, npls, n_past=2048, n_gen=128):
-    """Generation with npl sequences decoded together (decode_attn_batch), the setup of a batched
+    """Generation with npl sequences decoded together (decode_step_batch), the setup of a batched
     bench: each sequence holds an n_past-token prompt of this workload's shape in its own cache, then
-    n_gen steps each append one token per sequence (kv_cache_append_batch) and decode all sequences in
-    one call (decode_attn_batch), in a CUDA graph.
+    n_gen steps each store one token per sequence and decode all sequences in one call
+    (decode_step_batch), in a CUDA graph.
     Reports generated tokens/s over all sequences and the algorithmic cache bytes read per second."""
     res = {}
     bt = cache_bytes_per_token(w)
@@ -579,8 +579,7 @@ def batched_decode(kvc, torch, w, device, npls, n_past=2048, n_gen=128):
         def gen():
             for t in range(n_gen):
                 pos = [n_past + t] * npl
-                kvc.kv_cache_append_batch(caches, 0, pos, ks[t], vs[t])
-                kvc.decode_attn_batch(caches, 0, pos, qs[t], out=out[t], scratch=scratch)
+                kvc.decode_step_batch(caches, 0, pos, qs[t], ks[t], vs[t], out=out[t], scratch=scratch)
         s = torch.cuda.Stream(device)
         with torch.cuda.stream(s):
             gen()
@@ -597,8 +596,8 @@ def batched_decode(kvc, torch, w, device, npls, n_past=2048, n_gen=128):
         res[str(npl)] = {"tg_tok_s": npl * n_gen / (ms / 1e3), "us_per_step": ms * 1e3 / n_gen,
                          "algorithmic_GB_s": cache_bytes / (ms / 1e3) / 1e9}
         del graph
-    res["setup"] = "npl sequences, %d-token prompts, %d generated tokens each, kv_cache_append_batch + " \
-                   "decode_attn_batch per step in a CUDA graph" % (n_past, n_gen)
+    res["setup"] = "npl sequences, %d-token prompts, %d generated tokens each, one decode_step_batch " \
+                   "per step in a CUDA graph" % (n_past, n_gen)
     return res
 
 

@@ -62,6 +62,8 @@ def _load():
         "kvc_pipeline_chunk": (ctypes.c_int, [I32, I32, I32, ctypes.c_double, P(I32)]),
         "kv_cache_truncate": (ctypes.c_int, [P(kvc_cache), I32, VP]),
         "decode_attn_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, I32, I32, VP, VP, SZ, VP]),
+        "decode_step": (ctypes.c_int, [P(kvc_cache), I32, I32, VP, VP, VP, I32, I32, VP, VP, SZ, VP]),
+        "decode_step_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, VP, VP, I32, I32, VP, VP, SZ, VP]),
         "kv_cache_append_batch": (ctypes.c_int, [P(kvc_cache), I32, I32, P(I32), VP, VP, I32, VP]),
         "kv_state_get_heads": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, SZ, VP]),
         "kv_state_set_heads": (ctypes.c_int, [P(kvc_cache), I32, VP, SZ, P(I32), VP]),
@@ -226,6 +228,46 @@ def decode_attn(cache, layer, pos, q, out=None, scratch=None, stream=None):
     st = _lib().decode_attn(ctypes.byref(cache.c), layer, pos, _ptr(q), DTYPES[q.dtype], n_head_q, _ptr(out),
                          _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream, q.device))
     _check(st, "decode_attn")
+    return out
+
+
+def decode_step(cache, layer, pos, q, k, v, out=None, scratch=None, stream=None):
+    """One decode step: store k, v [H_kv, D] at position pos (as kv_cache_append) and attend with
+    q [H_q, D] over positions [0, pos] (as decode_attn); returns out [H_q, D] f32."""
+    _need(q, "q"); _need(k, "k", q.dtype); _need(v, "v", q.dtype)
+    n_head_q = q.shape[0]
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if scratch is None:
+        scratch = torch.empty(cache.scratch_bytes(n_head_q), dtype=torch.uint8, device=q.device)
+    _need(out, "out", torch.float32); _need(scratch, "scratch")
+    st = _lib().decode_step(ctypes.byref(cache.c), layer, pos, _ptr(q), _ptr(k), _ptr(v), DTYPES[q.dtype], n_head_q,
+                            _ptr(out), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                            _stream(stream, q.device))
+    _check(st, "decode_step")
+    return out
+
+
+def decode_step_batch(caches, layer, pos, q, k, v, out=None, scratch=None, stream=None):
+    """decode_step for len(caches) sequences in one call: q [n_seq][H_q][D], k and v [n_seq][H_kv][D]
+    (CUDA), pos a list; returns out [n_seq][H_q][D] f32."""
+    n = len(caches)
+    if n != len(pos) or q.dim() != 3 or q.shape[0] != n or k.shape[0] != n or v.shape != k.shape:
+        raise ValueError("one position, one query and one K/V row block per sequence")
+    _need(q, "q"); _need(k, "k", q.dtype); _need(v, "v", q.dtype)
+    c0 = caches[0]
+    n_head_q = q.shape[1]
+    if out is None:
+        out = torch.empty(n, n_head_q, c0.head_dim, dtype=torch.float32, device=c0.device)
+    _need(out, "out", torch.float32)
+    if scratch is None:
+        scratch = torch.empty(n * c0.scratch_bytes(n_head_q), dtype=torch.uint8, device=c0.device)
+    _need(scratch, "scratch")
+    arr = (kvc_cache * n)(*[c.c for c in caches])
+    ps = (ctypes.c_int32 * n)(*[int(p) for p in pos])
+    st = _lib().decode_step_batch(arr, n, layer, ps, _ptr(q), _ptr(k), _ptr(v), DTYPES[q.dtype], n_head_q, _ptr(out),
+                                  _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream, c0.device))
+    _check(st, "decode_step_batch")
     return out
 
 

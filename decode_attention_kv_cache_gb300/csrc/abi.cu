@@ -174,6 +174,48 @@ int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *
                          (cudaStream_t)stream);
 }
 
+int decode_step(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, const void *k, const void *v,
+                int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes, kvc_stream_t stream) {
+    if (!cache_ok(cache) || !dtype_ok(dtype)) return KVC_EINVAL;
+    if (cache->d.head_dim != 64 && cache->d.head_dim != 128) return KVC_EINVAL;
+    if (n_head_q <= 0 || n_head_q % cache->d.n_head_kv || n_head_q / cache->d.n_head_kv > 16)
+        return KVC_EINVAL;
+    if (layer < 0 || layer >= cache->d.n_layer || pos < 0 || pos >= cache->d.n_ctx) return KVC_ERANGE;
+    if (!q || !k || !v || !out || !scratch || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        !aligned16(scratch))
+        return KVC_EINVAL;
+    size_t need = 0;
+    kvc_scratch_bytes(&cache->d, n_head_q, &need);
+    if (scratch_bytes < need) return KVC_ENOSPC;
+    return launch_decode_step(*cache, layer, pos, q, k, v, dtype, n_head_q, out, static_cast<float *>(scratch),
+                              (cudaStream_t)stream);
+}
+
+int decode_step_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *q,
+                      const void *k, const void *v, int32_t dtype, int32_t n_head_q, float *out, void *scratch,
+                      size_t scratch_bytes, kvc_stream_t stream) {
+    if (!caches || !pos || n_seq < 1 || n_seq > decode_max_batch() || !dtype_ok(dtype)) return KVC_EINVAL;
+    const kvc_desc &d = caches[0].d;
+    for (int i = 0; i < n_seq; ++i) {
+        const kvc_desc &e = caches[i].d;
+        if (!cache_ok(&caches[i]) || e.n_layer != d.n_layer || e.n_ctx != d.n_ctx || e.n_head_kv != d.n_head_kv ||
+            e.head_dim != d.head_dim || e.type != d.type)
+            return KVC_EINVAL;
+    }
+    if (d.head_dim != 64 && d.head_dim != 128) return KVC_EINVAL;
+    if (n_head_q <= 0 || n_head_q % d.n_head_kv || n_head_q / d.n_head_kv > 16) return KVC_EINVAL;
+    for (int i = 0; i < n_seq; ++i)
+        if (layer < 0 || layer >= d.n_layer || pos[i] < 0 || pos[i] >= d.n_ctx) return KVC_ERANGE;
+    if (!q || !k || !v || !out || !scratch || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        !aligned16(scratch))
+        return KVC_EINVAL;
+    size_t need = 0;
+    kvc_scratch_bytes(&d, n_head_q, &need);
+    if (scratch_bytes / (size_t)n_seq < need) return KVC_ENOSPC;
+    return launch_decode_step_batch(caches, n_seq, layer, pos, q, k, v, dtype, n_head_q, out,
+                                    static_cast<float *>(scratch), need, (cudaStream_t)stream);
+}
+
 int decode_attn_noalloc(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, int32_t dtype,
                         int32_t n_head_q, float *out, kvc_stream_t stream) {
     if (!cache_ok(cache) || !dtype_ok(dtype)) return KVC_EINVAL;

@@ -13,14 +13,8 @@
 // Work split.  q8_0: one thread per 32-value block.  A warp's 32 blocks are
 // one contiguous run of input, loaded 16 bytes per lane (consecutive lanes on
 // consecutive chunks) into shared memory, from which each lane takes its own
-// block; 32 code bytes and one 2-byte scale are stored per block.  The
-// quotient x/d is taken as x times the IEEE reciprocal of d and rounded with a
-// 1.5*2^23 shift; that product is within 5e-5 of the IEEE quotient, so the
-// rounded code can differ from round(x/d) only when the product lies within
-// that distance of a .5 boundary, and exactly those values are recomputed with
-// the IEEE division (both values of a pair, the one away from the boundary
-// giving the same code either way).  The arithmetic runs on fp32 pairs.  A
-// non-finite block (outside the method's domain) stores zero codes.  f16: one
+// block; 32 code bytes and one 2-byte scale are stored per block.  The block
+// quantiser (quant.cuh) is shared with the fused decode step.  f16: one
 // thread per 8 values.  HBM-bound.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -29,6 +23,7 @@
 
 #include "kvc_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace kvc {
 namespace {
@@ -170,49 +165,15 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
     const int64_t row = blk / nb;                    // (token, head) in input order
     const int b = (int)(blk - row * nb);
     const int tok = (int)(row / H), head = (int)(row - (int64_t)tok * H);
-    float m2[2] = {0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-        m2[0] = ptx::fmax3(m2[0], fabsf(x[i]), fabsf(x[i + 1]));
-        m2[1] = ptx::fmax3(m2[1], fabsf(x[i + 2]), fabsf(x[i + 3]));
-    }
-    const float amax = fmaxf(m2[0], m2[1]);
-    const float d = __fdiv_rn(amax, 127.0f);
-    uint32_t packed[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    // codes are zero when amax/127 is zero (x/d undefined); |x * r| <= 127 (to an ulp) otherwise
-    if (d > 0.f && amax <= 3.402823466e38f) {
-        const float r = __frcp_rn(d);
-        const uint64_t r2 = ptx::f2_pack(r, r), mz = ptx::f2_pack(-0.f, -0.f), M2 = ptx::f2_pack(12582912.f, 12582912.f),
-                       nM2 = ptx::f2_pack(-12582912.f, -12582912.f), n1 = ptx::f2_pack(-1.f, -1.f);
-        int q[32];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            const uint64_t y = ptx::f2_fma(ptx::f2_pack(x[i], x[i + 1]), r2, mz);   // x * r, one rounding
-            const uint64_t t = ptx::f2_add(y, M2);                                // y rounded to an integer (to even)
-            const uint64_t f = ptx::f2_fma(ptx::f2_add(t, nM2), n1, y);              // y minus that integer
-            float t0, t1, f0, f1;
-            ptx::f2_unpack(t, t0, t1);
-            ptx::f2_unpack(f, f0, f1);
-            q[i] = __float_as_int(t0) - 0x4B400000;
-            q[i + 1] = __float_as_int(t1) - 0x4B400000;
-            if (fmaxf(fabsf(f0), fabsf(f1)) > 0.4999f) {  // near a tie: exact quotients
-                q[i] = (int)roundf(__fdiv_rn(x[i], d));
-                q[i + 1] = (int)roundf(__fdiv_rn(x[i + 1], d));
-            }
-        }
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-            packed[w] = __byte_perm(__byte_perm(q[4 * w], q[4 * w + 1], 0x0040),
-                                    __byte_perm(q[4 * w + 2], q[4 * w + 3], 0x0040), 0x5410);
-    }
+    uint32_t packed[8];
+    const uint16_t scale = q8_0_quantize32(x, packed);
     const int64_t pos = dst_of.pos(tok);
     const Geom &g = dst_of.geom(tok);
     int8_t *dst = static_cast<int8_t *>(dst_of.codes(is_v, tok)) + layer * g.c_layer + pos * g.c_tok +
                   head * g.c_head + b * 32;
     reinterpret_cast<uint4 *>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     reinterpret_cast<uint4 *>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    dst_of.scales(is_v, tok)[layer * g.s_layer + pos * g.s_tok + head * g.s_head + b] =
-        __half_as_ushort(__float2half_rn(d));
+    dst_of.scales(is_v, tok)[layer * g.s_layer + pos * g.s_tok + head * g.s_head + b] = scale;
 }
 
 // n tokens of k and v ([n][H_kv][head_dim]) to the destinations dst_of gives them; desc: their shape

@@ -46,6 +46,7 @@
 
 #include "kvc_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace kvc {
 namespace {
@@ -139,6 +140,12 @@ struct DecodeArgs {
     int layer, n_keys, group, split_len, n_split, n_head_kv;
     float scale_log2;
     uint64_t stall_ns;   // test hook (tensor-core pass): > 0 makes the MMA thread's first P wait one that runs out
+    // Fused decode step (tensor-core pass only; all null for decode_attn).  k_new / v_new: the token's
+    // K and V rows, [n_head_kv][128] in the query's dtype, stored at position n_keys - 1 of the cache
+    // (codes kq / vq, scales ks_w / vs_w) by the CTA whose split holds that position.
+    const void *k_new, *v_new;
+    void *kq, *vq;
+    uint16_t *ks_w, *vs_w;
 };
 
 // Several sequences decoded by one launch: each has its own cache (and so its own tensor maps),
@@ -515,30 +522,14 @@ __global__ void __maxnreg__(200)
     if (threadIdx.x == 0 && *s_abort) atomicExch(&g_decode_status, 1);
 }
 
-// One CTA per query head, one thread per output value.  With up to MC splits (one wave of split
-// CTAs gives at most 19 per kv head at 8 kv heads) a thread issues every split's (m, l) pair and
-// partial value at once, so the pass costs one round trip to L2 and no block barrier; more splits
-// take the same steps in rounds of 8.  The weights are ex2(m_i - M) (M the largest split maximum),
-// the denominator and the value are summed in split order, so the result is deterministic.
-template <int D, int NS>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS> cb, int group, int n_head_kv) {
+// One output value merged over the splits: split i's (m, l) at ml_src[i * ml_step] and unnormalised
+// value at o_src[i * o_step].  With up to MC splits (one wave of split CTAs gives at most 19 per kv
+// head at 8 kv heads) every load is issued at once, so the merge costs one round trip to L2; more
+// splits take the same steps in rounds of 8.  The weights are ex2(m_i - M) (M the largest split
+// maximum); the denominator and the value are summed in split order, so the result is deterministic.
+__device__ __forceinline__ float merge_splits(const float2 *ml_src, int64_t ml_step, const float *o_src, int64_t o_step,
+                                              int n_split) {
     constexpr int MC = 24;
-    const int seq = NS == 1 ? 0 : (int)blockIdx.y;
-    const float *__restrict__ part = cb.part[seq];
-    float *__restrict__ out = cb.out[seq];
-    const int n_split = cb.n_split[seq];
-    const int h = blockIdx.x, d = threadIdx.x;
-    const int hkv = h / group, row = h % group;
-    // the next kernel (the next step's append) may be scheduled now; it waits for this grid
-    asm volatile("griddepcontrol.launch_dependents;");
-    // launched as a programmatic dependent of the split pass: wait until its partials are visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const float *part_o = part;
-    const float *part_ml = part + (int64_t)n_head_kv * MAX_SPLIT * group * D;
-    const int64_t p0 = ((int64_t)hkv * MAX_SPLIT) * group + row;   // partial index of split 0
-    const float2 *ml_src = reinterpret_cast<const float2 *>(part_ml) + p0;   // split i at + i * group
-    const float *o_src = part_o + p0 * D + d;                                 // split i at + i * group * D
-    const int64_t o_step = (int64_t)group * D;
     float M = -INFINITY, L = 0.f, acc = 0.f;
     if (n_split <= MC) {
         float2 ml[MC];
@@ -546,7 +537,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS
 #pragma unroll
         for (int i = 0; i < MC; ++i) {
             if (i < n_split) {
-                ml[i] = __ldcg(ml_src + (int64_t)i * group);
+                ml[i] = __ldcg(ml_src + (int64_t)i * ml_step);
                 v[i] = __ldcg(o_src + (int64_t)i * o_step);
             } else {
                 ml[i] = make_float2(-INFINITY, 0.f);
@@ -564,14 +555,14 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS
             }
         }
     } else {
-        for (int i = 0; i < n_split; ++i) M = fmaxf(M, __ldcg(ml_src + (int64_t)i * group).x);
+        for (int i = 0; i < n_split; ++i) M = fmaxf(M, __ldcg(ml_src + (int64_t)i * ml_step).x);
         for (int i0 = 0; i0 < n_split; i0 += 8) {
             float2 ml[8];
             float v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 if (i0 + u < n_split) {
-                    ml[u] = __ldcg(ml_src + (int64_t)(i0 + u) * group);
+                    ml[u] = __ldcg(ml_src + (int64_t)(i0 + u) * ml_step);
                     v[u] = __ldcg(o_src + (int64_t)(i0 + u) * o_step);
                 } else {
                     ml[u] = make_float2(-INFINITY, 0.f);
@@ -588,7 +579,26 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS
             }
         }
     }
-    out[(int64_t)h * D + d] = acc / L;
+    return acc / L;
+}
+
+// One CTA per query head, one thread per output value (merge_splits).
+template <int D, int NS>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS> cb, int group, int n_head_kv) {
+    const int seq = NS == 1 ? 0 : (int)blockIdx.y;
+    const float *__restrict__ part = cb.part[seq];
+    float *__restrict__ out = cb.out[seq];
+    const int n_split = cb.n_split[seq];
+    const int h = blockIdx.x, d = threadIdx.x;
+    const int hkv = h / group, row = h % group;
+    // the next kernel (the next step's append) may be scheduled now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
+    // launched as a programmatic dependent of the split pass: wait until its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float *part_ml = part + (int64_t)n_head_kv * MAX_SPLIT * group * D;
+    const int64_t p0 = ((int64_t)hkv * MAX_SPLIT) * group + row;   // partial index of split 0
+    out[(int64_t)h * D + d] = merge_splits(reinterpret_cast<const float2 *>(part_ml) + p0, group,
+                                           part + p0 * D + d, (int64_t)group * D, n_split);
 }
 
 // ---- tensor-core split pass for head_dim 128 ---------------------------------------------
@@ -669,10 +679,10 @@ struct TCfg {
 // whose second block lies where no codes are, so no thread overwrites another thread's codes.
 enum TcBar {
     T_QREADY, T_QRAW, T_SFULL, T_SFREE, T_PFULL0, T_PFULL1, T_ODONE0, T_ODONE1, T_XCHG, T_DRAIN, T_DRAIN2, T_STALL,
-    T_KFULL, T_KEMPTY = T_KFULL + 4, T_VFULL = T_KEMPTY + 4, T_VEMPTY = T_VFULL + 4, T_KRAW = T_VEMPTY + 4,
+    T_APPEND, T_KFULL, T_KEMPTY = T_KFULL + 4, T_VFULL = T_KEMPTY + 4, T_VEMPTY = T_VFULL + 4, T_KRAW = T_VEMPTY + 4,
     T_VRAW = T_KRAW + 4, T_NBAR = T_VRAW + 4
 };
-static_assert(T_NBAR * 8 + 8 <= 512, "barrier area too small");
+static_assert(T_NBAR * 8 + 8 <= 512, "barrier area too small");   // + TMEM address and abort flag
 
 // byte offset of 16-byte chunk c of row r in a 128-byte-swizzled block of 128-byte rows
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
@@ -721,6 +731,57 @@ __device__ __forceinline__ void to_f32x8(const uint4 (&raw)[N], int i, float (&x
     }
 }
 
+// Fused decode step: one warp stores the token's K and V rows of kv head hkv at position n_keys - 1,
+// exactly as the append kernel does (q8_0 blocks by the shared quantiser, f16 values rounded to
+// nearest even).  q8_0: lanes 0-7 take one 32-value block each (K blocks 0-3, then V's); f16: each lane
+// takes 8 values (K on lanes 0-15, V on 16-31).  The rows are read through L2: a kernel just before
+// this one may have written them.
+template <bool Q8, int DT>
+__device__ __forceinline__ void store_new_token(const DecodeArgs &a, int hkv, int lane) {
+    constexpr int D = 128;
+    constexpr int ESZ = DT == KVC_IN_F32 ? 4 : 2;
+    const int64_t pos = a.n_keys - 1;
+    const Geom &g = a.g;
+    if constexpr (Q8) {
+        if (lane < 8) {
+            const int is_v = lane >> 2, b = lane & 3;
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(is_v ? a.v_new : a.k_new) +
+                                                               ((int64_t)hkv * D + b * 32) * ESZ);
+            constexpr int NW = 32 * ESZ / 16;   // 16-byte words of one block's input
+            uint4 raw[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) raw[i] = __ldcg(src + i);
+            float x[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float x8[8];
+                to_f32x8<DT>(raw, c, x8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[8 * c + e] = x8[e];
+            }
+            uint32_t packed[8];
+            const uint16_t scale = q8_0_quantize32(x, packed);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<int8_t *>(is_v ? a.vq : a.kq) + a.layer * g.c_layer +
+                                                   pos * g.c_tok + hkv * g.c_head + b * 32);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            (is_v ? a.vs_w : a.ks_w)[a.layer * g.s_layer + pos * g.s_tok + hkv * g.s_head + b] = scale;
+        }
+    } else {
+        const int is_v = lane >> 4, c = lane & 15;
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(is_v ? a.v_new : a.k_new) +
+                                                           ((int64_t)hkv * D + c * 8) * ESZ);
+        uint4 raw[ESZ / 2];
+#pragma unroll
+        for (int i = 0; i < ESZ / 2; ++i) raw[i] = __ldcg(src + i);
+        float x[8];
+        to_f32x8<DT>(raw, 0, x);
+        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(is_v ? a.vq : a.kq) + a.layer * g.c_layer + pos * g.c_tok +
+                                   hkv * g.c_head + c * 8) =
+            make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+    }
+}
+
 // NS: sequences of a batch the parameters hold (1, or MAX_BATCH for a batched call; grid z = sequence)
 template <bool Q8, int DT, int NS, int HS>
 __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
@@ -745,6 +806,8 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
     const int j_begin = split * a.split_len;
     const int j_end = min(a.n_keys, j_begin + a.split_len);
     const int T = (j_end - j_begin + TK - 1) / TK;   // tiles of this split
+    // fused decode step: this CTA stores the new token (at n_keys - 1, inside its last tile)
+    const bool owns_new = a.k_new != nullptr && split == a.n_split - 1;
 
     if (threadIdx.x == 0) {
         *s_abort = 0;
@@ -760,6 +823,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
         mbar_init(&bars[T_DRAIN], 1);
         mbar_init(&bars[T_DRAIN2], 1);
         mbar_init(&bars[T_STALL], 1);   // nothing arrives here: only the test hook waits on it
+        mbar_init(&bars[T_APPEND], 1);  // the new token is in the cache (fused step)
         for (int s = 0; s < L::NK; ++s) {
             mbar_init(&bars[T_KFULL + s], Q8 ? L::NDQ : 1);
             mbar_init(&bars[T_KEMPTY + s], 1);
@@ -813,6 +877,8 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
                 const int j = j_begin + k * TK;
                 const int s = k % n;
                 if (k >= n && !mbar_wait(&bars[bar_empty + s], ((k / n) - 1) & 1, s_abort)) break;
+                // the last tile holds the new token: copy it once the token is stored
+                if (owns_new && k == T - 1 && !mbar_wait(&bars[T_APPEND], 0, s_abort)) break;
                 KVC_TR(1 + (int)is_v, k);
                 uint8_t *dst = ring + s * L::OPT;
                 if constexpr (Q8) {
@@ -887,6 +953,14 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------------ PV issuer
+        if (owns_new) {
+            // fused step: store the new token first (the first P comes much later); its bytes reach the
+            // TMA copies of the last tile through the async-proxy fence and the barrier's release
+            store_new_token<Q8, DT>(a, hkv, lane);
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[T_APPEND]);
+        }
         if (lane == 0) {
             constexpr uint32_t IDESC_O = idesc_f16(128, 2 * D, 0, 1);   // A = P' (K-major), B = V (MN-major)
             const uint32_t sP = smem_u32(sm + L::OFF_P), sV = smem_u32(sm + L::OFF_V);
@@ -1130,6 +1204,8 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             // the four fp16 scales of my key's row (keys past the end: any finite scale, their codes are
             // zero-filled), loaded through L2: the append before this kernel may have written them
             auto scales = [&](int k) -> uint2 {
+                // the last tile's scales include the new token's (fused step): read them once it is stored
+                if (owns_new && k == T - 1) mbar_wait(&bars[T_APPEND], 0, s_abort);
                 const int key = min(j_begin + k * TK + t, a.n_keys - 1);
                 return __ldcg(reinterpret_cast<const uint2 *>(scl + a.layer * a.g.s_layer + hkv * a.g.s_head +
                                                                (int64_t)key * a.g.s_tok));
@@ -1188,7 +1264,7 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
 
 // The tensor-core split pass and the combine, one launch each, over n_seq sequences (NS = 1, or
 // MAX_BATCH for a batched call).  Sequence i: cache caches[i], arguments a0[i] (its q and its scratch
-// as part), output outs[i].  The sequences share the SMs evenly: one wave over (split, kv head,
+// as part), output outs[i].  A fused step (a0[i].k_new set) stores the token in the split pass.  The sequences share the SMs evenly: one wave over (split, kv head,
 // sequence), whole tiles per split.
 template <bool Q8, int DT, int NS>
 int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_head_q, float *const *outs,
@@ -1262,11 +1338,22 @@ int launch_tc(const kvc_cache *caches, const DecodeArgs *a0, int n_seq, int n_he
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 
+// The fused-step fields of a: the token's rows k and v and the cache's buffers it is stored in.
+void set_fused(DecodeArgs &a, const kvc_cache &c, const void *k, const void *v) {
+    a.k_new = k;
+    a.v_new = v;
+    a.kq = c.k_q;
+    a.vq = c.v_q;
+    a.ks_w = static_cast<uint16_t *>(c.k_s);
+    a.vs_w = static_cast<uint16_t *>(c.v_s);
+}
+
 template <int D, bool Q8, int DT>
 int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q, float *out,
-             float *scratch, cudaStream_t s) {
+             float *scratch, cudaStream_t s, const void *k_new = nullptr, const void *v_new = nullptr) {
     using L = DCfg<D, Q8>;
     DecodeArgs a;
+    memset(&a, 0, sizeof(a));
     a.q = q;
     a.ks = static_cast<const uint16_t *>(c.k_s);
     a.vs = static_cast<const uint16_t *>(c.v_s);
@@ -1279,6 +1366,7 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
     a.stall_ns = 0;
     if constexpr (D == 128) {
+        if (k_new != nullptr) set_fused(a, c, k_new, v_new);
         return launch_tc<Q8, DT, 1>(&c, &a, 1, n_head_q, &out, s);
     } else {
     // one wave: CTAS_PER_SM CTAs per SM over (split, kv head), whole stages per split
@@ -1339,11 +1427,11 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
 
 template <int D, bool Q8>
 int launch_d(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q, float *out,
-             float *scratch, cudaStream_t s) {
+             float *scratch, cudaStream_t s, const void *k_new = nullptr, const void *v_new = nullptr) {
     switch (dtype) {
-        case KVC_IN_F32: return launch_t<D, Q8, KVC_IN_F32>(c, layer, pos, q, n_head_q, out, scratch, s);
-        case KVC_IN_BF16: return launch_t<D, Q8, KVC_IN_BF16>(c, layer, pos, q, n_head_q, out, scratch, s);
-        default: return launch_t<D, Q8, KVC_IN_F16>(c, layer, pos, q, n_head_q, out, scratch, s);
+        case KVC_IN_F32: return launch_t<D, Q8, KVC_IN_F32>(c, layer, pos, q, n_head_q, out, scratch, s, k_new, v_new);
+        case KVC_IN_BF16: return launch_t<D, Q8, KVC_IN_BF16>(c, layer, pos, q, n_head_q, out, scratch, s, k_new, v_new);
+        default: return launch_t<D, Q8, KVC_IN_F16>(c, layer, pos, q, n_head_q, out, scratch, s, k_new, v_new);
     }
 }
 
@@ -1436,10 +1524,13 @@ namespace {
 
 template <bool Q8, int DT>
 int launch_batch_t(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, int n_head_q,
-                   float *out, float *scratch, size_t seq_scratch_floats, cudaStream_t s) {
+                   float *out, float *scratch, size_t seq_scratch_floats, cudaStream_t s, const void *k = nullptr,
+                   const void *v = nullptr) {
     constexpr int D = 128;
     DecodeArgs a[MAX_BATCH];
+    memset(a, 0, sizeof(a));
     float *outs[MAX_BATCH];
+    const size_t kv_bytes = (size_t)caches[0].d.n_head_kv * D * dtype_bytes(DT);
     const size_t q_bytes = (size_t)n_head_q * D * dtype_bytes(DT);
     for (int i = 0; i < n_seq; ++i) {
         const kvc_cache &c = caches[i];
@@ -1456,6 +1547,8 @@ int launch_batch_t(const kvc_cache *caches, int n_seq, int layer, const int *pos
         a[i].scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
         a[i].stall_ns = 0;
         outs[i] = out + (size_t)i * n_head_q * D;
+        if (k != nullptr)
+            set_fused(a[i], c, static_cast<const uint8_t *>(k) + i * kv_bytes, static_cast<const uint8_t *>(v) + i * kv_bytes);
     }
     return launch_tc<Q8, DT, MAX_BATCH>(caches, a, n_seq, n_head_q, outs, s);
 }
@@ -1498,6 +1591,48 @@ int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dty
                   : launch_d<128, false>(c, layer, pos, q, dtype, n_head_q, out, scratch, s);
     return q8 ? launch_d<64, true>(c, layer, pos, q, dtype, n_head_q, out, scratch, s)
               : launch_d<64, false>(c, layer, pos, q, dtype, n_head_q, out, scratch, s);
+}
+
+int launch_decode_step(const kvc_cache &c, int layer, int pos, const void *q, const void *k, const void *v, int dtype,
+                       int n_head_q, float *out, float *scratch, cudaStream_t s) {
+    const bool q8 = c.d.type == KVC_Q8_0;
+    if (c.d.head_dim == 128)
+        return q8 ? launch_d<128, true>(c, layer, pos, q, dtype, n_head_q, out, scratch, s, k, v)
+                  : launch_d<128, false>(c, layer, pos, q, dtype, n_head_q, out, scratch, s, k, v);
+    // head_dim 64: the append, then decode_attn's split pass and combine
+    const int rc = launch_append(c, layer, pos, 1, k, v, dtype, s);
+    return rc != KVC_OK ? rc : launch_decode(c, layer, pos, q, dtype, n_head_q, out, scratch, s);
+}
+
+int launch_decode_step_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, const void *k,
+                             const void *v, int dtype, int n_head_q, float *out, float *scratch,
+                             size_t seq_scratch_bytes, cudaStream_t s) {
+    const kvc_desc &d = caches[0].d;
+    const size_t seq_floats = seq_scratch_bytes / sizeof(float);
+    if (n_seq == 1 || d.head_dim != 128) {
+        const size_t q_bytes = (size_t)n_head_q * d.head_dim * dtype_bytes(dtype);
+        const size_t kv_bytes = (size_t)d.n_head_kv * d.head_dim * dtype_bytes(dtype);
+        for (int i = 0; i < n_seq; ++i) {
+            const int rc = launch_decode_step(caches[i], layer, pos[i], static_cast<const uint8_t *>(q) + i * q_bytes,
+                                              static_cast<const uint8_t *>(k) + i * kv_bytes,
+                                              static_cast<const uint8_t *>(v) + i * kv_bytes, dtype, n_head_q,
+                                              out + (size_t)i * n_head_q * d.head_dim, scratch + i * seq_floats, s);
+            if (rc != KVC_OK) return rc;
+        }
+        return KVC_OK;
+    }
+    const bool q8 = d.type == KVC_Q8_0;
+    switch (dtype) {
+        case KVC_IN_F32:
+            return q8 ? launch_batch_t<true, KVC_IN_F32>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s, k, v)
+                      : launch_batch_t<false, KVC_IN_F32>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s, k, v);
+        case KVC_IN_BF16:
+            return q8 ? launch_batch_t<true, KVC_IN_BF16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s, k, v)
+                      : launch_batch_t<false, KVC_IN_BF16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s, k, v);
+        default:
+            return q8 ? launch_batch_t<true, KVC_IN_F16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s, k, v)
+                      : launch_batch_t<false, KVC_IN_F16>(caches, n_seq, layer, pos, q, n_head_q, out, scratch, seq_floats, s, k, v);
+    }
 }
 
 }  // namespace kvc

@@ -32,6 +32,7 @@ inline Geom geom_of(const kvc_desc &d) {
 
 inline int dtype_bytes(int dtype) { return dtype == KVC_IN_F32 ? 4 : 2; }
 
+
 // A 3-D tiled TMA tensor map (dims innermost first, strides of dims 1 and 2 in bytes); false when
 // the driver entry point is missing or the encoding is rejected.
 bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
@@ -55,6 +56,11 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
 int decode_max_split();
 int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                   float *out, float *scratch, cudaStream_t s);
+int launch_decode_step(const kvc_cache &c, int layer, int pos, const void *q, const void *k, const void *v, int dtype,
+                       int n_head_q, float *out, float *scratch, cudaStream_t s);
+int launch_decode_step_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, const void *k,
+                             const void *v, int dtype, int n_head_q, float *out, float *scratch,
+                             size_t seq_scratch_bytes, cudaStream_t s);
 int decode_max_batch();
 int launch_decode_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, int dtype,
                         int n_head_q, float *out, float *scratch, size_t seq_scratch_bytes, cudaStream_t s);

@@ -110,8 +110,9 @@ typedef struct {
  * Returns KVC_EINVAL for an invalid descriptor. */
 int kvc_cache_bytes(const kvc_desc *desc, size_t *k_q, size_t *k_s, size_t *v_q, size_t *v_s);
 
-/* Bytes of the scratch buffer decode_attn needs for this cache and n_head_q:
- * float32 partial results of the split-K pass, [n_head_q][max_split][head_dim + 2]. */
+/* Bytes of the scratch buffer decode_attn and decode_step need for this cache
+ * and n_head_q: float32 partial results of the split-K pass,
+ * [n_head_q][max_split][head_dim + 2]. */
 int kvc_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, size_t *bytes);
 
 /* Bytes of the serialised state of n_tokens positions: 32 + n_layer * n_tokens *
@@ -227,6 +228,38 @@ int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *
 int decode_attn_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *q,
                       int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
                       kvc_stream_t stream);
+
+/* One decode step in one call: store the token's K/V at position pos, exactly
+ * as kv_cache_append(cache, layer, pos, 1, k, v, dtype) does (the same bytes),
+ * then attend with its query over positions [0, pos] exactly as decode_attn
+ * does (the same bits of out).  This is the per-token work of generation, which
+ * the pages time as "generation t/s" (llama.cpp PR #58 "completion : allow the
+ * prompt to be processed under its own split mode", section "Why"; llama.cpp
+ * PR #59 "llama : switch the split mode of a live context", section "Why").
+ * q: [n_head_q][head_dim], k and v: [n_head_kv][head_dim], all device memory
+ * in `dtype`, 16-byte aligned; out: [n_head_q][head_dim] float32.
+ * With head_dim 128 it is two kernels: the split pass, in which the CTA whose
+ * key range holds pos quantises and stores the token before it copies that
+ * tile, then decode_attn's combine.  With head_dim 64 the append and
+ * decode_attn's two kernels run in turn.  scratch: as for decode_attn
+ * (kvc_scratch_bytes, no initialisation); calls on one scratch buffer must not
+ * overlap on the GPU.  Errors: KVC_EINVAL (null or unaligned pointers, dtype,
+ * head_dim, heads), KVC_ERANGE (layer, pos), KVC_ENOSPC (scratch too small). */
+int decode_step(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, const void *k, const void *v,
+                int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes, kvc_stream_t stream);
+
+/* decode_step for n_seq sequences in one call (1 <= n_seq <= 8): sequence i
+ * stores row i of k and v at position pos[i] of caches[i] and attends with row
+ * i of q, as decode_step would.  caches, pos: host arrays as for
+ * decode_attn_batch.  q: [n_seq][n_head_q][head_dim]; k, v: [n_seq][n_head_kv]
+ * [head_dim]; out: [n_seq][n_head_q][head_dim] float32.  scratch: as for
+ * decode_attn_batch.  With head_dim 128 the sequences share one split pass and
+ * one combine (decode_attn_batch's kernels, whose split boundaries it shares,
+ * so out matches decode_attn_batch bit for bit); otherwise each sequence is its
+ * own decode_step.  Errors as decode_attn_batch. */
+int decode_step_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *q,
+                      const void *k, const void *v, int32_t dtype, int32_t n_head_q, float *out, void *scratch,
+                      size_t scratch_bytes, kvc_stream_t stream);
 
 /* decode_attn without a scratch argument, for callers that cannot allocate
  * device memory themselves (code hosted by an engine that owns every device

@@ -148,6 +148,20 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     assert kvc.lib.decode_attn_batch(nine, 3, 0, p9, k, 1, 4, k, k, 3 * one.value - 16, S) == kvc.KVC_ENOSPC
     mixed = (kvc.kvc_cache * 2)(cb, c)                                                            # head_dim 128 and 64
     assert kvc.lib.decode_attn_batch(mixed, 2, 0, p9, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL
+    # the fused step: decode_attn's checks plus k and v
+    assert kvc.lib.decode_step(ctypes.byref(c), 0, 64, k, k, k, 1, 4, k, k, big, S) == kvc.KVC_ERANGE      # pos
+    assert kvc.lib.decode_step(ctypes.byref(c), 2, 5, k, k, k, 1, 4, k, k, big, S) == kvc.KVC_ERANGE       # layer
+    assert kvc.lib.decode_step(ctypes.byref(c), 0, 5, k, None, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL    # k
+    assert kvc.lib.decode_step(ctypes.byref(c), 0, 5, k, k, ctypes.c_void_p(0x40008), 1, 4, k, k, big, S) == \
+        kvc.KVC_EINVAL                                                                                    # unaligned v
+    assert kvc.lib.decode_step(ctypes.byref(c), 0, 5, k, k, k, 1, 3, k, k, big, S) == kvc.KVC_EINVAL       # n_head_q
+    assert kvc.lib.decode_step(ctypes.byref(c), 0, 5, k, k, k, 7, 4, k, k, big, S) == kvc.KVC_EINVAL       # dtype
+    assert kvc.lib.decode_step(ctypes.byref(c), 0, 5, k, k, k, 1, 4, k, k, 100, S) == kvc.KVC_ENOSPC
+    assert kvc.lib.decode_step_batch(nine, 9, 0, p9, k, k, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL    # n_seq > 8
+    assert kvc.lib.decode_step_batch(nine, 2, 0, bad, k, k, k, 1, 4, k, k, big, S) == kvc.KVC_ERANGE   # pos[1]
+    assert kvc.lib.decode_step_batch(mixed, 2, 0, p9, k, k, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL
+    assert kvc.lib.decode_step_batch(nine, 2, 0, p9, k, None, k, 1, 4, k, k, big, S) == kvc.KVC_EINVAL
+    assert kvc.lib.decode_step_batch(nine, 3, 0, p9, k, k, k, 1, 4, k, k, 3 * one.value - 16, S) == kvc.KVC_ENOSPC
     # batched append
     assert kvc.lib.kv_cache_append_batch(nine, 9, 0, p9, k, k, 1, S) == kvc.KVC_EINVAL           # n_seq > 8
     assert kvc.lib.kv_cache_append_batch(nine, 2, 0, bad, k, k, 1, S) == kvc.KVC_ERANGE          # pos[1] = n_ctx

@@ -68,6 +68,29 @@ def test_decode_wait_that_gives_up_then_next_call_is_correct(kvc, cache_type):
 
 
 @pytest.mark.parametrize("cache_type", ["q8_0", "f16"])
+def test_decode_step_wait_that_gives_up_then_next_step_is_correct(kvc, cache_type):
+    # the fused step: the split pass gives up (after the token was stored); the next steps on the same
+    # cache and scratch are correct
+    w = si.small_workload("failstep", 40, 8, 128, cache_type, "bf16", n_prompt=5000, chunk=5000, n_decode=2, seed=37)
+    q, k, v = si.layer_qkv(w, 0)
+    g = kvc.KVCache(1, w.n_ctx, w.n_head_kv, w.head_dim, cache_type, "head_major")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    kvc.kv_cache_append(g, 0, 0, kd[:5000], vd[:5000])
+    o = OracleCache(1, w.n_ctx, w.n_head_kv, w.head_dim, cache_type)
+    o.append(0, 0, np32(k[:5000]), np32(v[:5000]))
+    scratch = torch.empty(g.scratch_bytes(w.n_head_q), dtype=torch.uint8, device="cuda")
+    kvc.arm_test_wait_timeout(kvc.TEST_DECODE, LIMIT_NS)
+    kvc.decode_step(g, 0, 5000, qd[5000], kd[5000], vd[5000], scratch=scratch)
+    rc, status = _status_code(kvc)
+    assert rc == kvc.KVC_EDEVICE and status != 0, (rc, status)
+    for p in (5000, 5001):                                 # the aborted step again, then the next one
+        out = kvc.decode_step(g, 0, p, qd[p], kd[p], vd[p], scratch=scratch)
+        o.append(0, p, np32(k[p:p + 1]), np32(v[p:p + 1]))
+        assert_close(out.cpu().numpy(), o.decode(0, p, np32(q[p])), "step after the abort, pos %d" % p)
+    assert kvc.kvc_device_status() == 0
+
+
+@pytest.mark.parametrize("cache_type", ["q8_0", "f16"])
 def test_prefill_wait_that_gives_up_then_next_call_is_correct(kvc, cache_type):
     w, q, g, o = _filled(kvc, cache_type, 3000)
     assert kvc.kvc_device_status() == 0
