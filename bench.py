@@ -67,18 +67,18 @@ TRAFFIC = {
     # the step's 29 attention calls (dequantising pass, attention, split merge), mean per call
     "prefill": {"sources": {"prefill.cu": "900fe085b81b05bd"},
                 "q8_0_58k": (535487390, "mean per call over the 29 chunk calls of one step (all three kernels)")},
-    "append_chunk": {"sources": {"append.cu": "a6f9e705a1d20ea1"},
-                     "q8_0_58k": (8411981, "one 2048-token chunk append (writes still in L2 at the launch end)")},
-    "append_prompt": {"sources": {"append.cu": "a6f9e705a1d20ea1"},
-                      "q8_0_58k": (330838784, "the 58,300-token prompt in one append")},
-    "decode_attn": {"sources": {"decode.cu": "c86cba417ecffa5b"},
-                    "q8_0_58k": (128015770, "split pass + combine at position 58,555")},
-    "decode_step": {"sources": {"decode.cu": "c86cba417ecffa5b", "append.cu": "a6f9e705a1d20ea1"},
-                    "q8_0_58k": (128079130, "append + split pass + combine at position 58,555")},
+    "append_chunk": {"sources": {"append.cu": "aa88d8f25b17248a", "quant.cuh": "356d3631d0d7a4c9"},
+                     "q8_0_58k": (8412211, "one 2048-token chunk append (writes still in L2 at the launch end)")},
+    "append_prompt": {"sources": {"append.cu": "aa88d8f25b17248a", "quant.cuh": "356d3631d0d7a4c9"},
+                      "q8_0_58k": (330845388, "the 58,300-token prompt in one append")},
+    "decode_attn": {"sources": {"decode.cu": "0ab01a08513ab5fd"},
+                    "q8_0_58k": (128083532, "split pass + combine at position 58,555")},
+    "decode_step": {"sources": {"decode.cu": "0ab01a08513ab5fd", "quant.cuh": "356d3631d0d7a4c9"},
+                    "q8_0_58k": (128028697, "split pass storing the token + combine at position 58,555")},
     "state_pack": {"sources": {"state.cu": "e0853a7210054393"},
-                   "q8_0_58k": (201684634, "header + pack of 58,556 tokens")},
+                   "q8_0_58k": (201607961, "header + pack of 58,556 tokens")},
     "state_unpack": {"sources": {"state.cu": "e0853a7210054393"},
-                     "q8_0_58k": (202314982, "unpack of 58,556 tokens")},
+                     "q8_0_58k": (202267392, "unpack of 58,556 tokens")},
 }
 
 
