@@ -617,8 +617,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineBatch<NS
 // probabilities at its keys' positions within their half and zeros elsewhere (cleared once at the
 // start, never written there again), so O' row r accumulates exactly its keys: the columns of the
 // row's own half (0..127 for keys 0..63, 128..255 for keys 64..127) hold sum_j p_j V_j, the other
-// half is unused.  At the end the eight rows of each head are merged (in replica order) into the
-// split's (m, l, O) partial.  A thread rescales its own O' row when its running max grows by more
+// half is unused.  At the end the replicas of each head are merged (inside each warp by shuffles, then
+// across the four warps) into the split's (m, l, O) partial.  A thread rescales its own O' row when its running max grows by more
 // than 2^8.
 //   warp 0      one lane copies the group's query rows (one bulk copy, first in the queue), then loads
 //               K tiles (f16) or their int8 codes (q8_0) by TMA
@@ -663,10 +663,10 @@ struct TCfg {
     static constexpr int USED = OFF_BAR + 512;
     static constexpr int ALLOC = USED + 1024;
     static_assert(ALLOC <= 232448, "shared memory plan too large");
-    // the merge at the end reuses the K ring (128 rows of 128 floats) and P' buffer 0 (m and l)
+    // the merge at the end reuses the K ring (a row of D + 4 floats per warp and head slot) and P' buffer 0
+    // (their maxima and sums)
     static constexpr int OFF_MRG = OFF_K;
     static constexpr int OFF_ML = OFF_P;
-    static_assert(128 * D * 4 <= NK * OPT && 128 * 8 <= PB, "merge area must fit in the freed buffers");
     static constexpr int NDQ = 128;                         // dequantising threads per K or V (q8_0)
     static constexpr int THREADS = Q8 ? 512 : 256;
     static constexpr int CTAS = 1;                          // CTAs per SM (all 512 TMEM columns)
@@ -1011,17 +1011,19 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             ok = mbar_wait(&bars[T_QRAW], 0, s_abort);
             uint8_t *qt = sm + L::OFF_Q;
             constexpr int QW = DT == KVC_IN_F32 ? 2 : 1;        // 16-byte words per 8 values
-            const uint8_t *qs = sm + L::OFF_QS + h * D * (DT == KVC_IN_F32 ? 4 : 2);
+            // 8 stored rows: thread r converts chunk r / 8 of row r % 8; 128 rows: thread r its own row
+            const int qrow = HS == 8 ? (r & 7) : r, qslot = qrow % HS;
+            const uint8_t *qs = sm + L::OFF_QS + qslot * D * (DT == KVC_IN_F32 ? 4 : 2);
 #pragma unroll 4
-            for (int cc = 0; cc < (r < L::QROWS ? D / 8 : 0); ++cc) {
+            for (int cc = HS == 8 ? (r >> 3) : 0; cc < (HS == 8 ? (r >> 3) + 1 : D / 8); ++cc) {
                 uint4 raw[QW];
 #pragma unroll
                 for (int i = 0; i < QW; ++i)
-                    raw[i] = (ok && h < G) ? *reinterpret_cast<const uint4 *>(qs + (cc * QW + i) * 16)
-                                           : make_uint4(0u, 0u, 0u, 0u);
+                    raw[i] = (ok && qslot < G) ? *reinterpret_cast<const uint4 *>(qs + (cc * QW + i) * 16)
+                                               : make_uint4(0u, 0u, 0u, 0u);
                 float x[8];
                 to_f32x8<DT>(raw, 0, x);
-                *reinterpret_cast<uint4 *>(qt + (cc >> 3) * L::QBLK + sw128(r, cc & 7)) =
+                *reinterpret_cast<uint4 *>(qt + (cc >> 3) * L::QBLK + sw128(qrow, cc & 7)) =
                     make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
                                pack_half2(x[6], x[7]));
             }
@@ -1126,30 +1128,58 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             mbar_arrive(&bars[T_PFULL0 + k % L::NP]);
             if (threadIdx.x == 128) KVC_TR(9, k);
         }
-        // ---- epilogue: the rows of real heads store (m, l, O) in shared memory (the operand rings are
-        // free once the last PV has completed); then each warp merges whole heads, a lane per four head
-        // dims, the replicas taken in order
+        // ---- epilogue (the operand rings are free once the last PV has completed).  The replicas of each
+        // head slot are merged first inside the warp - lanes h, h + HS, ... hold slot h's replicas - by a
+        // reduce-scatter over shuffles that leaves each lane a quarter (8 slots) or half (16 slots) of the
+        // slot's columns, written to shared memory; then across the four warps, one warp per head and a
+        // lane per four head dims.  The orders are fixed, so the result is deterministic.
         if (threadIdx.x == 128) KVC_TR(0, 3);
-        float *mrg = reinterpret_cast<float *>(sm + L::OFF_MRG);   // [row][128], float4 chunks rotated
-        float *mls = reinterpret_cast<float *>(sm + L::OFF_ML);    // [row][2]
-        if (ok && T > 0 && wait_pv(T - 1)) {
+        constexpr int RW = 32 / HS;                  // replicas of a head slot in one warp (4 or 2)
+        constexpr int WROW = D + 4;                  // floats per (warp, slot) row in shared memory
+        float *wm = reinterpret_cast<float *>(sm + L::OFF_MRG);   // [quarter][slot][WROW]
+        float *wml = reinterpret_cast<float *>(sm + L::OFF_ML);   // [quarter][slot][2]: (max, sum)
+        static_assert(4 * HS * WROW * 4 <= L::NK * L::OPT && 4 * HS * 8 <= L::PB, "merge areas too small");
+        bool have = ok && T > 0 && wait_pv(T - 1);
+        have = __all_sync(0xffffffffu, have);        // the shuffles below need the whole warp
+        if (have) {
+            float mw = m_run;
+#pragma unroll
+            for (int off = HS; off < 32; off <<= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
+            const float w = m_run == -INFINITY ? 0.f : ex2(m_run - mw);
+            float lw = w * l_run;
+#pragma unroll
+            for (int off = HS; off < 32; off <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+            float *dst = wm + (quarter * HS + h) * WROW;
+            const bool up16 = (lane & 16) != 0, up8 = (lane & 8) != 0;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tmem + COL_O + 128 * hf + 32 * c + lane_base, o);
                 tmem_ld_wait();
-                if (h < G) {
+                // lanes 16 apart: the lower keeps columns 0-15 of the chunk, the upper 16-31
+                float k1[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int ch = c * 8 + e;
-                        *reinterpret_cast<float4 *>(mrg + r * D + 4 * (ch ^ (r & 31))) =
-                            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                        __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
-                    }
+                for (int e = 0; e < 16; ++e) {
+                    const float lo = __uint_as_float(o[e]) * w, hi = __uint_as_float(o[e + 16]) * w;
+                    k1[e] = (up16 ? hi : lo) + __shfl_xor_sync(0xffffffffu, up16 ? lo : hi, 16);
+                }
+                if constexpr (RW == 4) {
+                    // lanes 8 apart: the lower keeps 8 of those 16 columns, the upper the other 8
+                    float k2[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        k2[e] = (up8 ? k1[e + 8] : k1[e]) + __shfl_xor_sync(0xffffffffu, up8 ? k1[e] : k1[e + 8], 8);
+                    float *d8 = dst + 32 * c + 16 * up16 + 8 * up8;
+                    *reinterpret_cast<float4 *>(d8) = make_float4(k2[0], k2[1], k2[2], k2[3]);
+                    *reinterpret_cast<float4 *>(d8 + 4) = make_float4(k2[4], k2[5], k2[6], k2[7]);
+                } else {
+                    float *d16 = dst + 32 * c + 16 * up16;
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(d16 + e) = make_float4(k1[e], k1[e + 1], k1[e + 2], k1[e + 3]);
                 }
             }
-            mls[2 * r] = m_run;
-            mls[2 * r + 1] = l_run;
+            if (lane < HS) *reinterpret_cast<float2 *>(wml + 2 * (quarter * HS + h)) = make_float2(mw, lw);
         } else {
             ok = false;
         }
@@ -1161,22 +1191,24 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
             float *part_o = a.part;
             float *part_ml = a.part + (int64_t)a.n_head_kv * MAX_SPLIT * G * D;
             for (int hh = quarter; hh < G; hh += 4) {
+                float2 ml[4];
                 float M = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < NREP; ++q) M = fmaxf(M, mls[2 * (HS * q + hh)]);
+                for (int q = 0; q < 4; ++q) {
+                    ml[q] = *reinterpret_cast<const float2 *>(wml + 2 * (q * HS + hh));
+                    M = fmaxf(M, ml[q].x);
+                }
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 float lsum = 0.f;
 #pragma unroll
-                for (int q = 0; q < NREP; ++q) {
-                    const int row = HS * q + hh;
-                    const float2 ml = *reinterpret_cast<const float2 *>(mls + 2 * row);
-                    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-                    lsum += w * ml.y;
-                    const float4 v = *reinterpret_cast<const float4 *>(mrg + row * D + 4 * (lane ^ (row & 31)));
-                    acc.x += w * v.x;
-                    acc.y += w * v.y;
-                    acc.z += w * v.z;
-                    acc.w += w * v.w;
+                for (int q = 0; q < 4; ++q) {
+                    const float wq = ml[q].x == -INFINITY ? 0.f : ex2(ml[q].x - M);
+                    lsum += wq * ml[q].y;
+                    const float4 v = *reinterpret_cast<const float4 *>(wm + (q * HS + hh) * WROW + 4 * lane);
+                    acc.x += wq * v.x;
+                    acc.y += wq * v.y;
+                    acc.z += wq * v.z;
+                    acc.w += wq * v.w;
                 }
                 *reinterpret_cast<float4 *>(part_o + (pbase + hh) * D + 4 * lane) = acc;
                 if (lane == 0) *reinterpret_cast<float2 *>(part_ml + (pbase + hh) * 2) = make_float2(M, lsum);
