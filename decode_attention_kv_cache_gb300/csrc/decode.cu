@@ -846,6 +846,18 @@ __global__ void __launch_bounds__(TCfg<Q8, HS>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    if ((warp == 0 || warp == 3) && lane == 0) {
+        // the ring's first tiles into L2 while the kernel before this one finishes (a hint, safe before the
+        // wait; prefetching further ahead inside the loop measured slower)
+        const int kv = warp == 3, n = kv ? L::NV : L::NK;
+        for (int k = 0; k < T && k < n; ++k) {
+            const int j = j_begin + k * TK;
+            for (int cb = 0; cb < (Q8 ? 1 : 2); ++cb) {
+                if (!kv) tma_prefetch_l2_3d(tm_k, cb * 64, j, hkv);
+                else for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(tm_v, cb * 64, j + hf * TKH, hkv);
+            }
+        }
+    }
     // inputs written by the kernels before this one are read only past this point
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");

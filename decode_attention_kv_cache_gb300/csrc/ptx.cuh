@@ -77,6 +77,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// A hint: bring one box of a 3-D tensor into L2.  It moves no data into the SM and completes on
+// nothing; a later load still reads whatever memory holds by then (L2 is the point of coherence), so it
+// may be issued before the data's producer has finished.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to shared
 // memory, completing on `bar` (tx bytes).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
