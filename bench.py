@@ -2,7 +2,7 @@
 """Benchmark of the attention-over-KV-cache hot path on GB300.
 
 One step = one request on every layer of the workload: the prompt prefilled in
-chunks (kv_cache_append + prefill_chunk_attn per chunk), the decode steps
+chunks (prefill_step per chunk: the chunk's store, then the attention), the decode steps
 (decode_step per token: the split pass stores the token and attends, then the
 combine; the loop captured once in a CUDA graph), then the cache state serialised from the head-major cache
 (kv_state_get) and restored into a layer-major cache (kv_state_set).
@@ -250,17 +250,15 @@ class GpuRequest:
         return layer if self.w.n_layer == 1 else 0
 
     def launches_per_step(self):
-        """Kernels one step launches: per chunk an append and the attention (q8_0: and the pass that
-        dequantises the attended keys into the prefill scratch), plus the split merge when
-        the chunk's last row reaches past the first key split; per decode step the split pass (which
-        stores the token) and the combine (head_dim 64: also the append); the state header, pack and
-        unpack."""
+        """Kernels one step launches: per chunk two (prefill_step: the chunk's store, with the fp16 copy
+        for q8_0, then the attention) plus the split merge when the chunk's last row reaches past the
+        first key split; per decode step the split pass (which stores the token) and the combine
+        (head_dim 64: also the append); the state header, pack and unpack."""
         w = self.w
         keys = prefill_split_keys(w.n_ctx)
         merges = sum(1 for p, c in self.chunks if p + c - 1 >= keys)
-        per_chunk = 3 if w.cache == "q8_0" else 2
         per_decode = 2 if w.head_dim == 128 else 3
-        return w.n_layer * (per_chunk * len(self.chunks) + merges + per_decode * w.n_decode) + 3
+        return w.n_layer * (2 * len(self.chunks) + merges + per_decode * w.n_decode) + 3
 
     def _decode_loop(self, layer):
         kvc, w = self.kvc, self.w
@@ -271,15 +269,15 @@ class GpuRequest:
                             scratch=self.scratch)
 
     def attention_only(self):
-        """Every chunk's attention call of every layer, back to back over the filled cache, as the
-        step issues them but without the appends between them (the roofline's timing of the kernel
-        with no event between two launches)."""
+        """Every chunk's prefill_step of every layer, back to back, as the step issues them (the
+        roofline's timing of the attention with no event between two launches; each call also stores
+        its chunk again, the same bytes, and for q8_0 writes the fp16 copy the attention reads)."""
         kvc, w = self.kvc, self.w
         for layer in range(w.n_layer):
-            q = self.dev_in[layer][0]
+            q, k, v = self.dev_in[layer]
             for p, c in self.chunks:
-                kvc.prefill_chunk_attn(self.src, layer, p, q[p:p + c], out=self.out_p[self.out_slot(layer), p:p + c],
-                                       scratch=self.pscratch)
+                kvc.prefill_step(self.src, layer, p, q[p:p + c], k[p:p + c], v[p:p + c],
+                                 out=self.out_p[self.out_slot(layer), p:p + c], scratch=self.pscratch)
 
     def capture(self):
         """Capture each layer's decode loop in a CUDA graph (after one eager run)."""
@@ -305,11 +303,10 @@ class GpuRequest:
             if ev is not None:
                 e0 = E(enable_timing=True); e0.record(); ev["prefill"].append([e0])
             for ci, (p, c) in enumerate(self.chunks):
-                kvc.kv_cache_append(self.src, layer, p, k[p:p + c], v[p:p + c])
                 if ev is not None:
                     a = E(enable_timing=True); a.record()
-                kvc.prefill_chunk_attn(self.src, layer, p, q[p:p + c], out=self.out_p[self.out_slot(layer), p:p + c],
-                                       scratch=self.pscratch)
+                kvc.prefill_step(self.src, layer, p, q[p:p + c], k[p:p + c], v[p:p + c],
+                                 out=self.out_p[self.out_slot(layer), p:p + c], scratch=self.pscratch)
                 if ev is not None:
                     b = E(enable_timing=True); b.record(); ev["attn"].append((a, b, self.flops[ci]))
             if ev is not None:
@@ -435,13 +432,14 @@ def run_gpu(args, rank, world, local):
     traffic, traffic_launch = recorded_traffic("prefill", w.name)
     achieved = attn_flops / (chain_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    roof = {"kernel": "prefill_chunk_attn (tcgen05 f16 x f16 -> f32)", "bound": "tensor",
+    roof = {"kernel": "prefill attention (prefill_step; tcgen05 f16 x f16 -> f32)", "bound": "tensor",
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "peak_source": "%s dense bf16 burst (f16 runs at the bf16 rate)" % peak_src,
             "traffic": traffic, "traffic_launch": traffic_launch, "launches": n_attn // K,
             "avg_launch_ms": chain_ms / n_attn,
-            "timed": "the step's attention calls back to back (attention and split-merge kernels, "
-                     "L2 flushed before each pass), CUDA events at the ends of each pass",
+            "timed": "the step's prefill_step calls back to back (each: the chunk's store, with the fp16 "
+                     "copy for q8_0, the attention and the split merge; L2 flushed before each pass), CUDA "
+                     "events at the ends of each pass",
             "achieved_calls_between_events": attn_flops / (attn_ms / 1e3) / 1e12,
             "algorithmic_flops_per_step": attn_flops / K}
     bt = cache_bytes_per_token(w)
@@ -502,6 +500,8 @@ def kernel_rooflines(kvc, torch, w, req, flush, reps, peak_gbs, peak_src):
 
     def obj(name, nbytes, fn, what):
         pairs = []
+        fn()   # untimed: the first launch of a kernel also loads its module
+        torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("kvc_kernel_" + name)
         for _ in range(reps):
             l2_flush(torch, flush)
@@ -673,7 +673,7 @@ def end_to_end(kvc, torch, w, req, device, rank, world, K, flush):
 
 
 def chunk_sweep(kvc, torch, w, req, device, flush, reps):
-    """Prefill time (appends + attention, L2 flushed before each) of the same prompt under each
+    """Prefill time (prefill_step calls, L2 flushed before each) of the same prompt under each
     chunking, and the fit T = b * chunks + a * tokens: b is this layer's fixed cost per chunk and a
     its cost per token, the two numbers the pipeline chunk rule takes as b/a."""
     import numpy as np

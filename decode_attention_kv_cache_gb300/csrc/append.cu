@@ -28,30 +28,6 @@
 namespace kvc {
 namespace {
 
-template <int DT>
-__device__ __forceinline__ void load8(const void *base, int64_t idx, float (&x)[8]) {
-    if constexpr (DT == KVC_IN_F32) {
-        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + idx);
-        float4 a = __ldcg(p), b = __ldcg(p + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
-        uint4 u = __ldcg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + idx));
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if constexpr (DT == KVC_IN_BF16) {
-                // bf16 -> f32 is exact: the bf16 bits are the top half of the f32
-                x[2 * i] = __uint_as_float(w[i] << 16);
-                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            } else {
-                x[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFF)));
-                x[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
-            }
-        }
-    }
-}
-
 // Where input token t goes: one cache, token t at position pos0 + t ...
 struct OneCache {
     void *kq, *vq;
@@ -95,7 +71,7 @@ __global__ void __launch_bounds__(256) append_f16_kernel(
     const int head = rem / units_per_head;
     const int c = rem % units_per_head;  // which 8-value group along head_dim
     float x[8];
-    load8<DT>(is_v ? v : k, u * 8, x);
+    load_inputs8<DT>(is_v ? v : k, u * 8, x);
     const int64_t pos = dst_of.pos(tok);
     const Geom &g = dst_of.geom(tok);
     const int64_t code_off = layer * g.c_layer + pos * g.c_tok + head * g.c_head + (int64_t)c * 8;

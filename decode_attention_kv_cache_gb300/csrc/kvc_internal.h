@@ -53,6 +53,9 @@ int launch_append_batch(const kvc_cache *caches, int n_seq, int layer, const int
 size_t prefill_scratch_bytes(const kvc_desc &d, int n_head_q, int max_tokens);
 int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, int dtype,
                    int n_head_q, float *out, void *scratch, size_t scratch_bytes, cudaStream_t s);
+int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, const void *k,
+                        const void *v, int dtype, int n_head_q, float *out, void *scratch, size_t scratch_bytes,
+                        cudaStream_t s);
 int decode_max_split();
 int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                   float *out, float *scratch, cudaStream_t s);

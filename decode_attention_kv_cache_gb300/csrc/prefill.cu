@@ -60,6 +60,7 @@
 
 #include "kvc_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace kvc {
 
@@ -203,6 +204,32 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+
+// One row's split partials merged: out = sum_s w_s O_s / sum_s w_s l_s, w_s = 2^(m_s - max_s m_s), the
+// splits taken in split order; the four output values at columns c4 .. c4 + 3 of the row whose split-0
+// partial starts at `base` (split s at base + s * sstride).
+template <int D>
+__device__ __forceinline__ float4 merge_row4(const float *base, int64_t sstride, int ns, int c4) {
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride + D));
+    float Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) {
+        const float *ps = base + s * sstride;
+        const float ms = __ldcg(ps + D), ls = __ldcg(ps + D + 1);
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(ps + c4));
+        const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
+        Lsum = fmaf(w, ls, Lsum);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    const float inv_l = 1.f / Lsum;
+    return make_float4(acc.x * inv_l, acc.y * inv_l, acc.z * inv_l, acc.w * inv_l);
 }
 
 template <int D, bool Q8, int QDT>
@@ -721,8 +748,7 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     }
 }
 
-// Merge of the key splits: out = sum_s w_s O_s / sum_s w_s l_s, w_s = 2^(m_s - max_s m_s), the
-// splits taken in split order.  A group of D/4 threads per row, 4 columns each; a block covers
+// Merge of the key splits (merge_row4).  A group of D/4 threads per row, 4 columns each; a block covers
 // 256 / (D/4) rows of one unit.
 template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
@@ -739,28 +765,9 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
     const int r = rb * RPB + threadIdx.x / TPR, c4 = (threadIdx.x % TPR) * 4;
     const int row = qt * BM + r;
     if (row >= a.C) return;
-    const int64_t sstride = BM * PART_ROW(D);
     const float *base = a.part + ((int64_t)unit * a.smax * BM + r) * PART_ROW(D);
-    float M = -INFINITY;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcs(base + s * sstride + D));
-    float Lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-        const float *ps = base + s * sstride;
-        const float ms = __ldcs(ps + D), ls = __ldcs(ps + D + 1);
-        const float4 v = __ldcs(reinterpret_cast<const float4 *>(ps + c4));
-        const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
-        Lsum += w * ls;
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
-    }
-    const float inv_l = 1.f / Lsum;
     *reinterpret_cast<float4 *>(a.out + ((int64_t)row * a.H_q + h) * D + c4) =
-        make_float4(acc.x * inv_l, acc.y * inv_l, acc.z * inv_l, acc.w * inv_l);
+        merge_row4<D>(base, (int64_t)BM * PART_ROW(D), ns, c4);
 }
 
 // ---- q8_0: the attended keys and values dequantised once per call --------------------------
@@ -796,12 +803,101 @@ __global__ void __launch_bounds__(256) dequant_range_kernel(const int8_t *__rest
     *reinterpret_cast<uint4 *>((is_v ? dv : dk) + row * D + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// ---- the fused step's first kernel --------------------------------------------------------
+struct FrontArgs {
+    const void *k, *v;     // the chunk's rows, [C][H][D] in the input dtype
+    void *kq, *vq;         // the cache's codes (q8_0) or values (f16)
+    uint16_t *ks, *vs;     // its scales (q8_0)
+    __half *dk, *dv;       // COPY: the fp16 copy, [H][kv_len][D] each
+    Geom g;
+    int layer, pos0, H, kv_len;
+    int64_t n_dq, n_app;
+};
+
+// Stores the chunk's K and V at positions [pos0, pos0 + C) exactly as the append kernel does (q8_0
+// blocks by the shared quantiser, f16 values rounded to nearest even).  With COPY (q8_0 with the full scratch) it also writes the fp16 copy of positions
+// [0, pos0 + C) that the attention pass reads: the chunk's from the codes it has just made, the earlier
+// positions dequantised from the cache as dequant_range_kernel does (the same values either way).
+// grid.y: K (0) or V (1).  Along x: first n_dq units of 8 earlier values (COPY only), then n_app units
+// of the chunk (a 32-value block for q8_0, 8 values for f16).  A programmatic dependent launch: nothing
+// global is read or written before griddepcontrol.wait (the previous call's attention pass may still be
+// reading the copy).
+template <int D, bool Q8, int DT, bool COPY>
+__global__ void __launch_bounds__(256) prefill_front_kernel(const FrontArgs f) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool is_v = blockIdx.y != 0;
+    const Geom &g = f.g;
+    if (COPY && u < f.n_dq) {
+        constexpr int UPR = D / 8;                   // 8-value units per head row
+        const int64_t row = u / UPR;                 // (head, position) over [0, pos0)
+        const int c = (int)(u - row * UPR);
+        const int h = (int)(row / f.pos0), t = (int)(row - (int64_t)h * f.pos0);
+        const int64_t src = f.layer * g.c_layer + (int64_t)t * g.c_tok + h * g.c_head + 8 * c;
+        const uint2 w = __ldcg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(is_v ? f.vq : f.kq) + src));
+        const uint16_t sb = __ldcg((is_v ? f.vs : f.ks) + f.layer * g.s_layer + (int64_t)t * g.s_tok + h * g.s_head + c / 4);
+        const __half2 d2 = __halves2half2(__ushort_as_half(sb), __ushort_as_half(sb));
+        uint32_t o[4];
+        dequant4(w.x, d2, o[0], o[1]);
+        dequant4(w.y, d2, o[2], o[3]);
+        *reinterpret_cast<uint4 *>((is_v ? f.dv : f.dk) + ((int64_t)h * f.kv_len + t) * D + 8 * c) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        return;
+    }
+    const int64_t ua = u - (COPY ? f.n_dq : 0);
+    if (ua < 0 || ua >= f.n_app) return;
+    const void *in = is_v ? f.v : f.k;
+    if constexpr (Q8) {
+        constexpr int NB = D / 32;
+        const int64_t row = ua / NB;                 // (token, head) in input order
+        const int b = (int)(ua - row * NB);
+        const int t = (int)(row / f.H), h = (int)(row - (int64_t)t * f.H);
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float x8[8];
+            load_inputs8<DT>(in, row * D + b * 32 + 8 * i, x8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[8 * i + e] = x8[e];
+        }
+        uint32_t packed[8];
+        const uint16_t scale = q8_0_quantize32(x, packed);
+        const int64_t pos = (int64_t)f.pos0 + t;
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<int8_t *>(is_v ? f.vq : f.kq) + f.layer * g.c_layer +
+                                               pos * g.c_tok + h * g.c_head + b * 32);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        (is_v ? f.vs : f.ks)[f.layer * g.s_layer + pos * g.s_tok + h * g.s_head + b] = scale;
+        if constexpr (COPY) {
+            const __half2 d2 = __halves2half2(__ushort_as_half(scale), __ushort_as_half(scale));
+            uint32_t o[16];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) dequant4(packed[w], d2, o[2 * w], o[2 * w + 1]);
+            uint4 *cp = reinterpret_cast<uint4 *>((is_v ? f.dv : f.dk) + ((int64_t)h * f.kv_len + pos) * D + b * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cp[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+    } else {
+        constexpr int UPR = D / 8;
+        const int64_t row = ua / UPR;                // (token, head) in input order
+        const int c = (int)(ua - row * UPR);
+        const int t = (int)(row / f.H), h = (int)(row - (int64_t)t * f.H);
+        float x[8];
+        load_inputs8<DT>(in, row * D + 8 * c, x);
+        const int64_t pos = (int64_t)f.pos0 + t;
+        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(is_v ? f.vq : f.kq) + f.layer * g.c_layer + pos * g.c_tok +
+                                   h * g.c_head + 8 * c) =
+            make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+    }
+}
+
 // ---- host side ----------------------------------------------------------------------
 // The work decomposition of one call (see the file comment).
 struct Plan {
     int G, n_qt, ST, smax, n_items;
     int cum[MAX_SPLITS + 1], qtmin[MAX_SPLITS];
-    size_t part_bytes;
+    size_t part_bytes;   // the key splits' partials
 };
 
 // Tiles per split: about a fifth of the cache in steps of 2048 keys, at least 4096 keys, and at
@@ -935,6 +1031,40 @@ int launch_d(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     }
 }
 
+// The fused step's first kernel for one variant (programmatic dependent launch).
+template <int D, bool Q8, int DT, bool COPY>
+int launch_front_t(const FrontArgs &f, cudaStream_t s) {
+    const int64_t units = (COPY ? f.n_dq : 0) + f.n_app;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((units + 255) / 256), 2);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_front_kernel<D, Q8, DT, COPY>, f) == cudaSuccess ? KVC_OK : KVC_ECUDA;
+}
+
+template <int D, bool Q8, bool COPY>
+int launch_front_d(const FrontArgs &f, int dtype, cudaStream_t s) {
+    switch (dtype) {
+        case KVC_IN_F32: return launch_front_t<D, Q8, KVC_IN_F32, COPY>(f, s);
+        case KVC_IN_BF16: return launch_front_t<D, Q8, KVC_IN_BF16, COPY>(f, s);
+        default: return launch_front_t<D, Q8, KVC_IN_F16, COPY>(f, s);
+    }
+}
+
+int launch_front(const FrontArgs &f, int D, bool q8, bool copy, int dtype, cudaStream_t s) {
+    if (D == 128)
+        return !q8 ? launch_front_d<128, false, false>(f, dtype, s)
+                   : copy ? launch_front_d<128, true, true>(f, dtype, s) : launch_front_d<128, true, false>(f, dtype, s);
+    return !q8 ? launch_front_d<64, false, false>(f, dtype, s)
+               : copy ? launch_front_d<64, true, true>(f, dtype, s) : launch_front_d<64, true, false>(f, dtype, s);
+}
+
 }  // namespace
 
 // q8_0: bytes of the fp16 copy of one layer's keys and values (capacity n_ctx positions)
@@ -996,6 +1126,56 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
                   : launch_d<128, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s);
     return q8 ? launch_d<64, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s)
               : launch_d<64, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, scratch, p, s);
+}
+
+int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, const void *k,
+                        const void *v, int dtype, int n_head_q, float *out, void *scratch, size_t scratch_bytes,
+                        cudaStream_t s) {
+    if (n_tokens == 0) return KVC_OK;
+    Plan p;
+    if (!make_plan(c.d, n_head_q, pos0, n_tokens, p)) return KVC_EINVAL;
+    if (scratch_need(p) > scratch_bytes) return KVC_ENOSPC;
+    const bool q8 = c.d.type == KVC_Q8_0;
+    const size_t copy_bytes = dequant_copy_bytes(c.d);
+    const bool copy = q8 && scratch_bytes >= copy_bytes + scratch_need(p);
+    const int kv_len = pos0 + n_tokens, H = c.d.n_head_kv, D = c.d.head_dim;
+    uint8_t *part = static_cast<uint8_t *>(scratch) + (copy ? copy_bytes : 0);
+    FrontArgs f;
+    f.k = k;
+    f.v = v;
+    f.kq = c.k_q;
+    f.vq = c.v_q;
+    f.ks = static_cast<uint16_t *>(c.k_s);
+    f.vs = static_cast<uint16_t *>(c.v_s);
+    f.dk = copy ? static_cast<__half *>(scratch) : nullptr;
+    f.dv = copy ? f.dk + (size_t)H * c.d.n_ctx * D : nullptr;
+    f.g = geom_of(c.d);
+    f.layer = layer;
+    f.pos0 = pos0;
+    f.H = H;
+    f.kv_len = kv_len;
+    f.n_dq = copy ? (int64_t)H * pos0 * (D / 8) : 0;
+    f.n_app = (int64_t)n_tokens * H * (q8 ? D / 32 : D / 8);
+    // the chunk stored (and, with the copy, the attended range in fp16), then the attention and the merge
+    const int rc = launch_front(f, D, q8, copy, dtype, s);
+    if (rc != KVC_OK) return rc;
+    if (copy) {
+        kvc_cache fc = {};
+        fc.d = c.d;
+        fc.d.n_layer = 1;
+        fc.d.n_ctx = kv_len;
+        fc.d.type = KVC_F16;
+        fc.d.layout = KVC_HEAD_MAJOR;
+        fc.k_q = f.dk;
+        fc.v_q = f.dv;
+        return D == 128 ? launch_d<128, false>(fc, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s)
+                        : launch_d<64, false>(fc, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s);
+    }
+    if (D == 128)
+        return q8 ? launch_d<128, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s)
+                  : launch_d<128, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s);
+    return q8 ? launch_d<64, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s)
+              : launch_d<64, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s);
 }
 
 int read_and_clear_device_status(int32_t *status) {

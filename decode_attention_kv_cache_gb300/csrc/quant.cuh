@@ -1,5 +1,5 @@
-// The q8_0 block quantiser, shared by the append kernel and the fused decode step so that both
-// store the same bytes.
+// The q8_0 block quantiser and the input loader, shared by the append kernel and the fused decode and
+// prefill steps so that all of them store the same bytes.
 //
 // One block is 32 values along head_dim: fp16 scale d = amax / 127, int8 codes q = round(x / d)
 // (llama.cpp PR #58 "completion : allow the prompt to be processed under its own split mode",
@@ -14,9 +14,35 @@
 
 #include <cuda_fp16.h>
 
+#include "kvc_internal.h"
 #include "ptx.cuh"
 
 namespace kvc {
+
+// 8 consecutive input values (f32, bf16 or f16: DT is a kvc_dtype) from element index idx, read through L2
+// (a kernel just before the reader may have written them), as floats: bf16 and f16 widen exactly.
+template <int DT>
+__device__ __forceinline__ void load_inputs8(const void *base, int64_t idx, float (&x)[8]) {
+    if constexpr (DT == KVC_IN_F32) {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + idx);
+        const float4 a = __ldcg(p), b = __ldcg(p + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+        const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + idx));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (DT == KVC_IN_BF16) {
+                x[2 * i] = __uint_as_float(w[i] << 16);          // the bf16 bits are the f32's top half
+                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            } else {
+                x[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFF)));
+                x[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+            }
+        }
+    }
+}
 
 // Quantise x[0..31]: the 32 codes packed four to a word (byte i of word w is code 4 w + i) and the
 // fp16 bits of the scale.

@@ -158,12 +158,12 @@ int kv_cache_append(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t
 int kv_cache_append_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, const int32_t *pos, const void *k,
                           const void *v, int32_t dtype, kvc_stream_t stream);
 
-/* Bytes of the scratch buffer prefill_chunk_attn needs for chunks of up to
- * max_tokens rows anywhere in this cache: the float32 partial results
- * (output row, running max, sum) of the key splits, at least 256 bytes, and for
- * a q8_0 cache in front of them room for an fp16 copy of one layer's keys and
- * values (2 * n_head_kv * n_ctx * head_dim * 2 bytes).  The contents need no
- * initialisation; every call writes what it reads. */
+/* Bytes of the scratch buffer prefill_chunk_attn and prefill_step need for
+ * chunks of up to max_tokens rows anywhere in this cache: the float32 partial
+ * results (output row, running max, sum) of the key splits, at least 256 bytes,
+ * and for a q8_0 cache in front of them room for an fp16 copy of one layer's
+ * keys and values (2 * n_head_kv * n_ctx * head_dim * 2 bytes).  The contents
+ * need no initialisation; every call writes what it reads. */
 int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t max_tokens, size_t *bytes);
 
 /* Causal attention of a chunk's query rows over the cache:
@@ -193,6 +193,25 @@ int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t ma
 int prefill_chunk_attn(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens,
                        const void *q, int32_t dtype, int32_t n_head_q, float *out, void *scratch,
                        size_t scratch_bytes, kvc_stream_t stream);
+
+/* One prompt chunk in one call: store its K/V at positions [pos0, pos0 +
+ * n_tokens) of `layer`, exactly as kv_cache_append does (the same bytes), then
+ * attend with its query rows exactly as prefill_chunk_attn does (the same bits
+ * of out): the ubatch step of prompt processing (llama.cpp PR #17
+ * "--split-overlap", section "How"; strata #1441 "Prompt chunks sized for a
+ * layer split's pipeline", "Summary").  q: [n_tokens][n_head_q][head_dim], k and
+ * v: [n_tokens][n_head_kv][head_dim], device memory in `dtype`, 16-byte
+ * aligned; out float32.  Kernels: the first stores the chunk (for q8_0 with
+ * the full scratch it also writes the fp16 copy of positions [0, pos0 +
+ * n_tokens) that the attention reads, so no separate dequantising pass runs),
+ * then the attention and, when rows span several key splits, the merge - two
+ * launches, or three with the merge, where the separate calls take three or
+ * four.  scratch: as for prefill_chunk_attn (kvc_prefill_scratch_bytes, no
+ * initialisation).  Errors as prefill_chunk_attn, and KVC_EINVAL for a null or
+ * unaligned k or v. */
+int prefill_step(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens, const void *q, const void *k,
+                 const void *v, int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
+                 kvc_stream_t stream);
 
 /* Single-token decode attention at position pos: the formula above with one
  * query row at pos, keys [0, pos].  The token's K/V must have been appended.
