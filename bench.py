@@ -64,21 +64,21 @@ def prefill_flops(w, chunks=None):
 # under csrc/); any change to one of them makes the bench report null for that kernel instead.
 # Entries: kernel -> {"sources": {file: sha16}, workload: (bytes per call, what was captured)}.
 TRAFFIC = {
-    # the step's 29 attention calls (dequantising pass, attention, split merge), mean per call
-    "prefill": {"sources": {"prefill.cu": "900fe085b81b05bd"},
-                "q8_0_58k": (535487390, "mean per call over the 29 chunk calls of one step (all three kernels)")},
-    "append_chunk": {"sources": {"append.cu": "aa88d8f25b17248a", "quant.cuh": "356d3631d0d7a4c9"},
-                     "q8_0_58k": (8412211, "one 2048-token chunk append (writes still in L2 at the launch end)")},
-    "append_prompt": {"sources": {"append.cu": "aa88d8f25b17248a", "quant.cuh": "356d3631d0d7a4c9"},
-                      "q8_0_58k": (330845388, "the 58,300-token prompt in one append")},
-    "decode_attn": {"sources": {"decode.cu": "0ab01a08513ab5fd"},
-                    "q8_0_58k": (128083532, "split pass + combine at position 58,555")},
-    "decode_step": {"sources": {"decode.cu": "0ab01a08513ab5fd", "quant.cuh": "356d3631d0d7a4c9"},
-                    "q8_0_58k": (128028697, "split pass storing the token + combine at position 58,555")},
+    # the step's 29 prefill_step calls (the front kernel, the attention, the split merge), mean per call
+    "prefill": {"sources": {"prefill.cu": "ab5eaee10c036180", "quant.cuh": "b2cae791609f3353"},
+                "q8_0_58k": (555756579, "mean per call over the 29 prefill_step calls of one step (all three kernels)")},
+    "append_chunk": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},
+                     "q8_0_58k": (8412236, "one 2048-token chunk append (writes still in L2 at the launch end)")},
+    "append_prompt": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},
+                      "q8_0_58k": (330848742, "the 58,300-token prompt in one append")},
+    "decode_attn": {"sources": {"decode.cu": "33c74136ea250b93"},
+                    "q8_0_58k": (128001433, "split pass + combine at position 58,555")},
+    "decode_step": {"sources": {"decode.cu": "33c74136ea250b93", "quant.cuh": "b2cae791609f3353"},
+                    "q8_0_58k": (128039475, "split pass storing the token + combine at position 58,555")},
     "state_pack": {"sources": {"state.cu": "e0853a7210054393"},
-                   "q8_0_58k": (201607961, "header + pack of 58,556 tokens")},
+                   "q8_0_58k": (201733555, "header + pack of 58,556 tokens")},
     "state_unpack": {"sources": {"state.cu": "e0853a7210054393"},
-                     "q8_0_58k": (202267392, "unpack of 58,556 tokens")},
+                     "q8_0_58k": (202430643, "unpack of 58,556 tokens")},
 }
 
 
