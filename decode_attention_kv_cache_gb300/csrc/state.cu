@@ -43,7 +43,16 @@ struct StateArgs {
     int64_t n_blocks;              // q8_0: 34-byte blocks in the body
     int64_t n_chunks;              // f16: 16-byte chunks in the body
     uint8_t *body;                 // stream body (after the header)
+    uint32_t hdr[8];               // pack: the header words, written by the first block before the body
 };
+
+// pack: the first block's first two threads write the 32-byte header in front of the body
+__device__ __forceinline__ void write_header_words(const StateArgs &a) {
+    if (blockIdx.x == 0 && threadIdx.x < 2)
+        reinterpret_cast<uint4 *>(a.body - 32)[threadIdx.x] =
+            make_uint4(a.hdr[4 * threadIdx.x], a.hdr[4 * threadIdx.x + 1], a.hdr[4 * threadIdx.x + 2],
+                       a.hdr[4 * threadIdx.x + 3]);
+}
 
 // Coordinates of block `beta` of the body: record (layer, t, kv), head h, block b within the head.
 struct BlockPos {
@@ -142,6 +151,7 @@ struct __align__(16) WarpStage {
 __device__ __forceinline__ int phys_chunk(int c) { return c ^ ((c >> 4) & 7); }
 
 __global__ void __launch_bounds__(QW * 32) pack_q8_kernel(const StateArgs a) {
+    write_header_words(a);
     __shared__ WarpStage stage[QW];
     const int lane = threadIdx.x & 31;
     WarpStage &S = stage[threadIdx.x >> 5];
@@ -286,6 +296,7 @@ __device__ __forceinline__ uint8_t *f16_cache_ptr(const StateArgs &a, int64_t ga
 // a warp moves 32 * F16_CHUNKS consecutive chunks, lane-interleaved: each access is 512 contiguous bytes
 template <bool PACK>
 __global__ void __launch_bounds__(THREADS) copy_f16_kernel(const StateArgs a) {
+    if (PACK) write_header_words(a);
     const int lane = threadIdx.x & 31;
     const int64_t first = ((int64_t)blockIdx.x * THREADS + (threadIdx.x - lane)) * F16_CHUNKS + lane;
     uint4 v[F16_CHUNKS];
@@ -473,12 +484,16 @@ int grid_for(int64_t work, int per_thread) {
 
 int launch_state_pack(const kvc_cache &c, int n_tokens, uint8_t *dst, cudaStream_t s) {
     const bool q8 = c.d.type == KVC_Q8_0;
-    write_header<<<1, 1, 0, s>>>(dst, c.d.n_layer, c.d.n_head_kv, c.d.head_dim, q8 ? 1u : 0u, n_tokens);
-    const StateArgs a = make_args(c, n_tokens, dst + 32);
-    if (n_tokens > 0) {
-        if (q8) pack_q8_kernel<<<grid_q8(a.n_blocks), QW * 32, 0, s>>>(a);
-        else copy_f16_kernel<true><<<grid_for(a.n_chunks, F16_CHUNKS), THREADS, 0, s>>>(a);
-    }
+    StateArgs a = make_args(c, n_tokens, dst + 32);
+    const uint32_t hdr[8] = {0x3143564Bu, 1u, (uint32_t)c.d.n_layer, (uint32_t)c.d.n_head_kv, (uint32_t)c.d.head_dim,
+                             q8 ? 1u : 0u, (uint32_t)n_tokens, 0u};
+    for (int i = 0; i < 8; ++i) a.hdr[i] = hdr[i];
+    if (n_tokens == 0)   // the header alone
+        write_header<<<1, 1, 0, s>>>(dst, c.d.n_layer, c.d.n_head_kv, c.d.head_dim, q8 ? 1u : 0u, 0u);
+    else if (q8)         // the kernels write the header too: one launch
+        pack_q8_kernel<<<grid_q8(a.n_blocks), QW * 32, 0, s>>>(a);
+    else
+        copy_f16_kernel<true><<<grid_for(a.n_chunks, F16_CHUNKS), THREADS, 0, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 

@@ -140,13 +140,13 @@ def test_layer_stack_state_restore_and_resumed_decode(kvc):
         req.out_d[0].copy_(saved[layer][1])
         rows = si.sample_rows(w.seed + layer, w.chunks(), n_random=2)
         check_layer(w, req, layer, q, k, v, o, rows, (0, w.n_decode - 1), "layer %d" % layer)
-        # decode resumes on both caches: bitwise equal, and equal to the oracle
+        # decode resumes on both caches - the head-major one by decode_step, the restored layer-major
+        # one by append + decode_attn: bitwise equal, and equal to the oracle
         qd, kd, vd = req.dev_in[layer]
         for pos in range(n, n + extra):
-            outs = []
-            for cache in (req.src, req.dst):
-                kvc.kv_cache_append(cache, layer, pos, kd[pos:pos + 1], vd[pos:pos + 1])
-                outs.append(kvc.decode_attn(cache, layer, pos, qd[pos]))
+            outs = [kvc.decode_step(req.src, layer, pos, qd[pos], kd[pos], vd[pos])]
+            kvc.kv_cache_append(req.dst, layer, pos, kd[pos:pos + 1], vd[pos:pos + 1])
+            outs.append(kvc.decode_attn(req.dst, layer, pos, qd[pos]))
             assert torch.equal(outs[0], outs[1])
         o.append(0, n, np32(k[n:n + extra]), np32(v[n:n + extra]))
         assert_close(outs[0].cpu().numpy(), o.decode(0, n + extra - 1, np32(q[n + extra - 1])), "resumed decode")
