@@ -8,16 +8,23 @@
 // mode", section "Why"; llama.cpp PR #59 "llama : switch the split mode of a
 // live context", section "Why").
 //
-// Split pass: one wave of CTAs, grid (split, kv head), two CTAs per SM.  A CTA
-// streams the key range [split*len, (split+1)*len) of one kv head: warp 0
-// issues TMA copies of 64-key K and V blocks into a ring of shared-memory
-// stages (128-byte swizzle; 64-byte for 64-byte rows), so many stages are in
-// flight at once; four consumer warps each take one 16-key group of a stage
-// for all G query heads of the group.  A consumer warp computes the group's
-// scores with mma.sync m16n8k16 (rows = query heads of the group, columns =
-// keys), keeps an online softmax per head, and accumulates P*V with a second
-// mma.sync (rows = heads, columns = head_dim), reading its fragments from the
-// stage:
+// Split pass, head_dim 128 (decode_tc_kernel, described where it is defined):
+// one wave of CTAs, one per SM, over (split, kv head); 128-key tiles by TMA;
+// tcgen05 MMAs over query-head rows replicated so that one thread owns one
+// row's online softmax; two MMA issuers; q8_0 codes dequantised in place.  For
+// decode_step the CTA whose split holds pos first quantises and stores the
+// token (the append kernel's quantiser), then copies that tile.
+//
+// Split pass, head_dim 64 (decode_split_kernel): one wave of CTAs, grid (split,
+// kv head), two CTAs per SM.  A CTA streams the key range [split*len,
+// (split+1)*len) of one kv head: warp 0 issues TMA copies of 64-key K and V
+// blocks into a ring of shared-memory stages (128-byte swizzle; 64-byte for the
+// 64-byte q8_0 rows), so many stages are in flight at once; four consumer warps each take one 16-key group of a
+// stage for all G query heads of the group.  A consumer warp computes the
+// group's scores with mma.sync m16n8k16 (rows = query heads of the group,
+// columns = keys), keeps an online softmax per head, and accumulates P*V with
+// a second mma.sync (rows = heads, columns = head_dim), reading its fragments
+// from the stage:
 //   - q8_0 codes are converted to exact fp16 integers with two byte permutes
 //     and one fp16 subtraction; the K scale is applied per 32-value block to
 //     the fp32 partial scores, the V scale is folded into P per block, so the

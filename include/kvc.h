@@ -33,13 +33,16 @@
  *     working context, PR #58 section "Memory"; PR #59 section "What this
  *     adds").  Errors of asynchronous work surface at the caller's next
  *     synchronisation; the kernels contain no unbounded waits.
- *   - The append, prefill attention (and its split merge) and decode kernels
- *     are launched with programmatic dependent launch: one may be scheduled
- *     while the kernel before it on `stream` is finishing, and it waits on the
- *     device (griddepcontrol.wait) for that kernel to complete before it reads
- *     or writes memory.  Stream order therefore holds exactly as for ordinary
- *     launches, also inside a captured CUDA graph.  The state kernels and the
- *     q8_0 prefill's dequantising pass are ordinary launches.
+ *   - The append, prefill attention (and its split merge), prefill_step's
+ *     first kernel and the decode kernels are launched with programmatic
+ *     dependent launch: one may be scheduled while the kernel before it on
+ *     `stream` is finishing, and it waits on the device (griddepcontrol.wait)
+ *     for that kernel to complete before it reads or writes memory (the decode
+ *     split pass only hints, before that wait, that L2 fetch its first tiles,
+ *     which moves no data it reads).  Stream order therefore holds exactly as
+ *     for ordinary launches, also inside a captured CUDA graph.  The state
+ *     kernels and prefill_chunk_attn's q8_0 dequantising pass are ordinary
+ *     launches.
  *
  * Cache contents.  A cache holds n_layer layers of n_ctx positions of
  * n_head_kv heads of head_dim values, for K and for V.  Cache types:
@@ -55,7 +58,7 @@
  *
  * Supported shapes: head_dim a multiple of 32 for append and state calls;
  * head_dim 64 or 128 for the attention calls; n_head_q a multiple of
- * n_head_kv; n_head_q / n_head_kv <= 16 for decode_attn.
+ * n_head_kv; n_head_q / n_head_kv <= 16 for the decode calls.
  */
 #ifndef KVC_H
 #define KVC_H
