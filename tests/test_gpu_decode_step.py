@@ -26,6 +26,8 @@ CASES = [
     (40, 8, 128, "f16", "bf16", 124, 8),     # ... and at 128
     (8, 8, 128, "q8_0", "f32", 60, 5),       # G = 1
     (32, 2, 128, "f16", "f16", 300, 4),      # G = 16
+    (32, 2, 128, "q8_0", "bf16", 200, 3),    # G = 16 with q8_0: 16 head slots, the token dequantised in place
+    (12, 4, 128, "f16", "f32", 127, 3),      # f32 inputs into an f16 cache, the first step at a tile edge
     (24, 2, 128, "q8_0", "bf16", 0, 6),      # from an empty cache: the first step attends to itself
     (4, 2, 64, "q8_0", "f32", 100, 4),       # head_dim 64: append and decode_attn in turn
     (4, 2, 64, "f16", "bf16", 63, 3),
