@@ -121,3 +121,35 @@ def test_step_batch_equals_append_batch_then_decode_batch(kvc, n_seq, cache, d, 
         o.append(0, 0, np32(k[:p + 1]), np32(v[:p + 1]))
         assert_cache_equal(gb[i], o, p + 1)
         assert_close(out[i].cpu().numpy(), o.decode(0, p, np32(q[p])), "seq %d vs oracle" % i)
+
+
+@pytest.mark.parametrize("cache", ["q8_0", "f16"])
+def test_step_loop_captured_in_a_cuda_graph(kvc, cache):
+    # the decode loop as the bench runs it: steps captured once in a CUDA graph (programmatic launches
+    # inside the graph), replayed; each step equals the eager step bit for bit, twice over
+    w = si.small_workload("stepgraph", 40, 8, 128, cache, "bf16", n_prompt=3000, chunk=3000, n_decode=8, seed=44)
+    q, k, v = (t.cuda() for t in si.layer_qkv(w, 0))
+    g = kvc.KVCache(1, w.n_ctx, 8, 128, cache, "head_major")
+    kvc.kv_cache_append(g, 0, 0, k[:3000], v[:3000])
+    scratch = torch.empty(g.scratch_bytes(40), dtype=torch.uint8, device="cuda")
+    eager = torch.empty(8, 40, 128, device="cuda")
+    graph_out = torch.empty_like(eager)
+
+    def loop(out):
+        for i in range(8):
+            p = 3000 + i
+            kvc.decode_step(g, 0, p, q[p], k[p], v[p], out=out[i], scratch=scratch)
+
+    loop(eager)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            loop(graph_out)
+    for _ in range(2):
+        graph_out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(graph_out, eager)
+    assert kvc.kvc_device_status() == 0
