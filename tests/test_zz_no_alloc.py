@@ -81,7 +81,7 @@ def test_noalloc_rejects_an_output_in_host_memory(cuda_device):
     f = _entry(kvc)
     g = kvc.KVCache(1, 64, 2, 64, "q8_0", "head_major")
     q = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
-    out = torch.empty(4, 64).pin_memory()      # not memory of the current device
+    out = torch.full((4, 64), 7.0).pin_memory()   # not memory of the current device (a known value: no NaN)
     before = out.clone()
     rc = f(ctypes.byref(g.c), 0, 3, ctypes.c_void_p(q.data_ptr()), 1, 4, ctypes.c_void_p(out.data_ptr()),
            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
