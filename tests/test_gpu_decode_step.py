@@ -153,3 +153,25 @@ def test_step_loop_captured_in_a_cuda_graph(kvc, cache):
         torch.cuda.synchronize()
         assert torch.equal(graph_out, eager)
     assert kvc.kvc_device_status() == 0
+
+
+@pytest.mark.parametrize("cache", ["q8_0", "f16"])
+def test_step_up_to_the_last_cache_position(kvc, cache):
+    # a cache filled to its last position: the final steps' tile reaches past n_ctx (zero-filled copies)
+    n_ctx = 300
+    w = si.small_workload("steplast", 40, 8, 128, cache, "bf16", n_prompt=296, chunk=296, n_decode=4, seed=52,
+                          n_ctx=n_ctx)
+    q, k, v = si.layer_qkv(w, 0)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    g = kvc.KVCache(1, n_ctx, 8, 128, cache, "layer_major")
+    kvc.kv_cache_append(g, 0, 0, kd[:296], vd[:296])
+    o = OracleCache(1, n_ctx, 8, 128, cache)
+    o.append(0, 0, np32(k[:296]), np32(v[:296]))
+    for pos in range(296, n_ctx):
+        out = kvc.decode_step(g, 0, pos, qd[pos], kd[pos], vd[pos])
+        o.append(0, pos, np32(k[pos:pos + 1]), np32(v[pos:pos + 1]))
+        assert_close(out.cpu().numpy(), o.decode(0, pos, np32(q[pos])), "pos %d" % pos)
+    assert_cache_equal(g, o, n_ctx)
+    with pytest.raises(kvc.KvcError):
+        kvc.decode_step(g, 0, n_ctx, qd[0], kd[0], vd[0])
+    assert kvc.kvc_device_status() == 0

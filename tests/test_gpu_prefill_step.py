@@ -117,3 +117,22 @@ def test_step_repeated_on_one_scratch(kvc):
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert kvc.kvc_device_status() == 0
+
+
+@pytest.mark.parametrize("cache", ["q8_0", "f16"])
+def test_step_chunk_ending_at_the_cache_end(kvc, cache):
+    # the last chunk fills the cache to n_ctx exactly (the largest copy and plan the scratch was sized for)
+    n_ctx = 2600
+    w = si.small_workload("pstepend", 10, 2, 128, cache, "bf16", n_prompt=n_ctx, chunk=1000, n_decode=0, seed=61,
+                          n_ctx=n_ctx)
+    qkv = si.layer_qkv(w, 0)
+    gb, oa, ob = two_ways(kvc, w, 1000, qkv)
+    assert torch.equal(oa, ob)
+    o = OracleCache(1, n_ctx, w.n_head_kv, w.head_dim, cache)
+    q, k, v = qkv
+    o.append(0, 0, np32(k), np32(v))
+    assert_cache_equal(gb, o, n_ctx)
+    rows = np.array([0, 999, 1000, 1999, 2000, 2598, 2599])
+    kh, vh = o.dequantized(0, n_ctx)
+    from oracle.attention import attend
+    assert_close(ob[rows].cpu().numpy(), attend(np32(q[rows]), rows, kh, vh), "rows at the end")
