@@ -634,19 +634,28 @@ def end_to_end(kvc, torch, w, req, device, rank, world, K, flush):
     E = torch.cuda.Event
 
     def run(n):
-        done, out_done = [], []
+        done, out_done, inp = [], [], []
         start = E(enable_timing=True)
         start.record(main)
         s_in.wait_event(start)
         s_out.wait_event(start)
+
+        def h2d(j):
+            # step j's inputs, once its request's previous step (j - 2) no longer reads them
+            if j >= 2:
+                s_in.wait_event(done[j - 2])
+            with torch.cuda.stream(s_in):
+                reqs[j % 2].h2d()
+            e = E(); e.record(s_in); inp.append(e)
+
+        h2d(0)
         for i in range(n):
             r = reqs[i % 2]
-            if i >= 2:
-                s_in.wait_event(done[i - 2])          # request r's previous step no longer reads its inputs
-            with torch.cuda.stream(s_in):
-                r.h2d()
-            inp = E(); inp.record(s_in)
-            main.wait_event(inp)
+            # the next step's inputs are queued before this step: the host may wait inside this step
+            # (kv_state_set reads the stream header), and the copy then still runs beside its compute
+            if i + 1 < n:
+                h2d(i + 1)
+            main.wait_event(inp[i])
             if i >= 2:
                 main.wait_event(out_done[i - 2])      # request r's previous outputs are on the host
             r.step()
