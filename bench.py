@@ -252,13 +252,12 @@ class GpuRequest:
     def launches_per_step(self):
         """Kernels one step launches: per chunk two (prefill_step: the chunk's store, with the fp16 copy
         for q8_0, then the attention) plus the split merge when the chunk's last row reaches past the
-        first key split; per decode step the split pass (which stores the token) and the combine
-        (head_dim 64: also the append); the state header, pack and unpack."""
+        first key split; per decode step the split pass (which stores the token) and the combine; the
+        state pack and unpack."""
         w = self.w
         keys = prefill_split_keys(w.n_ctx)
         merges = sum(1 for p, c in self.chunks if p + c - 1 >= keys)
-        per_decode = 2 if w.head_dim == 128 else 3
-        return w.n_layer * (2 * len(self.chunks) + merges + per_decode * w.n_decode) + 3
+        return w.n_layer * (2 * len(self.chunks) + merges + 2 * w.n_decode) + 2
 
     def _decode_loop(self, layer):
         kvc, w = self.kvc, self.w

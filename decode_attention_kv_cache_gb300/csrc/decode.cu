@@ -33,7 +33,8 @@
 // Head-dim slots are permuted inside each MMA (the dot product does not care)
 // so that every thread reads 8 or 16 (K) and 4 or 8 (V) contiguous bytes per
 // row.  The four warps are merged in shared memory in a fixed order and the
-// CTA writes (m, l, O) for its range to the scratch buffer.
+// CTA writes (m, l, O) for its range to the scratch buffer.  For decode_step, warp 0 of the CTA whose
+// split holds pos stores the token first, before any stage is copied.
 //
 // Combine pass: launched with programmatic dependent launch, so its CTAs are
 // resident while the split pass runs and wait for it on the device
@@ -255,6 +256,83 @@ __device__ __forceinline__ void load_group_v(const uint8_t *sb, int cw, int gq, 
     }
 }
 
+// 8 query values (chunk i of the loaded 16-byte words) as fp32
+template <int DT, int N>
+__device__ __forceinline__ void to_f32x8(const uint4 (&raw)[N], int i, float (&x)[8]) {
+    if constexpr (DT == KVC_IN_F32) {
+        const uint4 a = raw[2 * i], b = raw[2 * i + 1];
+        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y); x[2] = __uint_as_float(a.z);
+        x[3] = __uint_as_float(a.w); x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+        x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+    } else {
+        const uint4 u = raw[i];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (DT == KVC_IN_BF16) {
+                x[2 * e] = __uint_as_float(w[e] << 16);
+                x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            } else {
+                x[2 * e] = __half2float(__ushort_as_half((unsigned short)(w[e] & 0xFFFFu)));
+                x[2 * e + 1] = __half2float(__ushort_as_half((unsigned short)(w[e] >> 16)));
+            }
+        }
+    }
+}
+
+// Fused decode step: one warp stores the token's K and V rows of kv head hkv at position n_keys - 1,
+// exactly as the append kernel does (q8_0 blocks by the shared quantiser, f16 values rounded to
+// nearest even).  q8_0: one lane per 32-value block (K's blocks, then V's); f16: one lane per 8 values
+// (K's, then V's).  The rows are read through L2: a kernel just before
+// this one may have written them.
+template <bool Q8, int DT, int D = 128>
+__device__ __forceinline__ void store_new_token(const DecodeArgs &a, int hkv, int lane) {
+    constexpr int ESZ = DT == KVC_IN_F32 ? 4 : 2;
+    constexpr int NB = D / 32;                     // q8_0 blocks per row
+    const int64_t pos = a.n_keys - 1;
+    const Geom &g = a.g;
+    if constexpr (Q8) {
+        if (lane < 2 * NB) {
+            const int is_v = lane / NB, b = lane % NB;
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(is_v ? a.v_new : a.k_new) +
+                                                               ((int64_t)hkv * D + b * 32) * ESZ);
+            constexpr int NW = 32 * ESZ / 16;   // 16-byte words of one block's input
+            uint4 raw[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) raw[i] = __ldcg(src + i);
+            float x[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float x8[8];
+                to_f32x8<DT>(raw, c, x8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[8 * c + e] = x8[e];
+            }
+            uint32_t packed[8];
+            const uint16_t scale = q8_0_quantize32(x, packed);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<int8_t *>(is_v ? a.vq : a.kq) + a.layer * g.c_layer +
+                                                   pos * g.c_tok + hkv * g.c_head + b * 32);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            (is_v ? a.vs_w : a.ks_w)[a.layer * g.s_layer + pos * g.s_tok + hkv * g.s_head + b] = scale;
+        }
+    } else {
+        constexpr int UPR = D / 8;                 // 8-value units per row
+        if (lane >= 2 * UPR) return;
+        const int is_v = lane / UPR, c = lane % UPR;
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(is_v ? a.v_new : a.k_new) +
+                                                           ((int64_t)hkv * D + c * 8) * ESZ);
+        uint4 raw[ESZ / 2];
+#pragma unroll
+        for (int i = 0; i < ESZ / 2; ++i) raw[i] = __ldcg(src + i);
+        float x[8];
+        to_f32x8<DT>(raw, 0, x);
+        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(is_v ? a.vq : a.kq) + a.layer * g.c_layer + pos * g.c_tok +
+                                   hkv * g.c_head + c * 8) =
+            make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+    }
+}
+
 template <int D, bool Q8, int DT>
 __global__ void __maxnreg__(200)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -291,6 +369,16 @@ __global__ void __maxnreg__(200)
     // pass may be scheduled from here on (it waits for this grid to finish)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    if (a.k_new != nullptr) {
+        // fused decode step: the CTA whose split holds the new position stores the token first; the
+        // barrier orders those stores before the stage copies (with the async-proxy fence) and the
+        // consumers' scale loads
+        if (warp == 0 && split == a.n_split - 1) {
+            store_new_token<Q8, DT, D>(a, hkv, lane);
+            fence_proxy_async_global();
+        }
+        __syncthreads();
+    }
 
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float o[NT][4];
@@ -714,80 +802,7 @@ __device__ __forceinline__ void dequant4(uint32_t w, __half2 d2, uint32_t &lo, u
     lo = *reinterpret_cast<uint32_t *>(&ra);
     hi = *reinterpret_cast<uint32_t *>(&rb);
 }
-// 8 query values (chunk i of the loaded 16-byte words) as fp32
-template <int DT, int N>
-__device__ __forceinline__ void to_f32x8(const uint4 (&raw)[N], int i, float (&x)[8]) {
-    if constexpr (DT == KVC_IN_F32) {
-        const uint4 a = raw[2 * i], b = raw[2 * i + 1];
-        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y); x[2] = __uint_as_float(a.z);
-        x[3] = __uint_as_float(a.w); x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
-        x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
-    } else {
-        const uint4 u = raw[i];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if constexpr (DT == KVC_IN_BF16) {
-                x[2 * e] = __uint_as_float(w[e] << 16);
-                x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-            } else {
-                x[2 * e] = __half2float(__ushort_as_half((unsigned short)(w[e] & 0xFFFFu)));
-                x[2 * e + 1] = __half2float(__ushort_as_half((unsigned short)(w[e] >> 16)));
-            }
-        }
-    }
-}
 
-// Fused decode step: one warp stores the token's K and V rows of kv head hkv at position n_keys - 1,
-// exactly as the append kernel does (q8_0 blocks by the shared quantiser, f16 values rounded to
-// nearest even).  q8_0: lanes 0-7 take one 32-value block each (K blocks 0-3, then V's); f16: each lane
-// takes 8 values (K on lanes 0-15, V on 16-31).  The rows are read through L2: a kernel just before
-// this one may have written them.
-template <bool Q8, int DT>
-__device__ __forceinline__ void store_new_token(const DecodeArgs &a, int hkv, int lane) {
-    constexpr int D = 128;
-    constexpr int ESZ = DT == KVC_IN_F32 ? 4 : 2;
-    const int64_t pos = a.n_keys - 1;
-    const Geom &g = a.g;
-    if constexpr (Q8) {
-        if (lane < 8) {
-            const int is_v = lane >> 2, b = lane & 3;
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(is_v ? a.v_new : a.k_new) +
-                                                               ((int64_t)hkv * D + b * 32) * ESZ);
-            constexpr int NW = 32 * ESZ / 16;   // 16-byte words of one block's input
-            uint4 raw[NW];
-#pragma unroll
-            for (int i = 0; i < NW; ++i) raw[i] = __ldcg(src + i);
-            float x[32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float x8[8];
-                to_f32x8<DT>(raw, c, x8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[8 * c + e] = x8[e];
-            }
-            uint32_t packed[8];
-            const uint16_t scale = q8_0_quantize32(x, packed);
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<int8_t *>(is_v ? a.vq : a.kq) + a.layer * g.c_layer +
-                                                   pos * g.c_tok + hkv * g.c_head + b * 32);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            (is_v ? a.vs_w : a.ks_w)[a.layer * g.s_layer + pos * g.s_tok + hkv * g.s_head + b] = scale;
-        }
-    } else {
-        const int is_v = lane >> 4, c = lane & 15;
-        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(is_v ? a.v_new : a.k_new) +
-                                                           ((int64_t)hkv * D + c * 8) * ESZ);
-        uint4 raw[ESZ / 2];
-#pragma unroll
-        for (int i = 0; i < ESZ / 2; ++i) raw[i] = __ldcg(src + i);
-        float x[8];
-        to_f32x8<DT>(raw, 0, x);
-        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(is_v ? a.vq : a.kq) + a.layer * g.c_layer + pos * g.c_tok +
-                                   hkv * g.c_head + c * 8) =
-            make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
-    }
-}
 
 // NS: sequences of a batch the parameters hold (1, or MAX_BATCH for a batched call; grid z = sequence)
 template <bool Q8, int DT, int NS, int HS>
@@ -1416,8 +1431,8 @@ int launch_t(const kvc_cache &c, int layer, int pos, const void *q, int n_head_q
     a.group = n_head_q / c.d.n_head_kv;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
     a.stall_ns = 0;
+    if (k_new != nullptr) set_fused(a, c, k_new, v_new);
     if constexpr (D == 128) {
-        if (k_new != nullptr) set_fused(a, c, k_new, v_new);
         return launch_tc<Q8, DT, 1>(&c, &a, 1, n_head_q, &out, s);
     } else {
     // one wave: CTAS_PER_SM CTAs per SM over (split, kv head), whole stages per split
@@ -1650,9 +1665,8 @@ int launch_decode_step(const kvc_cache &c, int layer, int pos, const void *q, co
     if (c.d.head_dim == 128)
         return q8 ? launch_d<128, true>(c, layer, pos, q, dtype, n_head_q, out, scratch, s, k, v)
                   : launch_d<128, false>(c, layer, pos, q, dtype, n_head_q, out, scratch, s, k, v);
-    // head_dim 64: the append, then decode_attn's split pass and combine
-    const int rc = launch_append(c, layer, pos, 1, k, v, dtype, s);
-    return rc != KVC_OK ? rc : launch_decode(c, layer, pos, q, dtype, n_head_q, out, scratch, s);
+    return q8 ? launch_d<64, true>(c, layer, pos, q, dtype, n_head_q, out, scratch, s, k, v)
+              : launch_d<64, false>(c, layer, pos, q, dtype, n_head_q, out, scratch, s, k, v);
 }
 
 int launch_decode_step_batch(const kvc_cache *caches, int n_seq, int layer, const int *pos, const void *q, const void *k,

@@ -260,10 +260,9 @@ int decode_attn_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer, con
  * PR #59 "llama : switch the split mode of a live context", section "Why").
  * q: [n_head_q][head_dim], k and v: [n_head_kv][head_dim], all device memory
  * in `dtype`, 16-byte aligned; out: [n_head_q][head_dim] float32.
- * With head_dim 128 it is two kernels: the split pass, in which the CTA whose
- * key range holds pos quantises and stores the token before it copies that
- * tile, then decode_attn's combine.  With head_dim 64 the append and
- * decode_attn's two kernels run in turn.  scratch: as for decode_attn
+ * It is two kernels: the split pass, in which the CTA whose key range holds
+ * pos quantises and stores the token before it copies that tile, then
+ * decode_attn's combine.  scratch: as for decode_attn
  * (kvc_scratch_bytes, no initialisation); calls on one scratch buffer must not
  * overlap on the GPU.  Errors: KVC_EINVAL (null or unaligned pointers, dtype,
  * head_dim, heads), KVC_ERANGE (layer, pos), KVC_ENOSPC (scratch too small). */
