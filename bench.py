@@ -66,19 +66,19 @@ def prefill_flops(w, chunks=None):
 TRAFFIC = {
     # the step's 29 prefill_step calls (the front kernel, the attention, the split merge), mean per call
     "prefill": {"sources": {"prefill.cu": "ab5eaee10c036180", "quant.cuh": "b2cae791609f3353"},
-                "q8_0_58k": (554770343, "mean per call over the 29 prefill_step calls of one step (all three kernels)")},
+                "q8_0_58k": (554697948, "mean per call over the 29 prefill_step calls of one step (all three kernels)")},
     "append_chunk": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},
-                     "q8_0_58k": (8412236, "one 2048-token chunk append (writes still in L2 at the launch end)")},
+                     "q8_0_58k": (8412364, "one 2048-token chunk append (writes still in L2 at the launch end)")},
     "append_prompt": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},
-                      "q8_0_58k": (330910540, "the 58,300-token prompt in one append")},
-    "decode_attn": {"sources": {"decode.cu": "fb622a163d1fe52b"},
-                    "q8_0_58k": (128027417, "split pass + combine at position 58,555")},
-    "decode_step": {"sources": {"decode.cu": "fb622a163d1fe52b", "quant.cuh": "b2cae791609f3353"},
-                    "q8_0_58k": (128047795, "split pass storing the token + combine at position 58,555")},
+                      "q8_0_58k": (330861952, "the 58,300-token prompt in one append")},
+    "decode_attn": {"sources": {"decode.cu": "d280bfd9f3fbd2ec"},
+                    "q8_0_58k": (128035097, "split pass + combine at position 58,555")},
+    "decode_step": {"sources": {"decode.cu": "d280bfd9f3fbd2ec", "quant.cuh": "b2cae791609f3353"},
+                    "q8_0_58k": (128019635, "split pass storing the token + combine at position 58,555")},
     "state_pack": {"sources": {"state.cu": "0b844f534c53c1b8"},
-                   "q8_0_58k": (201783116, "pack of 58,556 tokens (the kernel writes the header)")},
+                   "q8_0_58k": (201804441, "pack of 58,556 tokens (the kernel writes the header)")},
     "state_unpack": {"sources": {"state.cu": "0b844f534c53c1b8"},
-                     "q8_0_58k": (202400384, "unpack of 58,556 tokens")},
+                     "q8_0_58k": (202305715, "unpack of 58,556 tokens")},
 }
 
 
