@@ -2,7 +2,8 @@
 """Benchmark of the attention-over-KV-cache hot path on GB300.
 
 One step = one request on every layer of the workload: the prompt prefilled in
-chunks (prefill_step per chunk: the chunk's store, then the attention), the decode steps
+chunks (prefill_step per chunk: the chunk's store, then the attention; for q8_0 each
+chunk adds its own positions to the layer's fp16 copy, copy_valid = pos0), the decode steps
 (decode_step per token: the split pass stores the token and attends, then the
 combine; the loop captured once in a CUDA graph), then the cache state serialised from the head-major cache
 (kv_state_get) and restored into a layer-major cache (kv_state_set).
@@ -65,8 +66,8 @@ def prefill_flops(w, chunks=None):
 # Entries: kernel -> {"sources": {file: sha16}, workload: (bytes per call, what was captured)}.
 TRAFFIC = {
     # the step's 29 prefill_step calls (the front kernel, the attention, the split merge), mean per call
-    "prefill": {"sources": {"prefill.cu": "ab5eaee10c036180", "quant.cuh": "b2cae791609f3353"},
-                "q8_0_58k": (554697948, "mean per call over the 29 prefill_step calls of one step (all three kernels)")},
+    "prefill": {"sources": {"prefill.cu": "89bee08b1308fd94", "quant.cuh": "b2cae791609f3353"},
+                "q8_0_58k": (416575929, "mean per call over the 29 prefill_step calls of one step (all three kernels)")},
     "append_chunk": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},
                      "q8_0_58k": (8412364, "one 2048-token chunk append (writes still in L2 at the launch end)")},
     "append_prompt": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},
@@ -250,8 +251,8 @@ class GpuRequest:
         return layer if self.w.n_layer == 1 else 0
 
     def launches_per_step(self):
-        """Kernels one step launches: per chunk two (prefill_step: the chunk's store, with the fp16 copy
-        for q8_0, then the attention) plus the split merge when the chunk's last row reaches past the
+        """Kernels one step launches: per chunk two (prefill_step: the chunk's store, with its part of the
+        fp16 copy for q8_0, then the attention) plus the split merge when the chunk's last row reaches past the
         first key split; per decode step the split pass (which stores the token) and the combine; the
         state pack and unpack."""
         w = self.w
@@ -270,13 +271,14 @@ class GpuRequest:
     def attention_only(self):
         """Every chunk's prefill_step of every layer, back to back, as the step issues them (the
         roofline's timing of the attention with no event between two launches; each call also stores
-        its chunk again, the same bytes, and for q8_0 writes the fp16 copy the attention reads)."""
+        its chunk again, the same bytes, and for q8_0 writes the chunk's part of the fp16 copy the
+        attention reads)."""
         kvc, w = self.kvc, self.w
         for layer in range(w.n_layer):
             q, k, v = self.dev_in[layer]
             for p, c in self.chunks:
                 kvc.prefill_step(self.src, layer, p, q[p:p + c], k[p:p + c], v[p:p + c],
-                                 out=self.out_p[self.out_slot(layer), p:p + c], scratch=self.pscratch)
+                                 out=self.out_p[self.out_slot(layer), p:p + c], scratch=self.pscratch, copy_valid=p)
 
     def capture(self):
         """Capture each layer's decode loop in a CUDA graph (after one eager run)."""
@@ -305,7 +307,7 @@ class GpuRequest:
                 if ev is not None:
                     a = E(enable_timing=True); a.record()
                 kvc.prefill_step(self.src, layer, p, q[p:p + c], k[p:p + c], v[p:p + c],
-                                 out=self.out_p[self.out_slot(layer), p:p + c], scratch=self.pscratch)
+                                 out=self.out_p[self.out_slot(layer), p:p + c], scratch=self.pscratch, copy_valid=p)
                 if ev is not None:
                     b = E(enable_timing=True); b.record(); ev["attn"].append((a, b, self.flops[ci]))
             if ev is not None:
@@ -424,7 +426,7 @@ def run_gpu(args, rank, world, local):
     # ---- end to end: host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(kvc, torch, w, req, device, rank, world, K, flush)
+        e2e = end_to_end(kvc, torch, w, req, device, rank, world, K, flush, local)
     assert kvc.kvc_device_status() == 0
 
     peaks, peak_src = load_peaks()
@@ -436,9 +438,9 @@ def run_gpu(args, rank, world, local):
             "peak_source": "%s dense bf16 burst (f16 runs at the bf16 rate)" % peak_src,
             "traffic": traffic, "traffic_launch": traffic_launch, "launches": n_attn // K,
             "avg_launch_ms": chain_ms / n_attn,
-            "timed": "the step's prefill_step calls back to back (each: the chunk's store, with the fp16 "
-                     "copy for q8_0, the attention and the split merge; L2 flushed before each pass), CUDA "
-                     "events at the ends of each pass",
+            "timed": "the step's prefill_step calls back to back (each: the chunk's store, for q8_0 with "
+                     "the chunk's part of the fp16 copy, the attention and the split merge; L2 flushed before "
+                     "each pass), CUDA events at the ends of each pass",
             "achieved_calls_between_events": attn_flops / (attn_ms / 1e3) / 1e12,
             "algorithmic_flops_per_step": attn_flops / K}
     bt = cache_bytes_per_token(w)
@@ -600,7 +602,7 @@ def batched_decode(kvc, torch, w, device, npls, n_past=2048, n_gen=128):
     return res
 
 
-def end_to_end(kvc, torch, w, req, device, rank, world, K, flush):
+def end_to_end(kvc, torch, w, req, device, rank, world, K, flush, local=0):
     """The same request through the public API with host buffers: every step copies its inputs in from
     pinned host memory and its outputs (prefill and decode attention, the state) back out, inside the
     timed region.  For a one-layer request two requests alternate, so that step i's input copy and
@@ -673,9 +675,12 @@ def end_to_end(kvc, torch, w, req, device, rank, world, K, flush):
     run(2)
     torch.cuda.synchronize()
     dist_barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
     e_total = dist_max(run(K), world)
+    clk = clocks.stop()
     return {"value": tokens * world * K / (e_total / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": e_total / K,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e_total / K, "clocks": clk,
             "overlap": "two requests alternate: copies in and out on their own streams beside compute",
             "l2": "each step copies in %d bytes of inputs (> L2)" % h2d}
 

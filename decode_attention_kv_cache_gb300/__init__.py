@@ -55,7 +55,7 @@ def _load():
         "kvc_prefill_scratch_bytes": (ctypes.c_int, [P(kvc_desc), I32, I32, P(SZ)]),
         "prefill_chunk_attn": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, I32, I32, VP, VP, SZ, VP]),
         "decode_attn": (ctypes.c_int, [P(kvc_cache), I32, I32, VP, I32, I32, VP, VP, SZ, VP]),
-        "prefill_step": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, VP, VP, I32, I32, VP, VP, SZ, VP]),
+        "prefill_step": (ctypes.c_int, [P(kvc_cache), I32, I32, I32, VP, VP, VP, I32, I32, VP, VP, SZ, I32, VP]),
         "kv_state_get": (ctypes.c_int, [P(kvc_cache), I32, VP, SZ, VP]),
         "kv_state_set": (ctypes.c_int, [P(kvc_cache), VP, SZ, P(I32), VP]),
         "kvc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -217,9 +217,11 @@ def prefill_chunk_attn(cache, layer, pos0, q, out=None, scratch=None, stream=Non
     return out
 
 
-def prefill_step(cache, layer, pos0, q, k, v, out=None, scratch=None, stream=None):
+def prefill_step(cache, layer, pos0, q, k, v, out=None, scratch=None, stream=None, copy_valid=0):
     """One prompt chunk: store k, v [C, H_kv, D] at positions [pos0, pos0 + C) (as kv_cache_append) and
-    attend with q [C, H_q, D] (as prefill_chunk_attn); returns out [C, H_q, D] f32."""
+    attend with q [C, H_q, D] (as prefill_chunk_attn); returns out [C, H_q, D] f32.  copy_valid: leading
+    positions of the scratch's fp16 copy (q8_0) already holding this layer's values from earlier calls
+    with this scratch (pos0 when the previous chunk of this layer went through it)."""
     _need(q, "q"); _need(k, "k", q.dtype); _need(v, "v", q.dtype)
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
@@ -228,7 +230,7 @@ def prefill_step(cache, layer, pos0, q, k, v, out=None, scratch=None, stream=Non
     _need(out, "out", torch.float32); _need(scratch, "scratch")
     st = _lib().prefill_step(ctypes.byref(cache.c), layer, pos0, q.shape[0], _ptr(q), _ptr(k), _ptr(v), DTYPES[q.dtype],
                              q.shape[1], _ptr(out), _ptr(scratch), scratch.numel() * scratch.element_size(),
-                             _stream(stream, q.device))
+                             copy_valid, _stream(stream, q.device))
     _check(st, "prefill_step")
     return out
 

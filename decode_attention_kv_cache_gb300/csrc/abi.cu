@@ -161,18 +161,19 @@ int prefill_chunk_attn(const kvc_cache *cache, int32_t layer, int32_t pos0, int3
 
 int prefill_step(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens, const void *q, const void *k,
                  const void *v, int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
-                 kvc_stream_t stream) {
+                 int32_t copy_valid, kvc_stream_t stream) {
     if (!cache_ok(cache) || !dtype_ok(dtype)) return KVC_EINVAL;
     if (cache->d.head_dim != 64 && cache->d.head_dim != 128) return KVC_EINVAL;
     if (n_head_q <= 0 || n_head_q % cache->d.n_head_kv || n_head_q > 65535 || n_tokens < 0) return KVC_EINVAL;
-    if (layer < 0 || layer >= cache->d.n_layer || pos0 < 0 || (int64_t)pos0 + n_tokens > cache->d.n_ctx)
+    if (layer < 0 || layer >= cache->d.n_layer || pos0 < 0 || (int64_t)pos0 + n_tokens > cache->d.n_ctx ||
+        copy_valid < 0 || copy_valid > pos0)
         return KVC_ERANGE;
     if (n_tokens == 0) return KVC_OK;
     if (!q || !k || !v || !out || !scratch || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
         !aligned16(scratch))
         return KVC_EINVAL;
     return launch_prefill_step(*cache, layer, pos0, n_tokens, q, k, v, dtype, n_head_q, out, scratch, scratch_bytes,
-                               (cudaStream_t)stream);
+                               copy_valid, (cudaStream_t)stream);
 }
 
 int decode_attn(const kvc_cache *cache, int32_t layer, int32_t pos, const void *q, int32_t dtype,

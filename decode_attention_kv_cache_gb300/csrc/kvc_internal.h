@@ -55,7 +55,7 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
                    int n_head_q, float *out, void *scratch, size_t scratch_bytes, cudaStream_t s);
 int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, const void *k,
                         const void *v, int dtype, int n_head_q, float *out, void *scratch, size_t scratch_bytes,
-                        cudaStream_t s);
+                        int copy_valid, cudaStream_t s);
 int decode_max_split();
 int launch_decode(const kvc_cache &c, int layer, int pos, const void *q, int dtype, int n_head_q,
                   float *out, float *scratch, cudaStream_t s);

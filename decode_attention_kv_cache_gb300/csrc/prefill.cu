@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const Args a) {
 }
 
 // ---- q8_0: the attended keys and values dequantised once per call --------------------------
-// fp16(d * q) of positions [0, kv_len) of one layer, K (grid.y 0) then V (1), each as [H][kv_len][D]:
+// fp16(d * q) of positions [0, kv_len) of one layer, K (grid.y 0) then V (1), each as [H][n_ctx][D]:
 // the very values the in-kernel dequantiser writes into the operand tiles (same op, same rounding),
 // so the attention pass then runs as for an f16 cache and gives the same bits.  A thread converts 8
 // values (8 code bytes and their block's scale) into 16 bytes.  Launched normally after the append, so
@@ -783,7 +783,8 @@ __global__ void __launch_bounds__(256) dequant_range_kernel(const int8_t *__rest
                                                             const uint16_t *__restrict__ ks,
                                                             const int8_t *__restrict__ vq,
                                                             const uint16_t *__restrict__ vs, Geom g, int layer,
-                                                            int kv_len, int64_t n_units, __half *dk, __half *dv) {
+                                                            int kv_len, int n_ctx, int64_t n_units, __half *dk,
+                                                            __half *dv) {
     asm volatile("griddepcontrol.launch_dependents;");
     const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (u >= n_units) return;
@@ -800,7 +801,8 @@ __global__ void __launch_bounds__(256) dequant_range_kernel(const int8_t *__rest
     uint32_t o[4];
     dequant4(w.x, d2, o[0], o[1]);
     dequant4(w.y, d2, o[2], o[3]);
-    *reinterpret_cast<uint4 *>((is_v ? dv : dk) + row * D + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>((is_v ? dv : dk) + ((int64_t)h * n_ctx + t) * D + 8 * c) =
+        make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ---- the fused step's first kernel --------------------------------------------------------
@@ -808,16 +810,18 @@ struct FrontArgs {
     const void *k, *v;     // the chunk's rows, [C][H][D] in the input dtype
     void *kq, *vq;         // the cache's codes (q8_0) or values (f16)
     uint16_t *ks, *vs;     // its scales (q8_0)
-    __half *dk, *dv;       // COPY: the fp16 copy, [H][kv_len][D] each
+    __half *dk, *dv;       // COPY: the fp16 copy, [H][n_ctx][D] each
     Geom g;
-    int layer, pos0, H, kv_len;
+    int layer, pos0, H, n_ctx;
+    int dq0;               // COPY: the first position converted from the cache (the copy holds [0, dq0))
     int64_t n_dq, n_app;
 };
 
 // Stores the chunk's K and V at positions [pos0, pos0 + C) exactly as the append kernel does (q8_0
-// blocks by the shared quantiser, f16 values rounded to nearest even).  With COPY (q8_0 with the full scratch) it also writes the fp16 copy of positions
-// [0, pos0 + C) that the attention pass reads: the chunk's from the codes it has just made, the earlier
-// positions dequantised from the cache as dequant_range_kernel does (the same values either way).
+// blocks by the shared quantiser, f16 values rounded to nearest even).  With COPY (q8_0 with the full
+// scratch) it also completes the fp16 copy of positions [0, pos0 + C) that the attention pass reads: the
+// chunk's from the codes it has just made, positions [dq0, pos0) dequantised from the cache as
+// dequant_range_kernel does (the same values either way); [0, dq0) are already there.
 // grid.y: K (0) or V (1).  Along x: first n_dq units of 8 earlier values (COPY only), then n_app units
 // of the chunk (a 32-value block for q8_0, 8 values for f16).  A programmatic dependent launch: nothing
 // global is read or written before griddepcontrol.wait (the previous call's attention pass may still be
@@ -831,9 +835,10 @@ __global__ void __launch_bounds__(256) prefill_front_kernel(const FrontArgs f) {
     const Geom &g = f.g;
     if (COPY && u < f.n_dq) {
         constexpr int UPR = D / 8;                   // 8-value units per head row
-        const int64_t row = u / UPR;                 // (head, position) over [0, pos0)
+        const int64_t row = u / UPR;                 // (head, position) over [dq0, pos0)
         const int c = (int)(u - row * UPR);
-        const int h = (int)(row / f.pos0), t = (int)(row - (int64_t)h * f.pos0);
+        const int nrow = f.pos0 - f.dq0;             // > 0 here: n_dq is zero otherwise
+        const int h = (int)(row / nrow), t = f.dq0 + (int)(row - (int64_t)h * nrow);
         const int64_t src = f.layer * g.c_layer + (int64_t)t * g.c_tok + h * g.c_head + 8 * c;
         const uint2 w = __ldcg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(is_v ? f.vq : f.kq) + src));
         const uint16_t sb = __ldcg((is_v ? f.vs : f.ks) + f.layer * g.s_layer + (int64_t)t * g.s_tok + h * g.s_head + c / 4);
@@ -841,7 +846,7 @@ __global__ void __launch_bounds__(256) prefill_front_kernel(const FrontArgs f) {
         uint32_t o[4];
         dequant4(w.x, d2, o[0], o[1]);
         dequant4(w.y, d2, o[2], o[3]);
-        *reinterpret_cast<uint4 *>((is_v ? f.dv : f.dk) + ((int64_t)h * f.kv_len + t) * D + 8 * c) =
+        *reinterpret_cast<uint4 *>((is_v ? f.dv : f.dk) + ((int64_t)h * f.n_ctx + t) * D + 8 * c) =
             make_uint4(o[0], o[1], o[2], o[3]);
         return;
     }
@@ -874,7 +879,7 @@ __global__ void __launch_bounds__(256) prefill_front_kernel(const FrontArgs f) {
             uint32_t o[16];
 #pragma unroll
             for (int w = 0; w < 8; ++w) dequant4(packed[w], d2, o[2 * w], o[2 * w + 1]);
-            uint4 *cp = reinterpret_cast<uint4 *>((is_v ? f.dv : f.dk) + ((int64_t)h * f.kv_len + pos) * D + b * 32);
+            uint4 *cp = reinterpret_cast<uint4 *>((is_v ? f.dv : f.dk) + ((int64_t)h * f.n_ctx + pos) * D + b * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) cp[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
@@ -1102,17 +1107,17 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
                                                            static_cast<const uint16_t *>(c.k_s),
                                                            static_cast<const int8_t *>(c.v_q),
                                                            static_cast<const uint16_t *>(c.v_s), g, layer, kv_len,
-                                                           n_units, dk, dv);
+                                                           c.d.n_ctx, n_units, dk, dv);
         else
             dequant_range_kernel<64><<<grid, 256, 0, s>>>(static_cast<const int8_t *>(c.k_q),
                                                           static_cast<const uint16_t *>(c.k_s),
                                                           static_cast<const int8_t *>(c.v_q),
                                                           static_cast<const uint16_t *>(c.v_s), g, layer, kv_len,
-                                                          n_units, dk, dv);
+                                                          c.d.n_ctx, n_units, dk, dv);
         kvc_cache f = {};
         f.d = c.d;
         f.d.n_layer = 1;
-        f.d.n_ctx = kv_len;
+        f.d.n_ctx = c.d.n_ctx;
         f.d.type = KVC_F16;
         f.d.layout = KVC_HEAD_MAJOR;
         f.k_q = dk;
@@ -1130,7 +1135,7 @@ int launch_prefill(const kvc_cache &c, int layer, int pos0, int n_tokens, const 
 
 int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, const void *q, const void *k,
                         const void *v, int dtype, int n_head_q, float *out, void *scratch, size_t scratch_bytes,
-                        cudaStream_t s) {
+                        int copy_valid, cudaStream_t s) {
     if (n_tokens == 0) return KVC_OK;
     Plan p;
     if (!make_plan(c.d, n_head_q, pos0, n_tokens, p)) return KVC_EINVAL;
@@ -1138,7 +1143,7 @@ int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, c
     const bool q8 = c.d.type == KVC_Q8_0;
     const size_t copy_bytes = dequant_copy_bytes(c.d);
     const bool copy = q8 && scratch_bytes >= copy_bytes + scratch_need(p);
-    const int kv_len = pos0 + n_tokens, H = c.d.n_head_kv, D = c.d.head_dim;
+    const int H = c.d.n_head_kv, D = c.d.head_dim;
     uint8_t *part = static_cast<uint8_t *>(scratch) + (copy ? copy_bytes : 0);
     FrontArgs f;
     f.k = k;
@@ -1153,8 +1158,9 @@ int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, c
     f.layer = layer;
     f.pos0 = pos0;
     f.H = H;
-    f.kv_len = kv_len;
-    f.n_dq = copy ? (int64_t)H * pos0 * (D / 8) : 0;
+    f.n_ctx = c.d.n_ctx;
+    f.dq0 = copy ? copy_valid : 0;
+    f.n_dq = copy ? (int64_t)H * (pos0 - f.dq0) * (D / 8) : 0;
     f.n_app = (int64_t)n_tokens * H * (q8 ? D / 32 : D / 8);
     // the chunk stored (and, with the copy, the attended range in fp16), then the attention and the merge
     const int rc = launch_front(f, D, q8, copy, dtype, s);
@@ -1163,7 +1169,7 @@ int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, c
         kvc_cache fc = {};
         fc.d = c.d;
         fc.d.n_layer = 1;
-        fc.d.n_ctx = kv_len;
+        fc.d.n_ctx = c.d.n_ctx;
         fc.d.type = KVC_F16;
         fc.d.layout = KVC_HEAD_MAJOR;
         fc.k_q = f.dk;

@@ -165,8 +165,10 @@ int kv_cache_append_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer,
  * chunks of up to max_tokens rows anywhere in this cache: the float32 partial
  * results (output row, running max, sum) of the key splits, at least 256 bytes,
  * and for a q8_0 cache in front of them room for an fp16 copy of one layer's
- * keys and values (2 * n_head_kv * n_ctx * head_dim * 2 bytes).  The contents
- * need no initialisation; every call writes what it reads. */
+ * keys and values (2 * n_head_kv * n_ctx * head_dim * 2 bytes, laid out
+ * [K|V][head][position][head_dim]).  The contents need no initialisation:
+ * every call writes what it reads, except the part of the copy that
+ * prefill_step's copy_valid says is already there. */
 int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t max_tokens, size_t *bytes);
 
 /* Causal attention of a chunk's query rows over the cache:
@@ -180,8 +182,8 @@ int kvc_prefill_scratch_bytes(const kvc_desc *desc, int32_t n_head_q, int32_t ma
  * prompt is cut into chunks.  Computed with fp16 tensor-core products and
  * float32 accumulation and softmax.  A q8_0 cache's keys and values enter the
  * products as fp16(d * q): with the full scratch of kvc_prefill_scratch_bytes,
- * positions [0, pos0 + n_tokens) are first dequantised once into the scratch
- * (one more kernel), and the attention reads that copy; with a scratch that
+ * positions [0, pos0 + n_tokens) are first dequantised once into the scratch's
+ * copy (one more kernel), and the attention reads that copy; with a scratch that
  * holds only the partials, the attention kernel dequantises each tile in
  * shared memory instead (slower: once per 128-row query tile).  Both give the
  * same bits.
@@ -205,16 +207,26 @@ int prefill_chunk_attn(const kvc_cache *cache, int32_t layer, int32_t pos0, int3
  * layer split's pipeline", "Summary").  q: [n_tokens][n_head_q][head_dim], k and
  * v: [n_tokens][n_head_kv][head_dim], device memory in `dtype`, 16-byte
  * aligned; out float32.  Kernels: the first stores the chunk (for q8_0 with
- * the full scratch it also writes the fp16 copy of positions [0, pos0 +
+ * the full scratch it also completes the fp16 copy of positions [0, pos0 +
  * n_tokens) that the attention reads, so no separate dequantising pass runs),
  * then the attention and, when rows span several key splits, the merge - two
  * launches, or three with the merge, where the separate calls take three or
- * four.  scratch: as for prefill_chunk_attn (kvc_prefill_scratch_bytes, no
- * initialisation).  Errors as prefill_chunk_attn, and KVC_EINVAL for a null or
- * unaligned k or v. */
+ * four.  scratch: as for prefill_chunk_attn (kvc_prefill_scratch_bytes).
+ * copy_valid (0 <= copy_valid <= pos0): how many leading positions of the
+ * scratch's fp16 copy already hold this layer's values, left there by earlier
+ * calls of prefill_step or prefill_chunk_attn with this scratch on this cache
+ * and layer, the cache's positions [0, copy_valid) unchanged since.  The call
+ * converts [copy_valid, pos0) from the cache and the chunk from the codes it
+ * stores, so a prompt processed chunk after chunk on one scratch with
+ * copy_valid = pos0 converts each position once (an fp16 copy per layer when
+ * chunks go through all layers in turn).  0 for a fresh scratch; a
+ * copy_valid that overstates the copy gives wrong outputs, not an error.
+ * Ignored for an f16 cache and for a scratch without the copy.
+ * Errors as prefill_chunk_attn, KVC_EINVAL for a null or unaligned k or v,
+ * KVC_ERANGE for copy_valid outside [0, pos0]. */
 int prefill_step(const kvc_cache *cache, int32_t layer, int32_t pos0, int32_t n_tokens, const void *q, const void *k,
                  const void *v, int32_t dtype, int32_t n_head_q, float *out, void *scratch, size_t scratch_bytes,
-                 kvc_stream_t stream);
+                 int32_t copy_valid, kvc_stream_t stream);
 
 /* Single-token decode attention at position pos: the formula above with one
  * query row at pos, keys [0, pos].  The token's K/V must have been appended.

@@ -112,13 +112,16 @@ def test_hot_path_checks_run_before_any_launch(kvc):
     assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 0, 5, k, 1, 4, k, k, 16, S) == kvc.KVC_ENOSPC
     assert kvc.lib.prefill_chunk_attn(ctypes.byref(c), 0, 3, 0, None, 1, 4, None, None, 0, S) == kvc.KVC_OK
     # the fused prefill step: prefill_chunk_attn's checks plus k and v
-    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 60, 5, k, k, k, 1, 4, k, k, 1 << 30, S) == kvc.KVC_ERANGE
-    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, None, k, 1, 4, k, k, 1 << 30, S) == kvc.KVC_EINVAL
-    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, k, ctypes.c_void_p(0x40004), 1, 4, k, k, 1 << 30, S) == \
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 60, 5, k, k, k, 1, 4, k, k, 1 << 30, 0, S) == kvc.KVC_ERANGE
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, None, k, 1, 4, k, k, 1 << 30, 0, S) == kvc.KVC_EINVAL
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, k, ctypes.c_void_p(0x40004), 1, 4, k, k, 1 << 30, 0, S) == \
         kvc.KVC_EINVAL
-    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, k, k, 1, 3, k, k, 1 << 30, S) == kvc.KVC_EINVAL
-    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, k, k, 1, 4, k, k, 16, S) == kvc.KVC_ENOSPC
-    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 3, 0, None, None, None, 1, 4, None, None, 0, S) == kvc.KVC_OK
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, k, k, 1, 3, k, k, 1 << 30, 0, S) == kvc.KVC_EINVAL
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 0, 5, k, k, k, 1, 4, k, k, 16, 0, S) == kvc.KVC_ENOSPC
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 3, 0, None, None, None, 1, 4, None, None, 0, 0, S) == kvc.KVC_OK
+    # copy_valid within [0, pos0]
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 8, 5, k, k, k, 1, 4, k, k, 1 << 30, 9, S) == kvc.KVC_ERANGE
+    assert kvc.lib.prefill_step(ctypes.byref(c), 0, 8, 5, k, k, k, 1, 4, k, k, 1 << 30, -1, S) == kvc.KVC_ERANGE
     assert kvc.lib.decode_attn(ctypes.byref(c), 0, 64, k, 1, 4, k, k, 1 << 20, S) == kvc.KVC_ERANGE
     assert kvc.lib.decode_attn(ctypes.byref(c), 0, 5, k, 1, 4, k, k, 100, S) == kvc.KVC_ENOSPC
     assert kvc.lib.decode_attn(ctypes.byref(c), 0, 5, k, 1, 36, k, k, 1 << 24, S) == kvc.KVC_EINVAL  # G = 18 > 16

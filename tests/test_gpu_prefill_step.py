@@ -136,3 +136,89 @@ def test_step_chunk_ending_at_the_cache_end(kvc, cache):
     kh, vh = o.dequantized(0, n_ctx)
     from oracle.attention import attend
     assert_close(ob[rows].cpu().numpy(), attend(np32(q[rows]), rows, kh, vh), "rows at the end")
+
+
+def chunked_steps(kvc, g, layer, qkv, chunks, scratch, out, valid):
+    """The prompt's chunks through prefill_step; valid(pos0) gives each call's copy_valid."""
+    q, k, v = qkv
+    for p, c in chunks:
+        kvc.prefill_step(g, layer, p, q[p:p + c], k[p:p + c], v[p:p + c], out=out[p:p + c], scratch=scratch,
+                         copy_valid=valid(p))
+
+
+@pytest.mark.parametrize("d,dt", [(128, "bf16"), (64, "f32")])
+def test_incremental_copy_equals_the_full_copy(kvc, d, dt):
+    # a q8_0 prompt whose chunks each convert only their own positions (copy_valid = pos0), or the
+    # positions from part-way back, against calls that convert the whole prefix: the same bits; the
+    # scratch starts as fp16 NaNs, so a position of the copy that no call wrote would show
+    w = si.small_workload("pinc", 10, 2, d, "q8_0", dt, n_prompt=9000, chunk=1500, n_decode=0, seed=71 + d,
+                          k_outlier_frac=0.01)
+    qkv = tuple(t.cuda() for t in si.layer_qkv(w, 0))
+    chunks = w.chunks(1500)
+    outs, caches = [], []
+    for valid in (lambda p: 0, lambda p: p, lambda p: max(0, p - 700)):
+        g = kvc.KVCache(1, w.n_ctx, w.n_head_kv, d, "q8_0", "head_major")
+        s = g.prefill_scratch(w.n_head_q, 1500).fill_(0xFF)
+        o = torch.empty(w.n_prompt, w.n_head_q, d, device="cuda")
+        chunked_steps(kvc, g, 0, qkv, chunks, s, o, valid)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status() == 0
+        outs.append(o)
+        caches.append(g)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert not torch.isnan(outs[1]).any()
+    n = w.n_prompt
+    for g in caches[1:]:
+        for kv in (0, 1):
+            assert torch.equal(g.codes(kv)[:, 0, :n], caches[0].codes(kv)[:, 0, :n])
+            assert torch.equal(g.scales(kv)[:, 0, :n].view(torch.int16), caches[0].scales(kv)[:, 0, :n].view(torch.int16))
+
+
+def test_incremental_copy_per_layer_with_chunks_through_all_layers(kvc):
+    # the model's order: each chunk through every layer before the next chunk, one scratch (one fp16
+    # copy) per layer; equals the same order converting the whole prefix every call
+    L, n, chunk = 3, 5000, 1024
+    w = si.small_workload("pincl", 8, 2, 128, "q8_0", "f16", n_prompt=n, chunk=chunk, n_decode=0, seed=81,
+                          n_layer=L)
+    qkv = [tuple(t.cuda() for t in si.layer_qkv(w, layer)) for layer in range(L)]
+    res = []
+    for incremental in (False, True):
+        g = kvc.KVCache(L, w.n_ctx, w.n_head_kv, 128, "q8_0", "layer_major")
+        scr = [g.prefill_scratch(w.n_head_q, chunk).fill_(0xFF) for _ in range(L)]
+        outs = [torch.empty(n, w.n_head_q, 128, device="cuda") for _ in range(L)]
+        for p, c in w.chunks(chunk):
+            for layer in range(L):
+                q, k, v = qkv[layer]
+                kvc.prefill_step(g, layer, p, q[p:p + c], k[p:p + c], v[p:p + c], out=outs[layer][p:p + c],
+                                 scratch=scr[layer], copy_valid=p if incremental else 0)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status() == 0
+        res.append(outs)
+    for layer in range(L):
+        assert torch.equal(res[0][layer], res[1][layer]), "layer %d" % layer
+    o = OracleCache(1, w.n_ctx, w.n_head_kv, 128, "q8_0")
+    q, k, v = qkv[2]
+    o.append(0, 0, np32(k[:n].cpu()), np32(v[:n].cpu()))
+    rows = np.array([0, 1023, 1024, 3000, 4999])
+    kh, vh = o.dequantized(0, n)
+    from oracle.attention import attend
+    assert_close(res[1][2][rows].cpu().numpy(), attend(np32(q[rows].cpu()), rows, kh, vh), "layer 2 rows")
+
+
+def test_copy_left_by_prefill_chunk_attn(kvc):
+    # prefill_chunk_attn's dequantising pass leaves the copy in the same layout: a following prefill_step
+    # may take it as valid
+    w = si.small_workload("pinca", 10, 2, 128, "q8_0", "bf16", n_prompt=4000, chunk=2000, n_decode=0, seed=91)
+    q, k, v = (t.cuda() for t in si.layer_qkv(w, 0))
+    ga = kvc.KVCache(1, w.n_ctx, 2, 128, "q8_0", "head_major")
+    gb = kvc.KVCache(1, w.n_ctx, 2, 128, "q8_0", "head_major")
+    sa = ga.prefill_scratch(10, 2000).fill_(0xFF)
+    sb = gb.prefill_scratch(10, 2000)
+    kvc.kv_cache_append(ga, 0, 0, k[:2000], v[:2000])
+    kvc.prefill_chunk_attn(ga, 0, 0, q[:2000], scratch=sa)
+    a = kvc.prefill_step(ga, 0, 2000, q[2000:], k[2000:], v[2000:], scratch=sa, copy_valid=2000)
+    kvc.prefill_step(gb, 0, 0, q[:2000], k[:2000], v[:2000], scratch=sb)
+    b = kvc.prefill_step(gb, 0, 2000, q[2000:], k[2000:], v[2000:], scratch=sb)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    assert torch.equal(a, b)
