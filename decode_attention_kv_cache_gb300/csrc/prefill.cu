@@ -12,8 +12,10 @@
 // Work decomposition.  A unit is 128 query rows of one query head.  Keys are
 // taken in tiles of 256 and cut at ABSOLUTE split boundaries of ST tiles (ST
 // is fixed by the cache size): an item is (unit, split).  Persistent CTAs (one
-// per SM) take items round-robin, split-major and kv-group-major so that the
-// CTAs running at one time read the same K/V tiles.  An item whose unit has
+// per SM) take items in split-major, kv-group-major order, so that the CTAs
+// running at one time read the same K/V tiles: round-robin, or (prefill_step)
+// the next item in that order whenever a CTA is free, from a counter in the
+// scratch that the step's first kernel zeroes.  An item whose unit has
 // one split writes the output directly; otherwise it writes its partial (O,
 // running max, sum), and a second, fully parallel kernel merges each row's
 // partials in split order.  Because tiles and splits sit at absolute
@@ -117,12 +119,18 @@ struct Cfg {
     static constexpr int SM_REGS = 176;                     // each softmax warpgroup
     static_assert(128 * WG0_REGS + 256 * SM_REGS + (Q8 ? 128 * DQ_REGS : 0) <= THREADS * LAUNCH_REGS,
                   "register split exceeds the launch allocation");
+    static_assert(NS <= 6 && NR <= 4, "more ring stages than barriers");
+    // warps that read each item index: the MMA issuer, the two Q warps, eight softmax warps, (q8_0) four
+    // dequantising warps
+    static constexpr int ITEM_READERS = Q8 ? 15 : 11;
 };
 
+constexpr int NIT = 4;            // slots of the item ring (item indices from the producer to the other roles)
 enum Bar {
     B_QFULL, B_QREADY, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN, B_STALL,
-    B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 8, B_RAW_FULL = B_RING_EMPTY + 8,
-    B_RAW_EMPTY = B_RAW_FULL + 8, NBAR = B_RAW_EMPTY + 8
+    B_RING_FULL, B_RING_EMPTY = B_RING_FULL + 6, B_RAW_FULL = B_RING_EMPTY + 6,
+    B_RAW_EMPTY = B_RAW_FULL + 4, B_ITEM_FULL = B_RAW_EMPTY + 4, B_ITEM_EMPTY = B_ITEM_FULL + NIT,
+    NBAR = B_ITEM_EMPTY + NIT
 };
 
 struct Args {
@@ -131,6 +139,8 @@ struct Args {
     const uint16_t *vs;
     float *out;
     float *part;      // partials [q-tile][head][split][row][PART_ROW]
+    unsigned *item_counter;  // null: CTA b takes items b, b + grid, ...; else items come from this counter,
+                             // which the kernel before this one on the stream set to zero
     Geom g;
     int layer, pos0, C, kv_len, H_q, G, H_kv, n_qt, ST, smax, n_items;
     int v8;                    // out and part are 32-byte aligned: rows are stored 32 bytes at a time
@@ -247,8 +257,9 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    volatile int *s_item = reinterpret_cast<volatile int *>(s_tmem + 2);
     volatile uint32_t *s_mb = reinterpret_cast<volatile uint32_t *>(sm + L::OFF_RED);
-    static_assert(NBAR * 8 + 8 <= 384, "barrier area too small");
+    static_assert(NBAR * 8 + 8 + 4 * NIT <= 384, "barrier area too small");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -273,6 +284,10 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             mbar_init(&bars[B_RAW_FULL + s], 1);
             mbar_init(&bars[B_RAW_EMPTY + s], 128);
         }
+        for (int s = 0; s < NIT; ++s) {
+            mbar_init(&bars[B_ITEM_FULL + s], 1);
+            mbar_init(&bars[B_ITEM_EMPTY + s], L::ITEM_READERS);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -284,6 +299,23 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int first_item = blockIdx.x, stride = gridDim.x;
+    // The CTA's items, in order: the producer takes each index (the next value of the item counter, or
+    // the next of blockIdx.x + n * gridDim.x) and passes it through a ring of NIT slots; every other role
+    // reads the same sequence.  An index of n_items ends it.  A reader frees its slot as soon as it has
+    // read the index, so the producer is never held by a role that waits for the producer's earlier data.
+    auto take_item = [&](uint32_t &seq, bool whole_warp) -> int {
+        const int slot = seq % NIT;
+        if (!mbar_wait(&bars[B_ITEM_FULL + slot], (seq / NIT) & 1, s_abort)) return -1;
+        const int i = s_item[slot];
+        ++seq;
+        if (whole_warp) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[B_ITEM_EMPTY + slot]);
+        } else {
+            mbar_arrive(&bars[B_ITEM_EMPTY + slot]);
+        }
+        return i;
+    };
     // launched as a programmatic dependent of the kernel before it on the stream (normally the append
     // of this chunk's keys): the set-up above overlapped that kernel's tail, and everything global
     // (the cache, Q, the outputs) is read and written only past this wait.  The merge pass may be
@@ -324,7 +356,16 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 }
                 return true;
             };
-            for (int i = first_item; ok && i < a.n_items; i += stride) {
+            for (uint32_t item_seq = 0; ok; ++item_seq) {
+                const int slot = item_seq % NIT;
+                if (item_seq >= NIT &&
+                    !mbar_wait(&bars[B_ITEM_EMPTY + slot], ((item_seq / NIT) - 1) & 1, s_abort))
+                    break;
+                int i = a.item_counter ? (int)atomicAdd(a.item_counter, 1u) : first_item + (int)item_seq * stride;
+                if (i > a.n_items) i = a.n_items;
+                s_item[slot] = i;
+                mbar_arrive(&bars[B_ITEM_FULL + slot]);
+                if (i == a.n_items) break;
                 const Item it = decode_item(a, i);
                 if (q_seq > 0 && !mbar_wait(&bars[B_QEMPTY], (q_seq - 1) & 1, s_abort)) break;
                 if (QDT != KVC_IN_F32) {
@@ -401,7 +442,9 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
                 KVC_PTR(5, p_seq - 1);
                 return true;
             };
-            for (int i = first_item; ok && i < a.n_items; i += stride) {
+            for (uint32_t item_seq = 0; ok;) {
+                const int i = take_item(item_seq, false);
+                if (i < 0 || i >= a.n_items) break;
                 const Item it = decode_item(a, i);
                 if (!mbar_wait(&bars[B_QREADY], q_seq & 1, s_abort)) break;
                 ++q_seq;
@@ -445,7 +488,9 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
         constexpr int RPI = 32 / CPR;          // rows per warp and iteration
         const int cc = lane % CPR, r_off = (warp - 2) * RPI + lane / CPR;
         uint32_t q_seq = 0;
-        for (int i = first_item; i < a.n_items; i += stride) {
+        for (uint32_t item_seq = 0;;) {
+            const int i = take_item(item_seq, true);
+            if (i < 0 || i >= a.n_items) break;
             const Item it = decode_item(a, i);
             if (!mbar_wait(&bars[B_QFULL], q_seq & 1, s_abort)) break;
             ++q_seq;
@@ -517,7 +562,9 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             ++mb_n;
             return true;
         };
-        for (int i = first_item; ok && i < a.n_items; i += stride) {
+        for (uint32_t item_seq = 0; ok;) {
+            const int i = take_item(item_seq, true);
+            if (i < 0 || i >= a.n_items) break;
             const Item it = decode_item(a, i);
             const int row = it.qt * BM + r;       // row within the chunk
             const int t = it.tf + r;              // absolute position
@@ -729,7 +776,9 @@ __global__ void __launch_bounds__(Cfg<D, Q8>::THREADS, 1)
             ++ring_seq;
             return true;
         };
-        for (int i = first_item; ok && i < a.n_items; i += stride) {
+        for (uint32_t item_seq = 0; ok;) {
+            const int i = take_item(item_seq, true);
+            if (i < 0 || i >= a.n_items) break;
             const Item it = decode_item(a, i);
             ok = convert(0, it.k0, it.g);
             for (int k = it.k0; ok && k < it.k1; ++k) {
@@ -815,6 +864,7 @@ struct FrontArgs {
     int layer, pos0, H, n_ctx;
     int dq0;               // COPY: the first position converted from the cache (the copy holds [0, dq0))
     int64_t n_dq, n_app;
+    unsigned *item_counter;  // the attention pass's item counter, set to zero here
 };
 
 // Stores the chunk's K and V at positions [pos0, pos0 + C) exactly as the append kernel does (q8_0
@@ -830,6 +880,9 @@ template <int D, bool Q8, int DT, bool COPY>
 __global__ void __launch_bounds__(256) prefill_front_kernel(const FrontArgs f) {
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the previous call's attention pass has completed (its merge pass waited for it): no CTA still takes
+    // items from the counter
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *f.item_counter = 0u;
     const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const bool is_v = blockIdx.y != 0;
     const Geom &g = f.g;
@@ -939,12 +992,16 @@ bool make_plan(const kvc_desc &d, int n_head_q, int pos0, int C, Plan &p) {
     return true;
 }
 
-// the documented scratch size: the partials, at least 256 bytes
-size_t scratch_need(const Plan &p) { return p.part_bytes > 256 ? p.part_bytes : 256; }
+// The partials' part of the scratch: a 256-byte header (word 0: prefill_step's item counter), then the
+// partials.
+constexpr size_t PART_HDR = 256;
+size_t scratch_need(const Plan &p) { return PART_HDR + p.part_bytes; }
 
+// scratch: the partials' part of the scratch (header, then partials); counter: null for the static item
+// order, else the header's item counter, zeroed by the kernel before this one on the stream.
 template <int D, bool Q8, int QDT>
 int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int n_head_q, float *out,
-             void *scratch, const Plan &p, cudaStream_t s) {
+             void *scratch, const Plan &p, cudaStream_t s, unsigned *counter) {
     using L = Cfg<D, Q8>;
     const Geom g = geom_of(c.d);
     const int H = c.d.n_head_kv, kv_len = pos0 + n;
@@ -978,8 +1035,9 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
     a.ks = static_cast<const uint16_t *>(c.k_s);
     a.vs = static_cast<const uint16_t *>(c.v_s);
     a.out = out;
-    a.part = static_cast<float *>(scratch);
-    a.v8 = ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(scratch)) & 31) == 0;
+    a.part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + PART_HDR);
+    a.item_counter = counter;
+    a.v8 = ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(a.part)) & 31) == 0;
     a.g = g;
     a.layer = layer;
     a.pos0 = pos0;
@@ -1028,11 +1086,14 @@ int launch_t(const kvc_cache &c, int layer, int pos0, int n, const void *q, int 
 
 template <int D, bool Q8>
 int launch_d(const kvc_cache &c, int layer, int pos0, int n, const void *q, int dtype, int n_head_q,
-             float *out, void *scratch, const Plan &p, cudaStream_t s) {
+             float *out, void *scratch, const Plan &p, cudaStream_t s, unsigned *counter = nullptr) {
     switch (dtype) {
-        case KVC_IN_F32: return launch_t<D, Q8, KVC_IN_F32>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s);
-        case KVC_IN_BF16: return launch_t<D, Q8, KVC_IN_BF16>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s);
-        default: return launch_t<D, Q8, KVC_IN_F16>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s);
+        case KVC_IN_F32:
+            return launch_t<D, Q8, KVC_IN_F32>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s, counter);
+        case KVC_IN_BF16:
+            return launch_t<D, Q8, KVC_IN_BF16>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s, counter);
+        default:
+            return launch_t<D, Q8, KVC_IN_F16>(c, layer, pos0, n, q, n_head_q, out, scratch, p, s, counter);
     }
 }
 
@@ -1162,9 +1223,13 @@ int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, c
     f.dq0 = copy ? copy_valid : 0;
     f.n_dq = copy ? (int64_t)H * (pos0 - f.dq0) * (D / 8) : 0;
     f.n_app = (int64_t)n_tokens * H * (q8 ? D / 32 : D / 8);
+    f.item_counter = reinterpret_cast<unsigned *>(part);
     // the chunk stored (and, with the copy, the attended range in fp16), then the attention and the merge
     const int rc = launch_front(f, D, q8, copy, dtype, s);
     if (rc != KVC_OK) return rc;
+    // the attention pass takes its items from the counter the front kernel has just zeroed: a CTA that
+    // finishes early takes the next item in order, and the order keeps concurrent CTAs on the same tiles
+    unsigned *ctr = f.item_counter;
     if (copy) {
         kvc_cache fc = {};
         fc.d = c.d;
@@ -1174,14 +1239,14 @@ int launch_prefill_step(const kvc_cache &c, int layer, int pos0, int n_tokens, c
         fc.d.layout = KVC_HEAD_MAJOR;
         fc.k_q = f.dk;
         fc.v_q = f.dv;
-        return D == 128 ? launch_d<128, false>(fc, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s)
-                        : launch_d<64, false>(fc, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s);
+        return D == 128 ? launch_d<128, false>(fc, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s, ctr)
+                        : launch_d<64, false>(fc, 0, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s, ctr);
     }
     if (D == 128)
-        return q8 ? launch_d<128, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s)
-                  : launch_d<128, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s);
-    return q8 ? launch_d<64, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s)
-              : launch_d<64, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s);
+        return q8 ? launch_d<128, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s, ctr)
+                  : launch_d<128, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s, ctr);
+    return q8 ? launch_d<64, true>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s, ctr)
+              : launch_d<64, false>(c, layer, pos0, n_tokens, q, dtype, n_head_q, out, part, p, s, ctr);
 }
 
 int read_and_clear_device_status(int32_t *status) {

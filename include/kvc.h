@@ -162,9 +162,10 @@ int kv_cache_append_batch(const kvc_cache *caches, int32_t n_seq, int32_t layer,
                           const void *v, int32_t dtype, kvc_stream_t stream);
 
 /* Bytes of the scratch buffer prefill_chunk_attn and prefill_step need for
- * chunks of up to max_tokens rows anywhere in this cache: the float32 partial
- * results (output row, running max, sum) of the key splits, at least 256 bytes,
- * and for a q8_0 cache in front of them room for an fp16 copy of one layer's
+ * chunks of up to max_tokens rows anywhere in this cache: a 256-byte header
+ * (prefill_step's work counter) and the float32 partial results (output row,
+ * running max, sum) of the key splits, and for a q8_0 cache in front of them
+ * room for an fp16 copy of one layer's
  * keys and values (2 * n_head_kv * n_ctx * head_dim * 2 bytes, laid out
  * [K|V][head][position][head_dim]).  The contents need no initialisation:
  * every call writes what it reads, except the part of the copy that

@@ -108,5 +108,28 @@ def test_prefill_wait_that_gives_up_then_next_call_is_correct(kvc, cache_type):
     assert kvc.kvc_device_status() == 0
 
 
+@pytest.mark.parametrize("cache_type", ["q8_0", "f16"])
+def test_prefill_step_wait_that_gives_up_then_next_call_is_correct(kvc, cache_type):
+    # the fused step takes its attention items from a counter: after the aborted call the next one (the
+    # same chunk again, then the next chunk, on the same scratch) is correct
+    w, q, g, o = _filled(kvc, cache_type, 3000)
+    _, k, v = si.layer_qkv(w, 0)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    c = 1000
+    scratch = g.prefill_scratch(w.n_head_q, c)
+    kvc.prefill_step(g, 0, 0, qd[:c], kd[:c], vd[:c], scratch=scratch)
+    kvc.arm_test_wait_timeout(kvc.TEST_PREFILL, LIMIT_NS)
+    kvc.prefill_step(g, 0, c, qd[c:2 * c], kd[c:2 * c], vd[c:2 * c], scratch=scratch, copy_valid=c)
+    rc, status = _status_code(kvc)
+    assert rc == kvc.KVC_EDEVICE and status != 0, (rc, status)
+    rows = [0, 1, 127, 128, 511, 998, 999]
+    for p0 in (c, 2 * c):
+        out = kvc.prefill_step(g, 0, p0, qd[p0:p0 + c], kd[p0:p0 + c], vd[p0:p0 + c], scratch=scratch,
+                               copy_valid=p0)
+        ref = o.prefill_chunk(0, p0, np32(q[p0:p0 + c]), rows=rows)
+        assert_close(out.cpu().numpy()[rows], ref, "prefill_step after the abort, pos0 %d" % p0)
+    assert kvc.kvc_device_status() == 0
+
+
 def test_arm_rejects_an_unknown_kernel(kvc):
     assert kvc.lib.kvc_test_arm_wait_timeout(7, LIMIT_NS) == kvc.KVC_EINVAL
