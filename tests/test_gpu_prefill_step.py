@@ -222,3 +222,33 @@ def test_copy_left_by_prefill_chunk_attn(kvc):
     torch.cuda.synchronize()
     assert kvc.kvc_device_status() == 0
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("cache", ["q8_0", "f16"])
+def test_prompt_captured_in_a_cuda_graph(kvc, cache):
+    # a whole prompt's prefill_step calls captured once and replayed: each replay's front kernels zero
+    # the item counter again, and the outputs equal the eager calls' bit for bit
+    w = si.small_workload("pgraph", 10, 2, 128, cache, "bf16", n_prompt=6000, chunk=1500, n_decode=0, seed=97)
+    q, k, v = (t.cuda() for t in si.layer_qkv(w, 0))
+    g = kvc.KVCache(1, w.n_ctx, 2, 128, cache, "head_major")
+    s = g.prefill_scratch(10, 1500)
+    eager = torch.empty(w.n_prompt, 10, 128, device="cuda")
+    graph_out = torch.empty_like(eager)
+
+    def prompt(out):
+        for p, c in w.chunks(1500):
+            kvc.prefill_step(g, 0, p, q[p:p + c], k[p:p + c], v[p:p + c], out=out[p:p + c], scratch=s, copy_valid=p)
+
+    prompt(eager)
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            prompt(graph_out)
+    for _ in range(2):
+        graph_out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(graph_out, eager)
+    assert kvc.kvc_device_status() == 0
