@@ -20,6 +20,7 @@ Multi-GPU (torchrun): every rank runs an independent replica (weak scaling).
 """
 
 import argparse
+import gc
 import json
 import os
 import subprocess
@@ -388,6 +389,10 @@ def run_gpu(args, rank, world, local):
     clocks.start()
     dist_barrier(world)
     torch.cuda.synchronize()
+    # no garbage-collector pass on the host while it issues the timed steps (a pass that stalls the host
+    # mid-step leaves the GPU idle inside the step's events)
+    gc.collect()
+    gc.disable()
     torch.cuda.nvtx.range_push("kvc_timed")
     for _ in range(args.steps):
         l2_flush(torch, flush)
@@ -409,6 +414,7 @@ def run_gpu(args, rank, world, local):
         b = torch.cuda.Event(enable_timing=True); b.record()
         chain.append((a, b))
     torch.cuda.synchronize()
+    gc.enable()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in steps]
     total_ms = dist_max(sum(step_ms), world)
@@ -473,7 +479,12 @@ def run_gpu(args, rank, world, local):
     }
     if w.n_layer == 1:
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        line["kernels"] = kernel_rooflines(kvc, torch, w, req, flush, max(10, K), hbm, peak_src)
+        gc.collect()
+        gc.disable()
+        try:
+            line["kernels"] = kernel_rooflines(kvc, torch, w, req, flush, max(10, K), hbm, peak_src)
+        finally:
+            gc.enable()
     if w.chunk_sweep:
         line["chunk_sweep"] = chunk_sweep(kvc, torch, w, req, device, flush, max(3, K))
     if args.npl:
@@ -677,7 +688,13 @@ def end_to_end(kvc, torch, w, req, device, rank, world, K, flush, local=0):
     dist_barrier(world)
     clocks = ClockSampler(local)
     clocks.start()
-    e_total = dist_max(run(K), world)
+    gc.collect()
+    gc.disable()
+    try:
+        e_ms = run(K)
+    finally:
+        gc.enable()
+    e_total = dist_max(e_ms, world)
     clk = clocks.stop()
     return {"value": tokens * world * K / (e_total / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e_total / K, "clocks": clk,
