@@ -221,22 +221,43 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
 // partial starts at `base` (split s at base + s * sstride).
 template <int D>
 __device__ __forceinline__ float4 merge_row4(const float *base, int64_t sstride, int ns, int c4) {
-    float M = -INFINITY;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride + D));
-    float Lsum = 0.f;
+    float M = -INFINITY, Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-        const float *ps = base + s * sstride;
-        const float ms = __ldcg(ps + D), ls = __ldcg(ps + D + 1);
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(ps + c4));
+    auto add = [&](float ms, float ls, float4 v) {
         const float w = (ms == -INFINITY) ? 0.f : (ms == M ? 1.f : ex2(ms - M));
         Lsum = fmaf(w, ls, Lsum);
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
         acc.w = fmaf(w, v.w, acc.w);
+    };
+    constexpr int MS = 8;   // up to MS splits: every load is issued before the first use (one round trip)
+    if (ns <= MS) {
+        float2 ml[MS];
+        float4 v[MS];
+#pragma unroll
+        for (int s = 0; s < MS; ++s) {
+            ml[s] = make_float2(-INFINITY, 0.f);
+            v[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < ns) {
+                ml[s] = __ldcg(reinterpret_cast<const float2 *>(base + s * sstride + D));
+                v[s] = __ldcg(reinterpret_cast<const float4 *>(base + s * sstride + c4));
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < MS; ++s)
+            if (s < ns) M = fmaxf(M, ml[s].x);
+#pragma unroll
+        for (int s = 0; s < MS; ++s)
+            if (s < ns) add(ml[s].x, ml[s].y, v[s]);
+    } else {
+#pragma unroll 4
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride + D));
+#pragma unroll 4
+        for (int s = 0; s < ns; ++s) {
+            const float *ps = base + s * sstride;
+            add(__ldcg(ps + D), __ldcg(ps + D + 1), __ldcg(reinterpret_cast<const float4 *>(ps + c4)));
+        }
     }
     const float inv_l = 1.f / Lsum;
     return make_float4(acc.x * inv_l, acc.y * inv_l, acc.z * inv_l, acc.w * inv_l);
