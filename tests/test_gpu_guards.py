@@ -110,3 +110,41 @@ def test_guard_check_sees_a_changed_byte(cuda_device):
         assert x.intact()
         x.buf[where:where + 1] ^= 1
         assert not x.intact()
+
+
+@pytest.mark.parametrize("cache", ["q8_0", "f16"])
+def test_batched_calls_stay_inside(kvc, cache):
+    # three sequences of different lengths in guarded caches of both layouts: batched appends and
+    # decode steps, the last sequence up to its cache's last position
+    hq, hkv, d, n_ctx = 10, 2, 128, 400
+    lengths = [390, 120, 7]
+    ws = [si.small_workload("gb%d" % i, hq, hkv, d, cache, "bf16", n_prompt=n, chunk=n, n_decode=n_ctx - n,
+                            seed=90 + i, n_ctx=n_ctx) for i, n in enumerate(lengths)]
+    qkv = [tuple(t.cuda() for t in si.layer_qkv(w, 0)) for w in ws]
+    guards = []
+    caches = [guarded_cache(kvc, guards, 1, n_ctx, hkv, d, cache, ("head_major", "layer_major")[i % 2], seed=40 + 4 * i)
+              for i in range(3)]
+    pscr = Guarded(caches[0].prefill_scratch_bytes(hq, max(lengths)), 51)
+    guards.append(pscr)
+    for g, (q, k, v), n in zip(caches, qkv, lengths):
+        kvc.prefill_step(g, 0, 0, q[:n], k[:n], v[:n], scratch=pscr.inner)
+    per = caches[0].scratch_bytes(hq)
+    bscr = Guarded(3 * per, 52)
+    out = Guarded(3 * hq * d * 4, 53)
+    guards += [bscr, out]
+    o = out.as_f32((3, hq, d))
+    for t in range(n_ctx - max(lengths)):
+        pos = [n + t for n in lengths]
+        qb = torch.stack([q[p] for (q, _, _), p in zip(qkv, pos)])
+        kb = torch.stack([k[p] for (_, k, _), p in zip(qkv, pos)])
+        vb = torch.stack([v[p] for (_, _, v), p in zip(qkv, pos)])
+        if t % 2 == 0:
+            kvc.decode_step_batch(caches, 0, pos, qb, kb, vb, out=o, scratch=bscr.inner)
+        else:
+            kvc.kv_cache_append_batch(caches, 0, pos, kb, vb)
+            kvc.decode_attn_batch(caches, 0, pos, qb, out=o, scratch=bscr.inner)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    assert torch.isfinite(o).all()
+    bad = [i for i, x in enumerate(guards) if not x.intact()]
+    assert not bad, "guard bytes changed around buffers %s" % bad
