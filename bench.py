@@ -67,8 +67,8 @@ def prefill_flops(w, chunks=None):
 # Entries: kernel -> {"sources": {file: sha16}, workload: (bytes per call, what was captured)}.
 TRAFFIC = {
     # the step's 29 prefill_step calls (the front kernel, the attention, the split merge), mean per call
-    "prefill": {"sources": {"prefill.cu": "05415fd9ff5d703c", "quant.cuh": "b2cae791609f3353"},
-                "q8_0_58k": (416667665, "mean per call over the 29 prefill_step calls of one step (all three kernels)")},
+    "prefill": {"sources": {"prefill.cu": "9b2cbe58ac7ea91d", "quant.cuh": "b2cae791609f3353"},
+                "q8_0_58k": (415433030, "mean per call over the 29 prefill_step calls of one step (all three kernels)")},
     "append_chunk": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},
                      "q8_0_58k": (8412364, "one 2048-token chunk append (writes still in L2 at the launch end)")},
     "append_prompt": {"sources": {"append.cu": "2302d1cd16863358", "quant.cuh": "b2cae791609f3353"},

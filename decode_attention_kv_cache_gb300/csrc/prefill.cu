@@ -159,7 +159,8 @@ __device__ __forceinline__ int unit_tl(const Args &a, int qt) {
     return a.pos0 + min(qt * BM + BM, a.C) - 1;
 }
 
-// Items are ordered by split, then kv group, then q-tile, then head within the group.
+// Items are ordered by split, then kv group, then q-tile (last first: the later q-tiles reach further
+// into the split, so the shorter items come last in each group), then head within the group.
 __device__ __forceinline__ Item decode_item(const Args &a, int i) {
     Item it;
     int s = 0;
@@ -168,7 +169,7 @@ __device__ __forceinline__ Item decode_item(const Args &a, int i) {
     const int per_g = (a.n_qt - a.qtmin[s]) * a.G;
     it.g = r / per_g;
     const int rem = r - it.g * per_g;
-    it.qt = a.qtmin[s] + rem / a.G;
+    it.qt = a.n_qt - 1 - rem / a.G;
     it.h = it.g * a.G + rem % a.G;
     it.s = s;
     it.tf = a.pos0 + it.qt * BM;
