@@ -212,7 +212,11 @@ int prefill_chunk_attn(const kvc_cache *cache, int32_t layer, int32_t pos0, int3
  * n_tokens) that the attention reads, so no separate dequantising pass runs),
  * then the attention and, when rows span several key splits, the merge - two
  * launches, or three with the merge, where the separate calls take three or
- * four.  scratch: as for prefill_chunk_attn (kvc_prefill_scratch_bytes).
+ * four.  The attention's CTAs take their work items in order from a counter
+ * in the scratch header, which the first kernel sets to zero; the result does
+ * not depend on which CTA takes which item.  scratch: as for
+ * prefill_chunk_attn (kvc_prefill_scratch_bytes); calls on one scratch buffer
+ * must not overlap on the GPU.
  * copy_valid (0 <= copy_valid <= pos0): how many leading positions of the
  * scratch's fp16 copy already hold this layer's values, left there by earlier
  * calls of prefill_step or prefill_chunk_attn with this scratch on this cache
